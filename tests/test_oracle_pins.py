@@ -1,0 +1,367 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each test checks the oracle against a closed form, an invariant of the
+mathematics, a brute-force computation written independently here, a library
+routine (torch's float8 / bfloat16 conversions), or a number printed on the
+pages (tests/golden/page_numbers.json).  Chosen so that a dropped term (RoPE
+columns), a wrong operand (V columns, transposes), a wrong index (page/offset,
+causal end, scale block) or a wrong sign fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_decode_attention_gb300 import roofline, workloads
+from tests._util import bf16_np
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_numbers.json")))
+SCALE = 1.0 / math.sqrt(192.0)
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# ----------------------------------------------------------------- formats
+
+def test_bf16_widening_matches_torch():
+    bits = rng(1).integers(0, 1 << 16, size=20000, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.bf16_bits_to_f64(bits)
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def test_e4m3_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_to_f64(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def test_e4m3_closed_values():
+    v = oracle.e4m3_to_f64(np.array([0x7E, 0x01, 0x08, 0x38, 0xB8, 0x00, 0x80], dtype=np.uint8))
+    assert v[0] == GOLDEN["e4m3_max"]["value"] == 448.0
+    assert v[1] == 2.0 ** -9          # smallest subnormal
+    assert v[2] == 2.0 ** -6          # smallest normal
+    assert v[3] == 1.0 and v[4] == -1.0
+    assert v[5] == 0.0 and v[6] == 0.0
+    assert np.isnan(oracle.e4m3_to_f64(np.array([0x7F], dtype=np.uint8)))[0]
+
+
+def test_fp8_token_layout_offsets():
+    """Byte offsets 0 / 512 / 528 and the c // 128 scale block, built by hand."""
+    tok = np.zeros(656, dtype=np.uint8)
+    tok[0:512] = 0x38                                     # every code = 1.0
+    scales = np.array([2.0, 3.0, 5.0, 7.0], dtype="<f4")
+    tok[512:528] = scales.view(np.uint8)
+    rope = torch.arange(64, dtype=torch.float32).to(torch.bfloat16)
+    tok[528:656] = rope.view(torch.int16).numpy().view(np.uint8)
+    x = oracle.fp8_tokens_to_f64(tok[None])[0]
+    assert x.shape == (576,)
+    for blk in range(4):
+        assert np.all(x[blk * 128:(blk + 1) * 128] == scales[blk])
+    assert np.array_equal(x[512:], np.arange(64, dtype=np.float64))
+    parts = GOLDEN["fp8_token_bytes"]["parts"]
+    assert sum(parts) == GOLDEN["fp8_token_bytes"]["value"] == oracle.FP8_TOKEN_BYTES == 656
+
+
+def test_fp8_quantise_decode_error_bound():
+    """Input encoder + oracle decoder: e4m3 round-to-nearest bound per element.
+
+    |x - decode(encode(x))| <= 2^-4 |x| (half an ulp of a 3-bit mantissa) for
+    normal codes, <= 2^-10 * scale for subnormal ones; RoPE round-trips bf16.
+    """
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(32, 576, generator=g)
+    x[:, 128:256] *= 50.0
+    x[:, 256:384] *= 0.001
+    raw = workloads.quantize_fp8_tokens(x).numpy()
+    assert raw.shape == (32, 656)
+    dec = oracle.fp8_tokens_to_f64(raw)
+    xs = x.to(torch.float64).numpy()
+    scales = raw[:, 512:528].copy().view("<f4").astype(np.float64)
+    for blk in range(4):
+        sl = slice(blk * 128, (blk + 1) * 128)
+        amax = np.abs(xs[:, sl]).max(axis=1)
+        assert np.allclose(scales[:, blk], (amax.astype(np.float32) / np.float32(448.0)), rtol=0, atol=0)
+        err = np.abs(dec[:, sl] - xs[:, sl])
+        bound = np.maximum(2.0 ** -4 * np.abs(xs[:, sl]), 2.0 ** -10 * scales[:, blk:blk + 1]) * (1 + 1e-6)
+        assert np.all(err <= bound + 1e-12)
+    rope_ref = x[:, 512:].to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(dec[:, 512:], rope_ref)
+
+
+def test_fp8_representable_roundtrip_exact():
+    """Values already on the e4m3 grid times a power-of-two scale survive."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = oracle.e4m3_to_f64(codes)
+    x = np.zeros((1, 576))
+    x[0, :512] = np.resize(vals, 512)
+    for blk in range(4):          # block absmax = 448 -> scale exactly 1
+        x[0, blk * 128] = 448.0
+    raw = workloads.quantize_fp8_tokens(torch.from_numpy(x).to(torch.float32)).numpy()
+    dec = oracle.fp8_tokens_to_f64(raw)
+    assert np.array_equal(dec[0, :512], x[0, :512])
+
+
+# ----------------------------------------------------------- attention core
+
+def test_single_key_returns_its_value_row():
+    q = rng(2).standard_normal((5, 576))
+    k = rng(3).standard_normal((1, 576))
+    out, lse = oracle.attend(q, k, SCALE)
+    assert np.array_equal(out, np.repeat(k[:, :512], 5, axis=0))
+    assert np.allclose(lse, SCALE * (q @ k[0]), rtol=0, atol=1e-14)
+
+
+def test_equal_scores_give_mean_of_values():
+    keys = rng(4).standard_normal((37, 576))
+    out, lse = oracle.attend(np.zeros((3, 576)), keys, SCALE)
+    assert np.allclose(out, keys[:, :512].mean(axis=0)[None], rtol=0, atol=1e-13)
+    assert np.allclose(lse, math.log(37), rtol=0, atol=1e-13)
+
+
+def test_two_keys_closed_form():
+    """Scores chosen through one coordinate; weights from math.exp by hand."""
+    q = np.zeros((1, 576)); q[0, 3] = 1.0
+    keys = np.zeros((2, 576))
+    keys[0, 3], keys[1, 3] = 2.0, -1.5
+    keys[0, :3] = [1.0, 2.0, 3.0]
+    keys[1, :3] = [-4.0, 0.5, 8.0]
+    a, b = SCALE * 2.0, SCALE * -1.5
+    wa = math.exp(a) / (math.exp(a) + math.exp(b))
+    wb = 1.0 - wa
+    out, lse = oracle.attend(q, keys, SCALE)
+    expect = wa * keys[0, :512] + wb * keys[1, :512]
+    assert np.allclose(out[0], expect, rtol=0, atol=1e-14)
+    assert abs(lse[0] - math.log(math.exp(a) + math.exp(b))) < 1e-14
+
+
+def test_rope_columns_score_but_are_not_values():
+    """Columns 512..575 enter the score only; the output has 512 columns."""
+    q = np.zeros((1, 576)); q[0, 512:] = 1.0
+    keys = np.zeros((2, 576))
+    keys[0, 512:] = 0.2            # rope dot = 12.8
+    keys[1, 512:] = -0.2
+    keys[0, :512] = 1.0
+    keys[1, :512] = -1.0
+    out, lse = oracle.attend(q, keys, 1.0)
+    w0 = 1.0 / (1.0 + math.exp(-25.6))
+    assert out.shape == (1, 512)
+    assert np.allclose(out[0], w0 * 1.0 + (1 - w0) * -1.0, atol=1e-14)
+    assert abs(lse[0] - math.log(math.exp(12.8) + math.exp(-12.8))) < 1e-12
+
+
+def _naive_rows(q_rows, keys, scale):
+    """Three-pass softmax attention with plain Python loops (no BLAS)."""
+    outs, lses = [], []
+    for q in q_rows.tolist():
+        s = [scale * sum(a * b for a, b in zip(q, k)) for k in keys.tolist()]
+        m = max(s)
+        e = [math.exp(v - m) for v in s]
+        z = sum(e)
+        o = [0.0] * 512
+        for w, k in zip(e, keys.tolist()):
+            for d in range(512):
+                o[d] += w * k[d]
+        outs.append([v / z for v in o])
+        lses.append(m + math.log(z))
+    return np.array(outs), np.array(lses)
+
+
+def test_brute_force_tiny():
+    q = rng(5).standard_normal((3, 576)) * 2
+    keys = rng(6).standard_normal((7, 576))
+    out, lse = oracle.attend(q, keys, SCALE)
+    ref_o, ref_l = _naive_rows(q, keys, SCALE)
+    assert np.allclose(out, ref_o, rtol=0, atol=1e-12)
+    assert np.allclose(lse, ref_l, rtol=0, atol=1e-12)
+
+
+def test_online_recurrence_equals_definition():
+    q = rng(7).standard_normal((1, 576)) * 3
+    keys = rng(8).standard_normal((300, 576))
+    o1, l1 = oracle.attend(q, keys, SCALE)
+    o2, l2 = oracle.attend_online(q[0], keys, SCALE)
+    assert np.allclose(o1[0], o2, rtol=0, atol=1e-12)
+    assert abs(l1[0] - l2) < 1e-12
+
+
+def test_combine_of_splits_equals_unsplit():
+    q = rng(9).standard_normal((4, 576))
+    keys = rng(10).standard_normal((250, 576))
+    cuts = [0, 0, 17, 130, 250]            # includes an empty split
+    parts = [oracle.attend(q, keys[a:b], SCALE) for a, b in zip(cuts[:-1], cuts[1:])]
+    o, l = oracle.combine(parts)
+    o_ref, l_ref = oracle.attend(q, keys, SCALE)
+    assert np.allclose(o, o_ref, rtol=0, atol=1e-12)
+    assert np.allclose(l, l_ref, rtol=0, atol=1e-12)
+
+
+def test_absorption_identity():
+    """Per-head attention with expanded K/V equals absorbed MQA on the latent.
+
+    score_h(t) = q_C,h . (W_UK,h c_t) + q_R,h . k_R,t
+               = (W_UK,h^T q_C,h) . c_t + q_R,h . k_R,t
+    o_h = sum_t p_h(t) W_UV,h c_t = W_UV,h (sum_t p_h(t) c_t)
+    """
+    r = rng(11)
+    H, dh, T = 3, 16, 9
+    W_UK = r.standard_normal((H, dh, 512)) / 20
+    W_UV = r.standard_normal((H, dh, 512)) / 20
+    c = r.standard_normal((T, 512))
+    k_R = r.standard_normal((T, 64))
+    q_C = r.standard_normal((H, dh))
+    q_R = r.standard_normal((H, 64))
+    for h in range(H):
+        k_full = np.concatenate([c @ W_UK[h].T, k_R], axis=1)          # [T, dh+64]
+        v_full = c @ W_UV[h].T                                          # [T, dh]
+        s = SCALE * (k_full @ np.concatenate([q_C[h], q_R[h]]))
+        p = np.exp(s - s.max()); p /= p.sum()
+        o_expanded = p @ v_full
+        q_abs = np.concatenate([W_UK[h].T @ q_C[h], q_R[h]])[None]      # [1, 576]
+        keys = np.concatenate([c, k_R], axis=1)                         # [T, 576]
+        lat, lse = oracle.attend(q_abs, keys, SCALE)
+        o_absorbed = W_UV[h] @ lat[0]
+        assert np.allclose(o_absorbed, o_expanded, rtol=1e-12, atol=1e-13)
+        assert abs(lse[0] - (s.max() + math.log(np.exp(s - s.max()).sum()))) < 1e-12
+
+
+# ------------------------------------------------------------------ gathers
+
+def _id_cache(n_pages):
+    """Cache whose column 0 holds the flat physical row id (page*64 + slot)."""
+    kv = np.zeros((n_pages, 64, 576))
+    kv[:, :, 0] = np.arange(n_pages * 64).reshape(n_pages, 64)
+    return kv
+
+
+def test_paged_gather_follows_block_table():
+    perm = rng(12).permutation(16)
+    bt = perm[:10].reshape(2, 5)
+    kv = _id_cache(16)
+    keys = oracle.paged_keys(kv, bt[1], 300)
+    t = np.arange(300)
+    assert np.array_equal(keys[:, 0], bt[1][t // 64] * 64 + t % 64)
+
+
+def test_dense_single_token_rows_copy_their_page_row():
+    """seqlen 1: out is the V row of block_table[b, 0] slot 0, bit for bit."""
+    kv = rng(13).standard_normal((8, 64, 576))
+    bt = np.array([[5, 1], [2, 7], [0, 3]])
+    q = rng(14).standard_normal((3, 1, 4, 576))
+    out, lse = oracle.dense_decode(q, kv, bt, np.array([1, 1, 1]), SCALE)
+    for b in range(3):
+        assert np.array_equal(out[b, 0], np.repeat(kv[bt[b, 0], 0, :512][None], 4, axis=0))
+
+
+def test_causal_end_alignment():
+    """s_q = 2 causal: token j sees L - 2 + j + 1 keys (bottom-right)."""
+    kv = rng(15).standard_normal((12, 64, 576))
+    bt = rng(16).permutation(12).reshape(2, 6)
+    L = np.array([300, 129])
+    q = rng(17).standard_normal((2, 2, 3, 576))
+    out, lse = oracle.dense_decode(q, kv, bt, L, SCALE, causal=True)
+    for b in range(2):
+        for j in range(2):
+            o1, l1 = oracle.dense_decode(q[b:b + 1, j:j + 1], kv, bt[b:b + 1],
+                                         np.array([L[b] - 1 + j]), SCALE)
+            assert np.array_equal(out[b, j], o1[0, 0])
+            assert np.array_equal(lse[b, :, j], l1[0, :, 0])
+    # and the two tokens really differ by the last key
+    assert not np.allclose(out[0, 0], out[0, 1])
+
+
+def test_sparse_index_order_invariance():
+    pool = rng(18).standard_normal((500, 576))
+    idx = rng(19).permutation(500)[:64].reshape(1, 1, 64)
+    idx[0, 0, [5, 40]] = -1
+    q = rng(20).standard_normal((1, 1, 8, 576))
+    o1, l1 = oracle.sparse_decode(q, pool, idx, SCALE)
+    for s in range(3):
+        perm = rng(21 + s).permutation(64)
+        o2, l2 = oracle.sparse_decode(q, pool, idx[:, :, perm], SCALE)
+        assert np.allclose(o1, o2, rtol=0, atol=1e-12)
+        assert np.allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+def test_sparse_invalid_and_out_of_range_are_skipped():
+    pool = rng(22).standard_normal((100, 576))
+    q = rng(23).standard_normal((1, 1, 2, 576))
+    good = np.array([3, 50, 99, 0, 17])
+    idx = np.array([3, -1, 50, 100, 99, 0, -7, 17, 1 << 30]).reshape(1, 1, -1)
+    o1, l1 = oracle.sparse_decode(q, pool, idx, SCALE)
+    o2, l2 = oracle.sparse_decode(q, pool, good.reshape(1, 1, -1), SCALE)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_dense_equals_sparse_over_all_rows_of_the_request():
+    kv = rng(24).standard_normal((10, 64, 576))
+    bt = rng(25).permutation(10).reshape(2, 5)
+    L = np.array([260, 70])
+    q = rng(26).standard_normal((2, 1, 4, 576))
+    od, ld = oracle.dense_decode(q, kv, bt, L, SCALE)
+    pool = kv.reshape(-1, 576)
+    for b in range(2):
+        t = np.arange(L[b])
+        idx = (bt[b][t // 64] * 64 + t % 64).reshape(1, 1, -1)
+        os_, ls_ = oracle.sparse_decode(q[b:b + 1], pool, idx, SCALE)
+        assert np.allclose(os_[0], od[b], rtol=0, atol=1e-12)
+        assert np.allclose(ls_[0], ld[b], rtol=0, atol=1e-12)
+
+
+def test_empty_key_sets():
+    q = rng(27).standard_normal((2, 2, 3, 576))
+    kv = rng(28).standard_normal((4, 64, 576))
+    bt = np.array([[0, 1], [2, 3]])
+    out, lse = oracle.dense_decode(q, kv, bt, np.array([0, 1]), SCALE)
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert np.all(out[1, 0] == 0) and np.all(np.isneginf(lse[1, :, 0]))   # L - s_q + 1 + 0 = 0
+    assert np.array_equal(out[1, 1], np.repeat(kv[2, 0, :512][None], 3, axis=0))
+    idx = -np.ones((1, 1, 8), dtype=np.int64)
+    o, l = oracle.sparse_decode(q[:1, :1], kv.reshape(-1, 576), idx, SCALE)
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+
+
+def test_bf16_bits_input_equals_float_input():
+    g = torch.Generator().manual_seed(3)
+    qt = torch.randn(1, 1, 4, 576, generator=g).to(torch.bfloat16)
+    kt = torch.randn(3, 64, 576, generator=g).to(torch.bfloat16)
+    bt = np.array([[2, 0, 1]])
+    a = oracle.dense_decode(bf16_np(qt), bf16_np(kt), bt, np.array([150]), SCALE)
+    b = oracle.dense_decode(qt.double().numpy(), kt.double().numpy(), bt, np.array([150]), SCALE)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------ numbers on the pages
+
+def test_page_numbers_dimensions_and_token_bytes():
+    assert GOLDEN["d_qk"]["value"] == oracle.D_QK == workloads.D_QK == 512 + 64
+    assert GOLDEN["d_v"]["value"] == oracle.D_V == workloads.D_V
+    assert GOLDEN["bf16_token_bytes"]["value"] == roofline.BF16_TOKEN_BYTES
+    t = GOLDEN["kv_bytes_128k_request"]["terms"]
+    n = t["d"] * t["bytes"] * t["layers"] * t["tokens"]
+    assert n == GOLDEN["kv_bytes_128k_request"]["value"]
+    assert round(n / 2 ** 30, 2) == GOLDEN["kv_bytes_128k_request"]["gib"]
+
+
+def test_page_numbers_cost_model():
+    c = GOLDEN["ai_dsv3_decode"]["config"]
+    fl = roofline.mla_analysis_flops(c["b"], c["h"], c["s"], c["t"], c["k"], c["p"])
+    by = roofline.mla_analysis_bytes(c["b"], c["h"], c["s"], c["t"], c["k"], c["p"], c["w"])
+    assert round(fl / by) == GOLDEN["ai_dsv3_decode"]["value"]
+    # our accounting adds LSE, page-table and length words: still ~228
+    f2, b2, kv = roofline.dense_counts([c["t"]] * c["b"], 1, c["h"])
+    assert f2 == fl
+    assert round(f2 / b2) == GOLDEN["ai_dsv3_decode"]["value"]
+    assert roofline.FLOP_PER_PAIR == GOLDEN["flops_per_token_per_row"]["value"]
+    g = GOLDEN["mma_cycles_per_token_64_heads_h800"]
+    assert round(64 * (576 + 512) * 2 / g["flop_per_clk_per_sm"]) == g["value"]
