@@ -1,0 +1,196 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * The operation: Multi-head Latent Attention decode over an absorbed, paged
+ * latent KV cache.  After weight absorption decode is MQA: h_q query heads
+ * share ONE key head whose rows are 576 wide (512 latent + 64 RoPE), and V is
+ * the first 512 columns of the same cached row (FlashMLA deep dive,
+ * "Theoretical Analysis of the MLA Algorithm"; DeepGEMM & FlashMLA article,
+ * section 6 "MLA", absorption).  For every query row (request b, new token j,
+ * head h):
+ *
+ *     s_t  = softmax_scale * <q[b,j,h,:], K[t,:]>          (t in the key set)
+ *     out  = sum_t exp(s_t - lse) * K[t, 0:512]            (bf16)
+ *     lse  = ln sum_t exp(s_t)                              (fp32)
+ *
+ * computed as split-KV online softmax plus an LSE combine (DeepGEMM & FlashMLA
+ * article, section 7 "split-KV" merge formula; FlashMLA deep dive, "tile
+ * scheduler" and "programmatic dependent launch").  Calling convention
+ * follows the FlashMLA README "Usage": schedule metadata once per shape, then
+ * one decode call per step.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE memory owned by the caller.  The library
+ *    never allocates, frees or synchronises; every launch goes on `stream`.
+ *  - Return value: MLA_OK (0) or a negative MLA_ERR_* code.  Errors are
+ *    detected on the host before any launch (nothing is launched then).
+ *  - `err` (optional, may be NULL): a device uint32 word the kernels OR
+ *    MLA_DEVERR_* bits into (bad page id, bad index, bounded-wait timeout).
+ *    The caller zeroes it and reads it back when it wants to.  Bad ids never
+ *    fault: the row they name is masked out.
+ *  - Row layouts (all contiguous, C order):
+ *      q      [batch, s_q, h_q, 576] bf16
+ *      out    [batch, s_q, h_q, 512] bf16
+ *      lse    [batch, h_q, s_q]      fp32   (transposed w.r.t. out, as in the
+ *                                            FlashMLA README "Return Values")
+ *  - Supported shapes: d_qk = 576, d_v = 512, page block 64 tokens,
+ *    h_q in {16, 32, 48, 64, 128}, 1 <= s_q <= 16.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+#define MLA_OK 0
+#define MLA_ERR_NULL (-1)        /* a required pointer is NULL                 */
+#define MLA_ERR_SHAPE (-2)       /* unsupported or inconsistent size argument  */
+#define MLA_ERR_ALIGN (-3)       /* pointer or stride not 16-byte aligned      */
+#define MLA_ERR_METADATA (-4)    /* metadata built for another shape/part count */
+#define MLA_ERR_CUDA (-5)        /* a CUDA runtime call failed                 */
+#define MLA_ERR_UNSUPPORTED (-6) /* device is not sm_103/sm_100 class          */
+
+/* ------------------------------------------------ device error word (err) */
+#define MLA_DEVERR_BAD_PAGE 1u   /* block_table entry outside [0, num_pages)  */
+#define MLA_DEVERR_BAD_INDEX 2u  /* sparse index < -1 or >= s_kv              */
+#define MLA_DEVERR_TIMEOUT 4u    /* an internal wait ran out (kernel bailed)  */
+
+/* -------------------------------------------------------- KV cache formats */
+#define MLA_KV_BF16 0    /* [num_pages, 64, 576] bf16, 1152 B per token        */
+#define MLA_KV_FP8_656 1 /* [num_pages, 64, 656] bytes per token: 512 e4m3      *
+                          * codes, 4 fp32 scales (one per 128 latent channels),  *
+                          * 64 bf16 RoPE values (FlashMLA "Hopper FP8 sparse     *
+                          * decode" note, "The FP8 KVCache Format")              */
+
+/* Human-readable name of a status code. Never NULL. */
+const char* mla_status_string(int status);
+
+/* Description of the last MLA_ERR_CUDA (or other recorded failure) raised on
+ * the calling host thread: the failing call and the CUDA error text.  Never
+ * NULL; the buffer is thread-local and overwritten by the next failure. */
+const char* mla_last_error(void);
+
+/*
+ * Number of work parts the kernels spread over the device: one part per
+ * group of ceil(h_q / 64) SMs (a part is one thread-block cluster; each
+ * block of the cluster owns 64 query heads).  Writes *num_sm_parts.
+ */
+int mla_num_sm_parts(int device, int h_q, int* num_sm_parts);
+
+/*
+ * Size in bytes of the schedule metadata for n_seq = batch * s_q query
+ * sequences split over num_sm_parts parts.
+ */
+int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes);
+
+/*
+ * Split-KV tile schedule (FlashMLA deep dive, "Tile Scheduler"; DeepGEMM &
+ * FlashMLA article, section 7: computed once, reused by every layer and step
+ * while shapes stay the same).  A device kernel on `stream` reads the
+ * lengths and writes the int32 metadata; there is no host synchronisation.
+ *
+ * Each (request b, new token j) is one sequence whose key count is
+ *   dense, causal:      max(0, cache_seqlens[b] - s_q + 1 + j)
+ *   dense, non-causal:  cache_seqlens[b]
+ *   sparse (topk > 0):  topk   (cache_seqlens ignored, may be NULL)
+ * Sequences are cut into 128-key tiles and the tiles are dealt out as
+ * contiguous ranges of balanced cost (tiles + 1 per sequence piece) to the
+ * parts; a sequence cut between parts becomes several splits that the
+ * combine step merges.  Layout of `metadata` (int32):
+ *   [0,16)                    header: magic 0x4D4C4131, version, n_seq,
+ *                             num_sm_parts, tile_tokens (128), s_q, batch,
+ *                             causal, topk, total_splits, cost_per_part, 0...
+ *   [16, 16 + 8 * parts)      per part: q_begin, t_begin, q_end, t_end,
+ *                             split_begin, 0, 0, 0 (half-open range of
+ *                             (sequence, tile) pairs in lexicographic order)
+ *   [.., + 8 * n_seq)         per sequence: n_tiles, split_offset, n_splits,
+ *                             key count, cost prefix, 0, 0, 0
+ * metadata: device buffer of mla_metadata_size() bytes, 16-byte aligned.
+ */
+int mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int causal, int topk,
+                     int num_sm_parts, void* metadata, cudaStream_t stream);
+
+/*
+ * The same schedule computed on the host from host lengths into a host
+ * buffer (identical bytes to mla_get_metadata).  For callers that already
+ * hold the lengths on the host, and for testing the device schedule.
+ */
+int mla_get_metadata_host(const int32_t* cache_seqlens_host, int batch, int s_q, int causal,
+                          int topk, int num_sm_parts, void* metadata_host);
+
+/*
+ * Size in bytes of the fp32 split workspace: partial outputs
+ * [batch*s_q + num_sm_parts, h_q, 512] followed by partial LSEs
+ * [batch*s_q + num_sm_parts, h_q].
+ */
+int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts, size_t* bytes);
+
+/*
+ * Dense paged decode (FlashMLA README "Usage": flash_mla_with_kvcache with
+ * q, kvcache, block_table, cache_seqlens).  Runs the split-KV kernel and then
+ * the combine kernel (programmatic dependent launch) on `stream`.
+ *
+ *  q            [batch, s_q, h_q, 576] bf16
+ *  kv_cache     MLA_KV_BF16: [num_pages, 64, 576] bf16;
+ *               MLA_KV_FP8_656: [num_pages, 64, 656] uint8
+ *  block_table  [batch, block_table_stride] int32; entry [b, p] = physical
+ *               page of tokens 64p .. 64p+63 of request b.  Only the first
+ *               ceil(cache_seqlens[b] / 64) entries of a row are read.
+ *  cache_seqlens [batch] int32, cached tokens per request (new tokens
+ *               included).  With causal != 0 and s_q > 1, new token j sees
+ *               keys 0 .. cache_seqlens[b] - s_q + j.
+ *  Cache slots past a request's length inside its last page must hold
+ *  finite values (they are masked, but multiply a zero weight).
+ *  metadata     from mla_get_metadata(cache_seqlens, batch, s_q, causal, 0,
+ *               num_sm_parts, ...) on the same lengths.
+ *  workspace    mla_workspace_size() bytes, 16-byte aligned.
+ *  out, lse     outputs as described at the top of this file.  A query row
+ *               with no visible key gets out = 0, lse = -inf.
+ */
+int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
+               const int32_t* block_table, int64_t block_table_stride,
+               const int32_t* cache_seqlens, int batch, int s_q, int h_q, float softmax_scale,
+               int causal, const void* metadata, int num_sm_parts, void* workspace, void* out,
+               float* lse, uint32_t* err, cudaStream_t stream);
+
+/*
+ * DSA top-k sparse decode (FlashMLA README, "indices Tensor"): each query
+ * token attends only to the pool rows its index list names.
+ *
+ *  kv       [s_kv, 576] bf16 pool of latent rows (a paged cache viewed flat:
+ *           row = page * 64 + offset)
+ *  indices  [batch, s_q, topk] int32; -1 marks an invalid slot.  Any other
+ *           value outside [0, s_kv) is also skipped and sets
+ *           MLA_DEVERR_BAD_INDEX (FlashMLA itself does no bound check).
+ *  metadata from mla_get_metadata(NULL, batch, s_q, 0, topk, num_sm_parts, ...)
+ *  Other arguments as for mla_decode.  Invariant to the order of indices up
+ *  to floating-point rounding.
+ */
+int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv, const int32_t* indices,
+                      int topk, int batch, int s_q, int h_q, float softmax_scale,
+                      const void* metadata, int num_sm_parts, void* workspace, void* out,
+                      float* lse, uint32_t* err, cudaStream_t stream);
+
+/*
+ * LSE combine of split partials (DeepGEMM & FlashMLA article, section 7:
+ * m = max m_i, l = sum l_i e^(m_i - m), o = sum o_i l_i e^(m_i - m) / l; here
+ * with lse_i = m_i + ln l_i and o_i already divided by l_i).  mla_decode and
+ * mla_sparse_decode launch it themselves; it is exported for callers that
+ * run the split kernels through their own graph.  Writes out/lse for every
+ * sequence with two or more splits, and zeros / -inf for empty sequences.
+ */
+int mla_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm_parts,
+                const void* workspace, void* out, float* lse, cudaStream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MLA_DECODE_H_ */

@@ -1,0 +1,145 @@
+// Host entry points of the split-KV decode: argument checks, TMA tensor maps,
+// the cluster launch of the split kernel and the PDL launch of the combine.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mla_decode.h"
+#include "mla_internal.h"
+#include "mla_splitkv.cuh"
+
+namespace mla {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 row-major tensor [rows, 576] with row stride `stride_bytes`; boxes
+// of [box_rows x 64 columns] with 128-byte swizzle.
+bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t stride_bytes,
+                   uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), rows};
+  const cuuint64_t strides[1] = {stride_bytes};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <KvMode kMode>
+int configure_kernel() {
+  static int state = 0;  // 0 unset, 1 ok, -1 failed
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (state == 0) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        mla_splitkv_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    state = e == cudaSuccess ? 1 : -1;
+    if (e != cudaSuccess) return record_cuda_error("cudaFuncSetAttribute(split kernel)", e);
+  }
+  return state == 1 ? MLA_OK : record_error("split kernel configuration failed earlier", MLA_ERR_CUDA);
+}
+
+template <KvMode kMode>
+int launch_split(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const SplitParams& prm,
+                 cudaStream_t stream) {
+  int rc = configure_kernel<kMode>();
+  if (rc != MLA_OK) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(prm.num_parts * prm.n_hblk, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = prm.n_hblk;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_splitkv_kernel<kMode>, tm_q, tm_kv, prm);
+  return e == cudaSuccess ? MLA_OK : record_cuda_error("split kernel launch", e);
+}
+
+}  // namespace
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
+                          const int32_t* block_table, int64_t block_table_stride,
+                          const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                          float softmax_scale, int causal, const void* metadata, int num_sm_parts,
+                          void* workspace, void* out, float* lse, uint32_t* err,
+                          cudaStream_t stream) {
+  int rc = check_common(batch, s_q, h_q, num_sm_parts);
+  if (rc != MLA_OK) return rc;
+  if (!q || !kv_cache || !block_table || !cache_seqlens || !metadata || !workspace || !out || !lse)
+    return MLA_ERR_NULL;
+  if (kv_format != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
+  if (num_pages <= 0 || num_pages > (int64_t{1} << 25) || block_table_stride <= 0)
+    return MLA_ERR_SHAPE;
+  if (!(softmax_scale > 0.f) || !(softmax_scale < 1e30f)) return MLA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(metadata) || !aligned16(workspace) ||
+      !aligned16(out))
+    return MLA_ERR_ALIGN;
+  (void)causal;  // causality is baked into the metadata's key counts
+
+  const int n_seq = batch * s_q;
+  const int n_hblk = head_blocks(h_q);
+  const int rows = h_q < kRowsPerCta ? h_q : kRowsPerCta;
+  CUtensorMap tm_q, tm_kv;
+  if (!make_rows_map(&tm_q, q, static_cast<uint64_t>(n_seq) * h_q, kDqk * 2, rows))
+    return record_error("cuTensorMapEncodeTiled failed for q", MLA_ERR_CUDA);
+  if (!make_rows_map(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kDqk * 2, kPage))
+    return record_error("cuTensorMapEncodeTiled failed for kv_cache", MLA_ERR_CUDA);
+
+  SplitParams prm = {};
+  prm.meta = static_cast<const int32_t*>(metadata);
+  prm.block_table = block_table;
+  prm.bt_stride = block_table_stride;
+  prm.num_pages = num_pages;
+  const int64_t ws_rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
+  prm.ws_o = static_cast<float*>(workspace);
+  prm.ws_lse = prm.ws_o + ws_rows * kDv;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.err = err;
+  prm.h = h_q;
+  prm.s_q = s_q;
+  prm.num_parts = num_sm_parts;
+  prm.n_hblk = n_hblk;
+  prm.rows = rows;
+  prm.scale_log2 = softmax_scale * 1.4426950408889634f;
+  rc = launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);
+  if (rc != MLA_OK) return rc;
+  return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, out, lse, stream, true);
+}
+
+extern "C" int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv,
+                                 const int32_t* indices, int topk, int batch, int s_q, int h_q,
+                                 float softmax_scale, const void* metadata, int num_sm_parts,
+                                 void* workspace, void* out, float* lse, uint32_t* err,
+                                 cudaStream_t stream) {
+  (void)q; (void)kv; (void)s_kv; (void)indices; (void)topk; (void)batch; (void)s_q; (void)h_q;
+  (void)softmax_scale; (void)metadata; (void)num_sm_parts; (void)workspace; (void)out;
+  (void)lse; (void)err; (void)stream;
+  return MLA_ERR_UNSUPPORTED;
+}

@@ -1,0 +1,228 @@
+// Tile-schedule metadata (device kernel and host mirror) and small host
+// entry points of the C ABI.
+#include <cstdio>
+#include <vector>
+
+#include "mla_decode.h"
+#include "mla_internal.h"
+#include "mla_schedule.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kMetaThreads = 1024;
+
+// Block-wide exclusive scan of one int64 per thread; returns the total.
+__device__ int64_t block_exclusive_scan(int64_t v, int64_t* out_excl, int64_t* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = (lane < (kMetaThreads / 32)) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  const int64_t before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  const int64_t total = warp_sums[kMetaThreads / 32 - 1];
+  __syncthreads();
+  *out_excl = before;
+  return total;
+}
+
+// One CTA builds the whole schedule.  Thread i owns the contiguous sequence
+// chunk [i*chunk, (i+1)*chunk).
+__global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* seqlens, int batch,
+                                                                int s_q, int causal, int topk,
+                                                                int num_parts, int32_t* meta) {
+  __shared__ int64_t warp_sums[32];
+  const int n_seq = batch * s_q;
+  const int chunk = (n_seq + kMetaThreads - 1) / kMetaThreads;
+  const int q0 = threadIdx.x * chunk;
+  const int q1 = min(n_seq, q0 + chunk);
+
+  // 1. tiles, keys and cost per sequence; chunk-local cost prefix.
+  int64_t local = 0;
+  for (int q = q0; q < q1; ++q) {
+    const int32_t keys = seq_keys(seqlens, q / s_q, q % s_q, s_q, causal, topk);
+    const int32_t nt = tiles_of(keys);
+    int32_t* s = meta_seq(meta, num_parts, q);
+    s[kSTiles] = nt; s[kSKeys] = keys; s[5] = 0; s[6] = 0; s[7] = 0;
+    s[kSCostPrefix] = static_cast<int32_t>(local);
+    local += cost_of(nt);
+  }
+  int64_t base;
+  const int64_t total = block_exclusive_scan(local, &base, warp_sums);
+  for (int q = q0; q < q1; ++q) meta_seq(meta, num_parts, q)[kSCostPrefix] += static_cast<int32_t>(base);
+  __syncthreads();
+  __threadfence_block();
+
+  const int64_t per_part = total > 0 ? (total + num_parts - 1) / num_parts : 1;
+
+  // 2. split counts per sequence (from the prefixes only).
+  int64_t nsplit_local = 0;
+  for (int q = q0; q < q1; ++q) {
+    int32_t* s = meta_seq(meta, num_parts, q);
+    const int32_t nt = s[kSTiles];
+    const int32_t ns = nt > 0 ? 1 + inner_boundaries(s[kSCostPrefix], nt, per_part) : 0;
+    s[kSNSplits] = ns;
+    nsplit_local += ns;
+  }
+  int64_t split_base;
+  const int64_t total_splits = block_exclusive_scan(nsplit_local, &split_base, warp_sums);
+  int64_t run = split_base;
+  for (int q = q0; q < q1; ++q) {
+    int32_t* s = meta_seq(meta, num_parts, q);
+    s[kSSplitOff] = static_cast<int32_t>(run);
+    run += s[kSNSplits];
+  }
+  __syncthreads();
+
+  // 3. part ranges.
+  for (int p = threadIdx.x; p < num_parts; p += kMetaThreads)
+    fill_part(meta, num_parts, n_seq, total, per_part, p);
+
+  if (threadIdx.x == 0) {
+    meta[kHMagic] = kMetaMagic; meta[kHVersion] = kMetaVersion; meta[kHNSeq] = n_seq;
+    meta[kHParts] = num_parts; meta[kHTile] = kTileTokens; meta[kHSq] = s_q;
+    meta[kHBatch] = batch; meta[kHCausal] = causal; meta[kHTopk] = topk;
+    meta[kHTotalSplits] = static_cast<int32_t>(total_splits);
+    meta[kHPerPart] = static_cast<int32_t>(per_part);
+    for (int i = kHPerPart + 1; i < kHeaderWords; ++i) meta[i] = 0;
+  }
+}
+
+}  // namespace
+
+namespace {
+thread_local char g_last_error[256] = "no error";
+}
+
+int record_cuda_error(const char* where, cudaError_t e) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e),
+                static_cast<int>(e));
+  return MLA_ERR_CUDA;
+}
+
+int record_error(const char* what, int status) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+  return status;
+}
+
+int check_common(int batch, int s_q, int h_q, int num_sm_parts) {
+  if (batch <= 0 || s_q <= 0 || s_q > kMaxSq || num_sm_parts <= 0) return MLA_ERR_SHAPE;
+  if (!heads_supported(h_q)) return MLA_ERR_SHAPE;
+  if (static_cast<int64_t>(batch) * s_q > (1 << 24)) return MLA_ERR_SHAPE;
+  return MLA_OK;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_NULL: return "a required pointer is NULL";
+    case MLA_ERR_SHAPE: return "unsupported or inconsistent size argument";
+    case MLA_ERR_ALIGN: return "pointer or stride is not 16-byte aligned";
+    case MLA_ERR_METADATA: return "metadata does not match this call";
+    case MLA_ERR_CUDA: return "a CUDA runtime call failed";
+    case MLA_ERR_UNSUPPORTED: return "device is not supported (needs sm_103 / sm_100 class)";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* mla_last_error(void) { return g_last_error; }
+
+extern "C" int mla_num_sm_parts(int device, int h_q, int* num_sm_parts) {
+  if (!num_sm_parts) return MLA_ERR_NULL;
+  if (!heads_supported(h_q)) return MLA_ERR_SHAPE;
+  int sms = 0;
+  const cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return record_cuda_error("cudaDeviceGetAttribute", e);
+  *num_sm_parts = sms / head_blocks(h_q);
+  return *num_sm_parts > 0 ? MLA_OK : MLA_ERR_UNSUPPORTED;
+}
+
+extern "C" int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes) {
+  if (!bytes) return MLA_ERR_NULL;
+  if (batch <= 0 || s_q <= 0 || s_q > kMaxSq || num_sm_parts <= 0) return MLA_ERR_SHAPE;
+  *bytes = static_cast<size_t>(meta_words(batch * s_q, num_sm_parts)) * sizeof(int32_t);
+  return MLA_OK;
+}
+
+extern "C" int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts, size_t* bytes) {
+  if (!bytes) return MLA_ERR_NULL;
+  const int rc = check_common(batch, s_q, h_q, num_sm_parts);
+  if (rc != MLA_OK) return rc;
+  const int64_t rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
+  *bytes = static_cast<size_t>(rows) * (kDv + 1) * sizeof(float);
+  return MLA_OK;
+}
+
+static int check_meta_args(const int32_t* seqlens, int batch, int s_q, int topk, int num_sm_parts,
+                           const void* meta) {
+  if (!meta) return MLA_ERR_NULL;
+  if (topk <= 0 && !seqlens) return MLA_ERR_NULL;
+  if (batch <= 0 || s_q <= 0 || s_q > kMaxSq || num_sm_parts <= 0 || topk < 0)
+    return MLA_ERR_SHAPE;
+  if (static_cast<int64_t>(batch) * s_q > (1 << 24)) return MLA_ERR_SHAPE;
+  if (!aligned16(meta)) return MLA_ERR_ALIGN;
+  return MLA_OK;
+}
+
+extern "C" int mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int causal,
+                                int topk, int num_sm_parts, void* metadata, cudaStream_t stream) {
+  const int rc = check_meta_args(cache_seqlens, batch, s_q, topk, num_sm_parts, metadata);
+  if (rc != MLA_OK) return rc;
+  metadata_kernel<<<1, kMetaThreads, 0, stream>>>(cache_seqlens, batch, s_q, causal ? 1 : 0, topk,
+                                                 num_sm_parts, static_cast<int32_t*>(metadata));
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MLA_OK : record_cuda_error("metadata kernel launch", e);
+}
+
+extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q, int causal,
+                                     int topk, int num_sm_parts, void* metadata_host) {
+  const int rc = check_meta_args(seqlens, batch, s_q, topk, num_sm_parts, metadata_host);
+  if (rc != MLA_OK) return rc;
+  int32_t* meta = static_cast<int32_t*>(metadata_host);
+  const int n_seq = batch * s_q;
+  int64_t total = 0;
+  for (int q = 0; q < n_seq; ++q) {
+    const int32_t keys = seq_keys(seqlens, q / s_q, q % s_q, s_q, causal ? 1 : 0, topk);
+    const int32_t nt = tiles_of(keys);
+    int32_t* s = meta_seq(meta, num_sm_parts, q);
+    s[kSTiles] = nt; s[kSKeys] = keys; s[5] = 0; s[6] = 0; s[7] = 0;
+    s[kSCostPrefix] = static_cast<int32_t>(total);
+    total += cost_of(nt);
+  }
+  const int64_t per_part = total > 0 ? (total + num_sm_parts - 1) / num_sm_parts : 1;
+  int64_t splits = 0;
+  for (int q = 0; q < n_seq; ++q) {
+    int32_t* s = meta_seq(meta, num_sm_parts, q);
+    const int32_t nt = s[kSTiles];
+    s[kSNSplits] = nt > 0 ? 1 + inner_boundaries(s[kSCostPrefix], nt, per_part) : 0;
+    s[kSSplitOff] = static_cast<int32_t>(splits);
+    splits += s[kSNSplits];
+  }
+  for (int p = 0; p < num_sm_parts; ++p) fill_part(meta, num_sm_parts, n_seq, total, per_part, p);
+  meta[kHMagic] = kMetaMagic; meta[kHVersion] = kMetaVersion; meta[kHNSeq] = n_seq;
+  meta[kHParts] = num_sm_parts; meta[kHTile] = kTileTokens; meta[kHSq] = s_q;
+  meta[kHBatch] = batch; meta[kHCausal] = causal ? 1 : 0; meta[kHTopk] = topk;
+  meta[kHTotalSplits] = static_cast<int32_t>(splits);
+  meta[kHPerPart] = static_cast<int32_t>(per_part);
+  for (int i = kHPerPart + 1; i < kHeaderWords; ++i) meta[i] = 0;
+  return MLA_OK;
+}

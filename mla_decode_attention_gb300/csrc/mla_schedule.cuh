@@ -1,0 +1,146 @@
+// Split-KV tile schedule shared by the metadata kernel, its host mirror and
+// the decode kernels.  Pure integer arithmetic, compiled for host and device.
+//
+// Each (request b, new token j) is a sequence q = b * s_q + j whose keys are
+// cut into 128-key tiles.  A sequence piece costs its tiles plus kFixedCost
+// (the Q load and the epilogue); the global cost line is cut into
+// num_parts equal ranges, so a sequence may be split between parts
+// (FlashMLA deep dive, "Tile Scheduler": balanced assignment of requests and
+// blocks to SMs; DeepGEMM & FlashMLA article, section 7 "split-KV").
+#pragma once
+
+#include <cstdint>
+
+#ifdef __CUDACC__
+#define MLA_HD __host__ __device__ __forceinline__
+#else
+#define MLA_HD inline
+#endif
+
+namespace mla {
+
+constexpr int kTileTokens = 128;
+constexpr int kFixedCost = 1;
+constexpr int32_t kMetaMagic = 0x4D4C4131;  // "MLA1"
+constexpr int32_t kMetaVersion = 1;
+
+// header words
+enum : int {
+  kHMagic = 0, kHVersion, kHNSeq, kHParts, kHTile, kHSq, kHBatch, kHCausal, kHTopk,
+  kHTotalSplits, kHPerPart, kHeaderWords = 16
+};
+constexpr int kPartWords = 8;  // q_begin, t_begin, q_end, t_end, split_begin, 0, 0, 0
+constexpr int kSeqWords = 8;   // n_tiles, split_offset, n_splits, keys, cost_prefix, 0, 0, 0
+enum : int { kSTiles = 0, kSSplitOff, kSNSplits, kSKeys, kSCostPrefix };
+
+MLA_HD int64_t meta_words(int n_seq, int num_parts) {
+  return kHeaderWords + static_cast<int64_t>(kPartWords) * num_parts +
+         static_cast<int64_t>(kSeqWords) * n_seq;
+}
+MLA_HD int32_t* meta_part(int32_t* m, int p) { return m + kHeaderWords + kPartWords * p; }
+MLA_HD const int32_t* meta_part(const int32_t* m, int p) {
+  return m + kHeaderWords + kPartWords * p;
+}
+MLA_HD int32_t* meta_seq(int32_t* m, int num_parts, int q) {
+  return m + kHeaderWords + kPartWords * num_parts + kSeqWords * q;
+}
+MLA_HD const int32_t* meta_seq(const int32_t* m, int num_parts, int q) {
+  return m + kHeaderWords + kPartWords * num_parts + kSeqWords * q;
+}
+
+// Key count of sequence (b, j).
+MLA_HD int32_t seq_keys(const int32_t* seqlens, int b, int j, int s_q, int causal, int topk) {
+  if (topk > 0) return topk;
+  int32_t L = seqlens[b];
+  if (L < 0) L = 0;
+  if (causal) {
+    L = L - s_q + 1 + j;
+    if (L < 0) L = 0;
+  }
+  return L;
+}
+
+MLA_HD int32_t tiles_of(int32_t keys) { return (keys + kTileTokens - 1) / kTileTokens; }
+MLA_HD int32_t cost_of(int32_t n_tiles) { return n_tiles > 0 ? n_tiles + kFixedCost : 0; }
+
+MLA_HD int64_t floordiv(int64_t a, int64_t b) {  // b > 0
+  return a >= 0 ? a / b : -((-a + b - 1) / b);
+}
+
+// Position (q, t) of cost offset x: q is the sequence whose cost range
+// [prefix[q], prefix[q] + cost[q]) contains x; t is the tile at that offset
+// (offsets inside the fixed cost map to tile 0).  x >= total maps to (n_seq, 0).
+MLA_HD void cost_position(const int32_t* meta, int num_parts, int n_seq, int64_t total, int64_t x,
+                          int* q_out, int* t_out) {
+  if (x >= total) {
+    *q_out = n_seq;
+    *t_out = 0;
+    return;
+  }
+  int lo = 0, hi = n_seq - 1;
+  while (lo < hi) {  // largest q with prefix[q] <= x
+    const int mid = (lo + hi + 1) >> 1;
+    if (meta_seq(meta, num_parts, mid)[kSCostPrefix] <= x) lo = mid; else hi = mid - 1;
+  }
+  const int64_t local = x - meta_seq(meta, num_parts, lo)[kSCostPrefix];
+  *q_out = lo;
+  *t_out = static_cast<int>(local > kFixedCost ? local - kFixedCost : 0);
+}
+
+// Number of part boundaries p*per_part that fall strictly inside the tiles of
+// a sequence with cost prefix `prefix` and `n_tiles` tiles (tile index >= 1).
+MLA_HD int32_t inner_boundaries(int64_t prefix, int32_t n_tiles, int64_t per_part) {
+  if (n_tiles <= 1) return 0;
+  const int64_t lo = prefix + kFixedCost + 1;          // first offset with tile >= 1
+  const int64_t hi = prefix + kFixedCost + n_tiles;    // one past the last offset
+  return static_cast<int32_t>(floordiv(hi - 1, per_part) - floordiv(lo - 1, per_part));
+}
+
+// Fills part p's record from the per-sequence cost prefixes.
+MLA_HD void fill_part(int32_t* meta, int num_parts, int n_seq, int64_t total, int64_t per_part,
+                      int p) {
+  int qb, tb, qe, te;
+  const int64_t xb = static_cast<int64_t>(p) * per_part;
+  int64_t xe = xb + per_part;
+  if (xe > total) xe = total;
+  cost_position(meta, num_parts, n_seq, total, xb, &qb, &tb);
+  cost_position(meta, num_parts, n_seq, total, xe, &qe, &te);
+  int32_t split_begin = 0;
+  if (qb < n_seq && tb > 0) {
+    const int64_t prefix = meta_seq(meta, num_parts, qb)[kSCostPrefix];
+    split_begin = static_cast<int32_t>(p - floordiv(prefix + kFixedCost, per_part));
+  }
+  int32_t* r = meta_part(meta, p);
+  r[0] = qb; r[1] = tb; r[2] = qe; r[3] = te; r[4] = split_begin;
+  r[5] = 0; r[6] = 0; r[7] = 0;
+}
+
+// The work a part walks: pieces (q, [t0, t1), split index) in order.
+struct PartCursor {
+  int q, t, q_end, t_end, split;
+};
+
+MLA_HD PartCursor part_cursor(const int32_t* meta, int p) {
+  const int32_t* r = meta_part(meta, p);
+  PartCursor c;
+  c.q = r[0]; c.t = r[1]; c.q_end = r[2]; c.t_end = r[3]; c.split = r[4];
+  return c;
+}
+
+// Advances to the next non-empty piece.  Returns false when the part is done.
+MLA_HD bool next_piece(const int32_t* meta, int num_parts, PartCursor* c, int* q, int* t0,
+                       int* t1, int* split) {
+  while (c->q < c->q_end || (c->q == c->q_end && c->t < c->t_end)) {
+    const int32_t n_tiles = meta_seq(meta, num_parts, c->q)[kSTiles];
+    const int stop = (c->q == c->q_end) ? c->t_end : n_tiles;
+    if (n_tiles > 0 && c->t < stop) {
+      *q = c->q; *t0 = c->t; *t1 = stop; *split = c->split;
+      c->q += 1; c->t = 0; c->split = 0;
+      return true;
+    }
+    c->q += 1; c->t = 0; c->split = 0;
+  }
+  return false;
+}
+
+}  // namespace mla

@@ -1,0 +1,478 @@
+// Split-KV MLA decode kernel for sm_103a (tcgen05 MMA, TMEM accumulators,
+// TMA-fed shared-memory ring, warp-specialised roles).
+//
+// One CTA owns 64 query rows (the heads of one block of one query token) and
+// walks the (sequence, 128-key tile) range its schedule part assigns.  Per
+// tile it computes, transposed so that key tokens sit on TMEM lanes:
+//
+//   S^T[128 tokens x 64 rows]  = K_tile[128 x 576] . Q^T          (QK^T, K = 576)
+//   online softmax over tokens (column-wise, fp32, warp shuffles)
+//   O^T[512 x 64 rows]        += V_tile^T[512 x 128] . P^T[128 x 64] (PV)
+//
+// with V_tile = the first 512 columns of the same shared-memory tile, so each
+// 576-wide cached row is loaded once and feeds both products (FlashMLA deep
+// dive, "Theoretical Analysis": K and V are the same latent row).  The TMEM
+// accumulators hold O^T (4 x 64 columns) and S^T (64 columns); no output
+// matrix lives in registers, which is why no seesaw schedule is needed here
+// (the seesaw in the FlashMLA deep dive exists because WGMMA keeps O in
+// registers).
+//
+// Roles (416 threads):
+//   warp 0 lane 0  : producer, TMA loads of Q (once per piece) and of each
+//                    tile's 9 column chunks (two 64-token pages per chunk)
+//   warps 4..7     : softmax warpgroup 0, query rows 0..31 of the block
+//   warps 8..11    : softmax warpgroup 1, query rows 32..63
+//   warp 12        : TMEM allocation and the single MMA-issuing thread
+//   warps 1..3     : idle
+//
+// Shared memory (1024-byte aligned): 9 KV chunk slots of [128 tok x 64 col]
+// bf16 (16 KB each, 128-byte swizzle), Q as 9 chunks of [64 rows x 64 col]
+// (8 KB each).  Slot 8 (the RoPE columns) is dead after QK^T and holds P^T
+// during PV.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstddef>
+
+#include "mla_decode.h"
+#include "mla_ptx.cuh"
+#include "mla_schedule.cuh"
+
+namespace mla {
+
+constexpr int kRowsPerCta = 64;           // query rows per CTA = MMA N
+constexpr int kChunks = 9;                // 576 / 64 columns
+constexpr int kChunkBytes = kTileTokens * 64 * 2;   // 16 KB
+constexpr int kQChunkBytes = kRowsPerCta * 64 * 2;  // 8 KB
+constexpr int kSmemKv = 0;
+constexpr int kSmemQ = kChunks * kChunkBytes;                 // 147456
+constexpr int kSmemSmall = kSmemQ + kChunks * kQChunkBytes;   // 221184
+constexpr int kNumBarriers = 2 * kChunks + 5;
+constexpr int kSmallBytes = 8 * kNumBarriers + 16 + 4 * 4 * 2 * 4 * 32;
+constexpr int kSmemBytes = kSmallBytes + kSmemSmall + 1024;   // + alignment slack
+constexpr int kThreads = 416;
+constexpr int kProducerWarp = 0;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kMmaWarp = 12;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0;     // O^T: 4 blocks of 64 columns
+constexpr uint32_t kTmemS = 256;   // S^T: 64 columns
+constexpr uint32_t kIdescQK = idesc_bf16(128, kRowsPerCta, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16(128, kRowsPerCta, true, true);
+
+enum class KvMode : int { kPagedBf16 = 0, kSparseBf16 = 1 };
+
+struct SplitParams {
+  const int32_t* meta;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int64_t num_pages;       // dense: pages in the cache
+  const int32_t* indices;  // sparse: [n_seq, topk]
+  int topk;
+  int64_t s_kv;            // sparse: pool rows
+  const __nv_bfloat16* kv_rows;  // sparse: pool base
+  float* ws_o;
+  float* ws_lse;
+  __nv_bfloat16* out;
+  float* lse;
+  uint32_t* err;
+  int h;
+  int s_q;
+  int num_parts;
+  int n_hblk;
+  int rows;                // query rows loaded per CTA (min(h, 64))
+  float scale_log2;        // softmax_scale * log2(e)
+};
+
+struct SmemSmall {
+  // float arrays first: each row of 32 floats is read back as float4 vectors,
+  // so every row must start on a 16-byte boundary.
+  alignas(16) float red_max[2][4][32];
+  alignas(16) float red_sum[2][4][32];
+  alignas(16) float bcast[2][4][32];
+  alignas(16) float bcast2[2][4][32];
+  uint64_t full[kChunks];
+  uint64_t empty[kChunks];
+  uint64_t q_full, q_empty, s_full, p_full, o_done;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+static_assert(offsetof(SmemSmall, bcast) % 16 == 0 && offsetof(SmemSmall, bcast2) % 16 == 0,
+              "broadcast rows are read as float4");
+static_assert(offsetof(SmemSmall, full) % 8 == 0, "mbarriers are 8-byte objects");
+static_assert(sizeof(SmemSmall) <= kSmallBytes, "small smem region");
+
+// Reduce 32 per-thread values (one per query row of this warpgroup) over the
+// warp's 32 lanes, leaving in lane l the reduction for row l.  Recursive
+// halving: at each step a lane keeps the half of its vector that its lane bit
+// selects and adds the partner's copy of that half.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter32(const float (&v)[32], int lane) {
+  float a[16], b[8], c[4], d[2];
+  bool hi = lane & 16;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float send = hi ? v[i] : v[i + 16];
+    const float keep = hi ? v[i + 16] : v[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 16);
+    a[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  hi = lane & 8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = hi ? a[i] : a[i + 8];
+    const float keep = hi ? a[i + 8] : a[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 8);
+    b[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  hi = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = hi ? b[i] : b[i + 4];
+    const float keep = hi ? b[i + 4] : b[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 4);
+    c[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  hi = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = hi ? c[i] : c[i + 2];
+    const float keep = hi ? c[i + 2] : c[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 2);
+    d[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  hi = lane & 1;
+  const float send = hi ? d[0] : d[1];
+  const float keep = hi ? d[1] : d[0];
+  const float r = __shfl_xor_sync(0xffffffffu, send, 1);
+  return kMax ? fmaxf(keep, r) : keep + r;
+}
+
+__device__ __forceinline__ void load_bcast32(const float* src, float (&dst)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const float4 t = *reinterpret_cast<const float4*>(src + i);
+    dst[i] = t.x; dst[i + 1] = t.y; dst[i + 2] = t.z; dst[i + 3] = t.w;
+  }
+}
+
+template <KvMode kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_splitkv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_kv,
+                       const __grid_constant__ SplitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  SmemSmall* sm = reinterpret_cast<SmemSmall*>(smem + kSmemSmall);
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t kv_base = smem_base + kSmemKv;
+  const uint32_t q_base = smem_base + kSmemQ;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int part = blockIdx.x / p.n_hblk;
+  const int hb = blockIdx.x % p.n_hblk;
+  const int32_t* meta = p.meta;
+
+  // ---- setup: barriers, TMEM, zeroed padding rows of Q
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < kChunks; ++c) {
+      mbar_init(smem_u32(&sm->full[c]), 1);
+      mbar_init(smem_u32(&sm->empty[c]), 1);
+    }
+    mbar_init(smem_u32(&sm->q_full), 1);
+    mbar_init(smem_u32(&sm->q_empty), 1);
+    mbar_init(smem_u32(&sm->s_full), 1);
+    mbar_init(smem_u32(&sm->p_full), 8);  // one arrive per softmax warp
+    mbar_init(smem_u32(&sm->o_done), 1);
+    sm->abort = 0;
+    fence_mbarrier_init();
+  }
+  if (p.rows < kRowsPerCta) {
+    // Rows [rows, 64) of every Q chunk are never written by TMA; zero them
+    // once so the padded columns of S^T stay finite.
+    const int pad_bytes = (kRowsPerCta - p.rows) * 128;
+    for (int i = threadIdx.x; i < kChunks * pad_bytes / 16; i += kThreads) {
+      const int c = i / (pad_bytes / 16), k = i % (pad_bytes / 16);
+      const uint32_t a = q_base + c * kQChunkBytes + p.rows * 128 + k * 16;
+      st_shared_v4(a, 0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile uint32_t* abort_flag = &sm->abort;
+
+  if (warp == kProducerWarp) {
+    // ===================================================== producer (TMA)
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_first();
+      const uint64_t pol_q = l2_policy_evict_last();
+      PartCursor cur = part_cursor(meta, part);
+      int q, t0, t1, split;
+      uint32_t tile_ctr = 0, item_ctr = 0;
+      int32_t issued[kChunks];  // tile counter of each slot's latest load, -1 = none
+      for (int c = 0; c < kChunks; ++c) issued[c] = -1;
+      bool ok = true;
+      while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+        // Q rows of this block: 9 boxes of [rows x 64 columns]
+        ok = mbar_wait(smem_u32(&sm->q_empty), (item_ctr & 1) ^ 1, abort_flag, p.err);
+        if (!ok) break;
+        mbar_arrive_expect_tx(smem_u32(&sm->q_full), kChunks * p.rows * 128);
+        const int q_row = q * p.h + hb * kRowsPerCta;
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(q_base + c * kQChunkBytes, &tm_q, c * 64, q_row, smem_u32(&sm->q_full), pol_q);
+        const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
+        const int b = q / p.s_q;
+        const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+        const int last_page = (keys - 1) / kPage;
+        for (int t = t0; t < t1 && ok; ++t) {
+          int32_t y[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int pg = min(2 * t + h2, last_page);
+            int32_t blk = bt_row[pg];
+            if (blk < 0 || static_cast<int64_t>(blk) >= p.num_pages) {
+              if (p.err) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
+              blk = static_cast<int32_t>(p.num_pages);  // out of range: TMA fills zeros
+            }
+            y[h2] = blk * kPage;
+          }
+          const uint32_t par = (tile_ctr & 1) ^ 1;
+          for (int c = 0; c < kChunks; ++c) {
+            ok = mbar_wait(smem_u32(&sm->empty[c]), par, abort_flag, p.err);
+            if (!ok) break;
+            const uint32_t bar = smem_u32(&sm->full[c]);
+            mbar_arrive_expect_tx(bar, kChunkBytes);
+            const uint32_t dst = kv_base + c * kChunkBytes;
+            tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol_kv);
+            tma_load_2d(dst + kChunkBytes / 2, &tm_kv, c * 64, y[1], bar, pol_kv);
+            issued[c] = static_cast<int32_t>(tile_ctr);
+          }
+          ++tile_ctr;
+        }
+        ++item_ctr;
+      }
+      if (!ok) {
+        // Let copies already in flight land before the CTA exits.
+        for (int c = 0; c < kChunks; ++c) {
+          if (issued[c] < 0) continue;
+          const uint64_t t_start = globaltimer_ns();
+          while (!mbar_try_wait(smem_u32(&sm->full[c]), static_cast<uint32_t>(issued[c]) & 1u) &&
+                 globaltimer_ns() - t_start < 1000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ===================================================== MMA issuer
+    if (lane == 0) {
+      PartCursor cur = part_cursor(meta, part);
+      int q, t0, t1, split;
+      uint32_t tile_ctr = 0, item_ctr = 0;
+      bool ok = true;
+      while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+        ok = mbar_wait(smem_u32(&sm->q_full), item_ctr & 1, abort_flag, p.err);
+        if (!ok) break;
+        for (int t = t0; t < t1 && ok; ++t) {
+          const uint32_t par = tile_ctr & 1;
+          // S^T = K_tile . Q^T: A = tile chunk (K-major), B = Q chunk (K-major)
+          for (int c = 0; c < kChunks; ++c) {
+            ok = mbar_wait(smem_u32(&sm->full[c]), par, abort_flag, p.err);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = sw128_desc(kv_base + c * kChunkBytes + 32 * k, 16, 1024);
+              const uint64_t bq = sw128_desc(q_base + c * kQChunkBytes + 32 * k, 16, 1024);
+              mma_bf16_ss(tmem + kTmemS, a, bq, kIdescQK, (c | k) != 0);
+            }
+          }
+          if (!ok) break;
+          if (t == t1 - 1) mma_commit(smem_u32(&sm->q_empty));
+          mma_commit(smem_u32(&sm->s_full));
+          // O^T += V^T . P^T: A = tile chunks 2m, 2m+1 read MN-major (the 64
+          // latent columns of a chunk are contiguous), B = P^T in slot 8
+          // (MN-major: the 64 rows of a token are contiguous)
+          ok = mbar_wait(smem_u32(&sm->p_full), par, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t p_base = kv_base + 8 * kChunkBytes;
+          for (int m = 0; m < 4; ++m) {
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+              const uint64_t a = sw128_desc(kv_base + 2 * m * kChunkBytes + 2048 * s, kChunkBytes, 1024);
+              const uint64_t bp = sw128_desc(p_base + 2048 * s, kChunkBytes, 1024);
+              mma_bf16_ss(tmem + kTmemO + 64 * m, a, bp, kIdescPV, (t != t0 || s != 0) ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&sm->empty[2 * m]));
+            mma_commit(smem_u32(&sm->empty[2 * m + 1]));
+          }
+          mma_commit(smem_u32(&sm->empty[8]));
+          mma_commit(smem_u32(&sm->o_done));
+          ++tile_ctr;
+        }
+        ++item_ctr;
+      }
+    }
+  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
+    // ===================================================== softmax / epilogue
+    const int g = (warp - kSoftmaxWarp0) >> 2;  // row half: rows 32g .. 32g+31
+    const int wq = warp & 3;                    // TMEM lane quarter
+    const int r = wq * 32 + lane;               // token row of the tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + kTmemS + 32 * g;
+    const uint32_t p_slot = kv_base + 8 * kChunkBytes;
+    const float NEG_INF = -INFINITY;
+    PartCursor cur = part_cursor(meta, part);
+    int q, t0, t1, split;
+    uint32_t tile_ctr = 0;
+    bool ok = true;
+    while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+      const int32_t* srec = meta_seq(meta, p.num_parts, q);
+      const int32_t keys = srec[kSKeys];
+      const int32_t* idx_row = (kMode == KvMode::kSparseBf16)
+                                   ? p.indices + static_cast<int64_t>(q) * p.topk : nullptr;
+      float m_run = NEG_INF, l_run = 0.f;  // for row 32g + lane
+      for (int t = t0; t < t1; ++t) {
+        const uint32_t par = tile_ctr & 1;
+        ok = mbar_wait(smem_u32(&sm->s_full), par, abort_flag, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        float x[32];
+        tmem_ld32(t_s, x);
+        tmem_wait_ld();
+        const int tok = t * kTileTokens + r;
+        bool valid = tok < keys;
+        if (kMode == KvMode::kSparseBf16 && valid) {
+          const int32_t id = idx_row[tok];
+          valid = id >= 0 && static_cast<int64_t>(id) < p.s_kv;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = valid ? x[i] * p.scale_log2 : NEG_INF;
+        // row max over the 128 tokens
+        float mx = warp_reduce_scatter32<true>(x, lane);
+        sm->red_max[g][wq][lane] = mx;
+        named_barrier_sync(1 + g, 128);
+        mx = fmaxf(fmaxf(sm->red_max[g][0][lane], sm->red_max[g][1][lane]),
+                   fmaxf(sm->red_max[g][2][lane], sm->red_max[g][3][lane]));
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = (m_new == NEG_INF) ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - m_use);  // 0 for the first tile
+        sm->bcast[g][wq][lane] = m_use;
+        __syncwarp();
+        float mb[32];
+        load_bcast32(&sm->bcast[g][wq][0], mb);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = fast_exp2(x[i] - mb[i]);
+        float sum = warp_reduce_scatter32<false>(x, lane);
+        sm->red_sum[g][wq][lane] = sum;
+        // P^T row r, rows 32g..32g+31 -> 16-byte units 4g..4g+3 (swizzled)
+        const uint32_t prow = p_slot + r * 128;
+#pragma unroll
+        for (int cu = 0; cu < 4; ++cu) {
+          const uint32_t unit = static_cast<uint32_t>((4 * g + cu) ^ (r & 7));
+          st_shared_v4(prow + unit * 16, pack_bf16x2(x[8 * cu + 0], x[8 * cu + 1]),
+                       pack_bf16x2(x[8 * cu + 2], x[8 * cu + 3]),
+                       pack_bf16x2(x[8 * cu + 4], x[8 * cu + 5]),
+                       pack_bf16x2(x[8 * cu + 6], x[8 * cu + 7]));
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1 + g, 128);
+        sum = (sm->red_sum[g][0][lane] + sm->red_sum[g][1][lane]) +
+              (sm->red_sum[g][2][lane] + sm->red_sum[g][3][lane]);
+        l_run = alpha * l_run + sum;
+        m_run = m_new;
+        if (t != t0) {
+          // PV of the previous tile must be complete before O^T is rescaled
+          ok = mbar_wait(smem_u32(&sm->o_done), par ^ 1, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            sm->bcast2[g][wq][lane] = alpha;
+            __syncwarp();
+            float ab[32];
+            load_bcast32(&sm->bcast2[g][wq][0], ab);
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
+              float o[32];
+              const uint32_t t_o = tmem + lane_off + kTmemO + 64 * m + 32 * g;
+              tmem_ld32(t_o, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= ab[i];
+              tmem_st32(t_o, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
+        ++tile_ctr;
+      }
+      if (!ok) break;
+      // ---- epilogue: O^T / l -> out (one split) or fp32 partial
+      ok = mbar_wait(smem_u32(&sm->o_done), (tile_ctr - 1) & 1, abort_flag, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      const bool has = l_run > 0.f;
+      const float inv_l = has ? 1.f / l_run : 0.f;
+      const float lse_v = has ? (m_run + __log2f(l_run)) * 0.69314718055994531f : NEG_INF;
+      sm->bcast2[g][wq][lane] = inv_l;
+      __syncwarp();
+      float il[32];
+      load_bcast32(&sm->bcast2[g][wq][0], il);
+      const bool final_out = srec[kSNSplits] == 1;
+      const int row0 = hb * kRowsPerCta + 32 * g;  // first head of this warpgroup
+      const int split_row = srec[kSSplitOff] + split;
+      const int b = q / p.s_q, j = q % p.s_q;
+#pragma unroll 1
+      for (int m = 0; m < 4; ++m) {
+        float o[32];
+        tmem_ld32(tmem + lane_off + kTmemO + 64 * m + 32 * g, o);
+        tmem_wait_ld();
+        const int d = 128 * m + 32 * wq + lane;
+        if (final_out) {
+          __nv_bfloat16* dst = p.out + (static_cast<int64_t>(q) * p.h + row0) * kDv + d;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (row0 + i < p.h) dst[static_cast<int64_t>(i) * kDv] = __float2bfloat16_rn(o[i] * il[i]);
+        } else {
+          float* dst = p.ws_o + (static_cast<int64_t>(split_row) * p.h + row0) * kDv + d;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (row0 + i < p.h) dst[static_cast<int64_t>(i) * kDv] = o[i] * il[i];
+        }
+      }
+      if (wq == 0 && row0 + lane < p.h) {
+        if (final_out)
+          p.lse[(static_cast<int64_t>(b) * p.h + row0 + lane) * p.s_q + j] = lse_v;
+        else
+          p.ws_lse[static_cast<int64_t>(split_row) * p.h + row0 + lane] = lse_v;
+      }
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  pdl_launch_dependents();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace mla

@@ -1,0 +1,184 @@
+"""Host-side tests of the C ABI (no GPU): exports, argument checks, schedule.
+
+The schedule tests pin ``mla_get_metadata_host`` by invariants: every
+(sequence, tile) pair is covered exactly once, pieces of a sequence are
+numbered 0..n_splits-1 in order, split offsets are the exclusive prefix of
+split counts, key counts follow the causal reading, and parts are balanced.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from mla_decode_attention_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_decode.h")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    if not os.path.exists(binding.LIB_PATH):
+        build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_are_exported():
+    names = declared_functions()
+    assert "mla_decode" in names and "mla_get_metadata" in names and len(names) >= 9
+    lib = ctypes.CDLL(binding.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/mla_decode.h but not exported"
+
+
+def test_binding_covers_every_declared_function():
+    assert set(declared_functions()) <= set(binding._SIGS)
+
+
+def test_status_strings():
+    assert binding.status_string(0) == "ok"
+    for s in (-1, -2, -3, -4, -5, -6):
+        assert binding.status_string(s) not in ("ok", "unknown status")
+    assert binding.status_string(12345) == "unknown status"
+
+
+def test_sizes():
+    assert binding.mla_metadata_size(64, 1, 76) == 4 * (16 + 8 * 76 + 8 * 64)
+    assert binding.mla_workspace_size(64, 1, 128, 76) == (64 + 76) * 128 * 513 * 4
+    with pytest.raises(binding.MlaError):
+        binding.mla_workspace_size(64, 1, 100, 76)      # unsupported head count
+    with pytest.raises(binding.MlaError):
+        binding.mla_metadata_size(0, 1, 76)
+    with pytest.raises(binding.MlaError):
+        binding.mla_metadata_size(4, 17, 76)             # s_q > 16
+
+
+def _decode_args(**over):
+    """Arguments of mla_decode with fake (never dereferenced) aligned pointers."""
+    a = dict(q=0x10000, kv=0x20000, fmt=0, pages=16, bt=0x30000, bt_stride=8, sl=0x40000,
+             batch=2, s_q=1, h=16, scale=0.07, causal=1, meta=0x50000, parts=4, ws=0x60000,
+             out=0x70000, lse=0x80000, err=None, stream=None)
+    a.update(over)
+    return a
+
+
+def _call_decode(a):
+    return binding.lib().mla_decode(a["q"], a["kv"], a["fmt"], a["pages"], a["bt"],
+                                    a["bt_stride"], a["sl"], a["batch"], a["s_q"], a["h"],
+                                    a["scale"], a["causal"], a["meta"], a["parts"], a["ws"],
+                                    a["out"], a["lse"], a["err"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), -1), (dict(kv=None), -1), (dict(out=None), -1), (dict(meta=None), -1),
+    (dict(h=100), -2), (dict(h=256), -2), (dict(s_q=0), -2), (dict(s_q=17), -2),
+    (dict(batch=0), -2), (dict(pages=0), -2), (dict(parts=0), -2), (dict(scale=0.0), -2),
+    (dict(scale=float("nan")), -2), (dict(q=0x10008), -3), (dict(kv=0x20004), -3),
+    (dict(out=0x70002), -3), (dict(fmt=7), -6),
+])
+def test_decode_rejects_bad_arguments_before_launch(over, code):
+    assert _call_decode(_decode_args(**over)) == code
+
+
+# ------------------------------------------------------------------ schedule
+
+def parse_meta(m, n_seq, parts):
+    hdr = m[:16]
+    prt = m[16:16 + 8 * parts].reshape(parts, 8)
+    seq = m[16 + 8 * parts:16 + 8 * parts + 8 * n_seq].reshape(n_seq, 8)
+    return hdr, prt, seq
+
+
+def walk_part(prt_row, seq):
+    """Pieces (q, t0, t1, split) a part processes, as the kernels walk them."""
+    q, t, qe, te, split = [int(x) for x in prt_row[:5]]
+    pieces = []
+    while q < qe or (q == qe and t < te):
+        nt = int(seq[q, 0])
+        stop = te if q == qe else nt
+        if nt > 0 and t < stop:
+            pieces.append((q, t, stop, split))
+        q, t, split = q + 1, 0, 0
+    return pieces
+
+
+def check_schedule(seqlens, s_q, causal, topk, parts):
+    b = len(seqlens)
+    m = binding.mla_get_metadata_host(None if topk else seqlens, b, s_q, causal, topk, parts)
+    hdr, prt, seq = parse_meta(m, b * s_q, parts)
+    assert hdr[0] == 0x4D4C4131 and hdr[2] == b * s_q and hdr[3] == parts and hdr[4] == 128
+    for q in range(b * s_q):
+        bi, j = divmod(q, s_q)
+        if topk:
+            keys = topk
+        else:
+            keys = max(0, seqlens[bi] - s_q + 1 + j) if causal else max(0, seqlens[bi])
+        assert seq[q, 3] == keys and seq[q, 0] == (keys + 127) // 128
+    covered = {}
+    per_part_cost = []
+    for p in range(parts):
+        cost = 0
+        for (q, t0, t1, split) in walk_part(prt[p], seq):
+            cost += (t1 - t0) + 1
+            for t in range(t0, t1):
+                assert (q, t) not in covered
+                covered[(q, t)] = (p, split)
+        per_part_cost.append(cost)
+    for q in range(b * s_q):
+        nt = int(seq[q, 0])
+        for t in range(nt):
+            assert (q, t) in covered, (q, t)
+        splits = [covered[(q, t)][1] for t in range(nt)]
+        # piece numbers start at 0 and grow by one at each part change
+        if nt:
+            assert splits[0] == 0
+            owners = [covered[(q, t)][0] for t in range(nt)]
+            for t in range(1, nt):
+                if owners[t] == owners[t - 1]:
+                    assert splits[t] == splits[t - 1]
+                else:
+                    assert splits[t] == splits[t - 1] + 1
+            assert seq[q, 2] == splits[-1] + 1
+        else:
+            assert seq[q, 2] == 0
+    offs = np.concatenate([[0], np.cumsum(seq[:, 2])[:-1]])
+    assert np.array_equal(seq[:, 1], offs)
+    assert hdr[9] == seq[:, 2].sum() <= b * s_q + parts
+    assert max(per_part_cost) <= hdr[10] + 1
+    return m
+
+
+@pytest.mark.parametrize("parts", [1, 2, 7, 76, 152, 400])
+def test_schedule_dense_invariants(parts):
+    rng = np.random.default_rng(parts)
+    seqlens = rng.integers(0, 5000, size=37).astype(np.int32)
+    seqlens[:4] = [0, 1, 128, 129]
+    check_schedule(seqlens, 1, True, 0, parts)
+
+
+@pytest.mark.parametrize("s_q,causal", [(2, True), (2, False), (3, True)])
+def test_schedule_spec_invariants(s_q, causal):
+    rng = np.random.default_rng(s_q)
+    seqlens = rng.integers(0, 20000, size=19).astype(np.int32)
+    seqlens[0] = 1   # causal: token 0 of this request sees nothing
+    check_schedule(seqlens, s_q, causal, 0, 76)
+
+
+def test_schedule_sparse_invariants():
+    check_schedule(np.zeros(64, np.int32), 1, False, 2048, 76)
+    check_schedule(np.zeros(5, np.int32), 2, False, 100, 152)
+
+
+def test_schedule_config_dense_v3_shape():
+    m = check_schedule(np.full(64, 4096, np.int32), 1, True, 0, 76)
+    hdr, prt, seq = parse_meta(m, 64, 76)
+    assert hdr[10] == (64 * 33 + 75) // 76          # balanced cost per part
+    assert seq[:, 2].max() <= 3

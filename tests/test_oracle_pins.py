@@ -365,3 +365,24 @@ def test_page_numbers_cost_model():
     assert roofline.FLOP_PER_PAIR == GOLDEN["flops_per_token_per_row"]["value"]
     g = GOLDEN["mma_cycles_per_token_64_heads_h800"]
     assert round(64 * (576 + 512) * 2 / g["flop_per_clk_per_sm"]) == g["value"]
+
+
+# ------------------------------------------------------- the parity checker
+
+def test_parity_checker_accepts_the_bf16_floor_and_rejects_real_errors():
+    """The ideal bf16 output passes; a 1% gain error or a dropped key fails."""
+    from tests._util import assert_parity
+    r = rng(30)
+    q = r.standard_normal((16, 576))
+    keys = r.standard_normal((40, 576))
+    o, l = oracle.attend(q, keys, SCALE)
+    o[3, 7] = 1.9                      # an element far above the RMS
+    ideal = torch.from_numpy(o).to(torch.bfloat16).double().numpy()
+    assert_parity(ideal, o, l, l, "ideal bf16")
+    with pytest.raises(AssertionError):
+        assert_parity(ideal * 1.01, o, l, l, "gain")
+    o2, l2 = oracle.attend(q, keys[1:], SCALE)
+    with pytest.raises(AssertionError):
+        assert_parity(torch.from_numpy(o2).to(torch.bfloat16).double().numpy(), o, l2, l, "drop")
+    with pytest.raises(AssertionError):
+        assert_parity(ideal, o, l + 2e-3, l, "lse")
