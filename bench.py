@@ -1,0 +1,473 @@
+"""Benchmark of MLA decode (absorbed, paged latent KV) on GB300.
+
+Metric: decode TFLOP/s on the DeepSeek-V3-shaped dense workload (b=64, s_q=1,
+h=128, 576/512, every request 4096 cached tokens, 64-token pages, shuffled
+page table), with the effective KV GB/s and the fraction of the GB300
+roofline min(bf16 peak, HBM BW x arithmetic intensity).
+
+One step = one pass of the whole decode path on one batch: schedule metadata
+(device kernel), split-KV kernel, combine kernel.  Steps are replayed from a
+CUDA graph; two full input sets (each larger than L2) alternate so that every
+step reads its KV cache from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has) on the host cores, on the same workload and metric.  Under
+torchrun every rank runs its own replica of the batch (weak scaling, no
+data-path collective); rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode TFLOPS & KV GB/s (b=64,h=128,t=4096) as fraction of GB300 roofline"
+UNIT = "TFLOP/s"
+WORKLOAD = "dense_v3"
+GRAPH_STEPS = 10
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+
+
+# --------------------------------------------------------------------- utils
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources; ncu traffic figures are valid only for it."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_decode_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    with open(os.path.join(ROOT, "include", "mla_decode.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(kernel, {}).get(workload)
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms", str(self.period_ms)],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_start: float, t_end: float):
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.tmp.name)
+        import datetime
+        clocks, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        in_window = []
+        for r in rows:
+            if len(r) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, mx = float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            in_window.append((t_start - 0.06 <= ts <= t_end + 0.06, clk, mx, r[6:10]))
+        chosen = [x for x in in_window if x[0]] or in_window
+        for _, clk, mx, flags in chosen:
+            clocks.append(clk)
+            maxes.append(mx)
+            for name, v in zip(names, flags):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(clocks) if clocks else None,
+                "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(clocks),
+                "in_timed_window": sum(1 for x in in_window if x[0])}
+
+
+# ---------------------------------------------------------------- ours (GPU)
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from mla_decode_attention_gb300 import binding, roofline, workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.config]
+    peaks = load_peaks()
+
+    # two input sets (each > L2), pinned host copies for the end-to-end leg
+    sets_host = [workloads.make_inputs(w, seed=w.seed + 1000 * rank + k) for k in range(2)]
+    for s in sets_host:
+        for key in ("q", "kv_cache", "block_table", "cache_seqlens"):
+            s[key] = s[key].pin_memory()
+    sets = [{k: (v.to(dev) if hasattr(v, "to") and hasattr(v, "pin_memory") else v)
+             for k, v in s.items()} for s in sets_host]
+    b, s_q, h = w.b, w.s_q, w.h
+    parts = binding.mla_num_sm_parts(local_rank, h)
+    bufs = [binding.DecodeBuffers(b, s_q, h, dev, parts) for _ in range(2)]
+    stream = torch.cuda.Stream(device=dev)
+    scale = workloads.SOFTMAX_SCALE
+
+    def step(k, split_only=False):
+        s, buf = sets[k % 2], bufs[k % 2]
+        if not split_only:
+            binding.mla_get_metadata(s["cache_seqlens"], b, s_q, True, 0, parts, buf.metadata,
+                                     stream)
+            binding.mla_decode(s["q"], s["kv_cache"], binding.MLA_KV_BF16, s["block_table"],
+                               s["cache_seqlens"], scale, True, buf.metadata, parts,
+                               buf.workspace, buf.out, buf.lse, buf.err, stream)
+        else:
+            binding.mla_decode_splitkv(s["q"], s["kv_cache"], binding.MLA_KV_BF16,
+                                       s["block_table"], s["cache_seqlens"], scale, True,
+                                       buf.metadata, parts, buf.workspace, buf.out, buf.lse,
+                                       buf.err, stream)
+
+    # metadata once so the split-only graph has a valid schedule
+    with torch.cuda.stream(stream):
+        for k in range(2):
+            step(k)
+    torch.cuda.synchronize(dev)
+    if args.profile:
+        # a few eager steps only: the command ncu captures
+        with torch.cuda.stream(stream):
+            for k in range(args.profile):
+                step(k)
+        torch.cuda.synchronize(dev)
+        return {"profile_steps": args.profile, "errors": [int(bf.err.item()) for bf in bufs]}
+
+    def capture(split_only):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for k in range(GRAPH_STEPS):
+                step(k, split_only)
+            g.capture_end()
+        return g
+
+    g_step = capture(False)
+    g_split = capture(True)
+    torch.cuda.synchronize(dev)
+
+    def replay(g, n_steps):
+        reps = n_steps // GRAPH_STEPS
+        rest = n_steps - reps * GRAPH_STEPS
+        for _ in range(reps):
+            g.replay()
+        with torch.cuda.stream(stream):
+            for k in range(rest):
+                step(k)
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        replay(g_step, max(args.warmup, 3))
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- timed region: exactly K steps
+    sampler = ClockSampler(dev.index)
+    with sampler:
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        t_wall0 = time.time()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            replay(g_step, args.steps)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        t_wall1 = time.time()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    clocks = sampler.summary(t_wall0, t_wall1)
+    ms_per_step = ms_total / args.steps
+
+    # ---- dominant kernel alone: split-KV launches back to back, same stream
+    n_split = max(GRAPH_STEPS, (min(args.steps, 2000) // GRAPH_STEPS) * GRAPH_STEPS)
+    torch.cuda.synchronize(dev)
+    k0 = torch.cuda.Event(enable_timing=True)
+    k1 = torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(n_split // GRAPH_STEPS):
+            g_split.replay()
+    k1.record(stream)
+    torch.cuda.synchronize(dev)
+    split_ms = k0.elapsed_time(k1) / n_split
+
+    errs = [int(bf.err.item()) for bf in bufs]
+
+    # ---- end to end through the public API with host buffers
+    n_e2e = max(3, min(args.steps, 50))
+    h2d = sum(sets_host[0][k].numel() * sets_host[0][k].element_size()
+              for k in ("q", "kv_cache", "block_table", "cache_seqlens"))
+    d2h = bufs[0].out.numel() * 2 + bufs[0].lse.numel() * 4
+    out_host = [torch.empty(bufs[0].out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    lse_host = [torch.empty(bufs[0].lse.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+
+    def e2e_step(k):
+        s_h, s_d, buf = sets_host[k % 2], sets[k % 2], bufs[k % 2]
+        for key in ("q", "kv_cache", "block_table", "cache_seqlens"):
+            s_d[key].copy_(s_h[key], non_blocking=True)
+        step(k)
+        out_host[k % 2].copy_(buf.out, non_blocking=True)
+        lse_host[k % 2].copy_(buf.lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            e2e_step(k)
+    torch.cuda.synchronize(dev)
+    barrier()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    with torch.cuda.stream(stream):
+        for k in range(n_e2e):
+            e2e_step(k)
+    x1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = x0.elapsed_time(x1) / n_e2e
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- accounting
+    seqlens = sets_host[0]["cache_seqlens"].tolist()
+    flops, bytes_, kv_bytes = roofline.dense_counts(seqlens, s_q, h, causal=True)
+    tflops = flops / (ms_per_step * 1e-3) / 1e12 * world
+    kv_gbs = kv_bytes / (ms_per_step * 1e-3) / 1e9 * world
+    ai = flops / bytes_
+    roof_tf = min(peaks["bf16_tflops"], peaks["hbm_gbs"] * ai / 1e3)
+    split_gbs = bytes_ / (split_ms * 1e-3) / 1e9
+    bound = "hbm" if peaks["hbm_gbs"] * ai / 1e3 < peaks["bf16_tflops"] else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = split_gbs, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = flops / (split_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    traffic = recorded_traffic("mla_splitkv_kernel", args.config)
+
+    result = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q and latent cache, shuffled page table)",
+        "config": {"workload": WORKLOAD if args.config == WORKLOAD else args.config,
+                   "batch": b, "s_q": s_q, "h_q": h, "d_qk": 576, "d_v": 512,
+                   "seqlen": seqlens[0] if len(set(seqlens)) == 1 else "mixed",
+                   "page_block": 64, "num_sm_parts": parts,
+                   "l2": "inputs larger than L2 (302 MB KV per set, two sets alternate)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kv_gbs": round(kv_gbs, 1),
+        "roofline_fraction": round(tflops / world / roof_tf, 4),
+        "roofline_tflops": round(roof_tf, 1),
+        "arithmetic_intensity": round(ai, 1),
+        "algorithmic": {"flops": flops, "bytes": bytes_, "kv_bytes": kv_bytes},
+        "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "mla_splitkv_kernel", "kernel_ms": round(split_ms, 5),
+                     "peak_source": f"{peaks.get('source')} (MEASURED_PEAKS.json burst copy)"},
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4),
+                "note": "all call inputs (q, KV cache, page table, lengths) copied from pinned "
+                        "host memory and out+lse copied back every step"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "device_error_word": errs,
+    }
+    return result
+
+
+# ------------------------------------------------------------ oracle on CPU
+
+def oracle_worker(argv):
+    """Subprocess: time the fp64 oracle on `n_req` requests of the workload."""
+    import numpy as np
+
+    import oracle
+    from mla_decode_attention_gb300 import roofline, workloads
+
+    cfg, n_req, reps = argv[0], int(argv[1]), int(argv[2])
+    w = workloads.WORKLOADS[cfg]
+    inp = workloads.make_inputs(w)
+    import torch
+    q = inp["q"].contiguous().view(torch.int16).numpy().view(np.uint16)
+    kv = inp["kv_cache"].contiguous().view(torch.int16).numpy().view(np.uint16)
+    bt = inp["block_table"].numpy()
+    sl = inp["cache_seqlens"].numpy()
+    rows = [(bi, j) for bi in range(min(n_req, w.b)) for j in range(w.s_q)]
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.dense_decode(q, kv, bt, sl, inp["softmax_scale"], True, rows)
+        times.append(time.perf_counter() - t0)
+    flops, _, _ = roofline.dense_counts(sl[:min(n_req, w.b)].tolist(), w.s_q, w.h)
+    print(json.dumps({"times": times, "flops": flops, "requests": min(n_req, w.b)}))
+
+
+def time_oracle(cfg, n_req, reps, threads):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", cfg,
+                        str(n_req), str(reps)], capture_output=True, text=True, env=env,
+                       timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle worker failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(cfg):
+    threads = os.cpu_count() or 1
+    probe = time_oracle(cfg, 1, 1, threads)
+    per_req = max(probe["times"][0], 1e-3)
+    n_req = max(1, min(64, int(20.0 / per_req)))
+    res = time_oracle(cfg, n_req, 1, threads)
+    t = res["times"][0]
+    return {"value": round(res["flops"] / t / 1e12, 6), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{res['requests']} of 64 requests of the same workload (all 128 heads, "
+                      f"4096 keys each), fp64 numpy, one pass, {t:.2f} s"}
+
+
+def run_reference(args):
+    threads = os.cpu_count() or 1
+    probe = time_oracle(args.config, 1, 1, threads)
+    per_req = max(probe["times"][0], 1e-3)
+    total_steps = args.steps + args.warmup
+    n_req = max(1, min(64, int(150.0 / (per_req * max(total_steps, 1)))))
+    res = time_oracle(args.config, n_req, total_steps, threads)
+    times = res["times"][args.warmup:] or res["times"]
+    t = sum(times) / len(times)
+    v = res["flops"] / t / 1e12
+    sample = (f"{res['requests']} of 64 requests per step (all 128 heads, 4096 keys), fp64 "
+              f"numpy oracle")
+    return {"metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same seeded workload)", "impl": "reference",
+            "config": {"workload": WORKLOAD if args.config == WORKLOAD else args.config},
+            "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------- main
+
+def main():
+    if len(sys.argv) > 1 and sys.argv[1] == "--oracle-worker":
+        oracle_worker(sys.argv[2:])
+        return
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", type=int, default=0,
+                    help="run only this many eager steps (for ncu captures) and exit")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    result = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline and not args.profile:
+            result["cpu_baseline"] = cpu_baseline(args.config)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -161,6 +161,20 @@ int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_p
                float* lse, uint32_t* err, cudaStream_t stream);
 
 /*
+ * The split-KV kernel of mla_decode alone (FlashMLA deep dive: the
+ * splitkv_mla kernel, before combine).  Same arguments and layouts.  Query
+ * rows whose keys fall in one split get their final out/lse here; rows cut
+ * into several splits get fp32 partials in `workspace`, merged by a
+ * following mla_combine on the same metadata and workspace.
+ */
+int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
+                       const int32_t* block_table, int64_t block_table_stride,
+                       const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                       float softmax_scale, int causal, const void* metadata, int num_sm_parts,
+                       void* workspace, void* out, float* lse, uint32_t* err,
+                       cudaStream_t stream);
+
+/*
  * DSA top-k sparse decode (FlashMLA README, "indices Tensor"): each query
  * token attends only to the pool rows its index list names.
  *

@@ -45,6 +45,8 @@ _SIGS = {
     "mla_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "mla_decode": (_i, [_vp, _vp, _i, _i64, _vp, _i64, _vp, _i, _i, _i, _f, _i, _vp, _i, _vp,
                         _vp, _vp, _vp, _vp]),
+    "mla_decode_splitkv": (_i, [_vp, _vp, _i, _i64, _vp, _i64, _vp, _i, _i, _i, _f, _i, _vp, _i,
+                                _vp, _vp, _vp, _vp, _vp]),
     "mla_sparse_decode": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _i, _vp, _vp, _vp,
                                _vp, _vp]),
     "mla_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
@@ -153,14 +155,8 @@ def mla_get_metadata_host(cache_seqlens, batch: int, s_q: int, causal: bool, top
 
 # ---------------------------------------------------------------- decode
 
-def mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, kv_format: int,
-               block_table: torch.Tensor, cache_seqlens: torch.Tensor, softmax_scale: float,
-               causal: bool, metadata: torch.Tensor, num_sm_parts: int,
-               workspace: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
-               err: Optional[torch.Tensor] = None, stream=None) -> None:
-    """q [b, s_q, h, 576] bf16; kv_cache [pages, 64, 576] bf16 (MLA_KV_BF16) or
-    [pages, 64, 656] uint8 (MLA_KV_FP8_656); block_table [b, max_pages] int32;
-    cache_seqlens [b] int32; out [b, s_q, h, 512] bf16; lse [b, h, s_q] fp32."""
+def _decode_call(name, q, kv_cache, kv_format, block_table, cache_seqlens, softmax_scale,
+                 causal, metadata, num_sm_parts, workspace, out, lse, err, stream):
     _dev(q, torch.bfloat16, "q")
     _dev(kv_cache, torch.bfloat16 if kv_format == MLA_KV_BF16 else torch.uint8, "kv_cache")
     _dev(cache_seqlens, torch.int32, "cache_seqlens")
@@ -172,12 +168,31 @@ def mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, kv_format: int,
     if err is not None:
         _dev(err, torch.int32, "err")
     b, s_q, h, d = q.shape
-    _check("mla_decode",
-           lib().mla_decode(_ptr(q), _ptr(kv_cache), kv_format, kv_cache.shape[0],
-                            _ptr(block_table), block_table.stride(0), _ptr(cache_seqlens),
-                            b, s_q, h, float(softmax_scale), int(bool(causal)), _ptr(metadata),
-                            num_sm_parts, _ptr(workspace), _ptr(out), _ptr(lse), _ptr(err),
-                            _stream(stream)))
+    _check(name, getattr(lib(), name)(
+        _ptr(q), _ptr(kv_cache), kv_format, kv_cache.shape[0], _ptr(block_table),
+        block_table.stride(0), _ptr(cache_seqlens), b, s_q, h, float(softmax_scale),
+        int(bool(causal)), _ptr(metadata), num_sm_parts, _ptr(workspace), _ptr(out), _ptr(lse),
+        _ptr(err), _stream(stream)))
+
+
+def mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, kv_format: int,
+               block_table: torch.Tensor, cache_seqlens: torch.Tensor, softmax_scale: float,
+               causal: bool, metadata: torch.Tensor, num_sm_parts: int,
+               workspace: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+               err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q [b, s_q, h, 576] bf16; kv_cache [pages, 64, 576] bf16 (MLA_KV_BF16) or
+    [pages, 64, 656] uint8 (MLA_KV_FP8_656); block_table [b, max_pages] int32;
+    cache_seqlens [b] int32; out [b, s_q, h, 512] bf16; lse [b, h, s_q] fp32."""
+    _decode_call("mla_decode", q, kv_cache, kv_format, block_table, cache_seqlens,
+                 softmax_scale, causal, metadata, num_sm_parts, workspace, out, lse, err, stream)
+
+
+def mla_decode_splitkv(q, kv_cache, kv_format, block_table, cache_seqlens, softmax_scale,
+                       causal, metadata, num_sm_parts, workspace, out, lse, err=None,
+                       stream=None) -> None:
+    """The split kernel of mla_decode alone (partials need mla_combine)."""
+    _decode_call("mla_decode_splitkv", q, kv_cache, kv_format, block_table, cache_seqlens,
+                 softmax_scale, causal, metadata, num_sm_parts, workspace, out, lse, err, stream)
 
 
 def mla_sparse_decode(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,

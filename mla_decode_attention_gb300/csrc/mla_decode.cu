@@ -83,12 +83,12 @@ int launch_split(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const SplitP
 
 using namespace mla;
 
-extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
-                          const int32_t* block_table, int64_t block_table_stride,
-                          const int32_t* cache_seqlens, int batch, int s_q, int h_q,
-                          float softmax_scale, int causal, const void* metadata, int num_sm_parts,
-                          void* workspace, void* out, float* lse, uint32_t* err,
-                          cudaStream_t stream) {
+extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_format,
+                                  int64_t num_pages, const int32_t* block_table,
+                                  int64_t block_table_stride, const int32_t* cache_seqlens,
+                                  int batch, int s_q, int h_q, float softmax_scale, int causal,
+                                  const void* metadata, int num_sm_parts, void* workspace,
+                                  void* out, float* lse, uint32_t* err, cudaStream_t stream) {
   int rc = check_common(batch, s_q, h_q, num_sm_parts);
   if (rc != MLA_OK) return rc;
   if (!q || !kv_cache || !block_table || !cache_seqlens || !metadata || !workspace || !out || !lse)
@@ -128,7 +128,19 @@ extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, in
   prm.n_hblk = n_hblk;
   prm.rows = rows;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
-  rc = launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);
+  return launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);
+}
+
+extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
+                          const int32_t* block_table, int64_t block_table_stride,
+                          const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                          float softmax_scale, int causal, const void* metadata, int num_sm_parts,
+                          void* workspace, void* out, float* lse, uint32_t* err,
+                          cudaStream_t stream) {
+  const int rc = mla_decode_splitkv(q, kv_cache, kv_format, num_pages, block_table,
+                                    block_table_stride, cache_seqlens, batch, s_q, h_q,
+                                    softmax_scale, causal, metadata, num_sm_parts, workspace, out,
+                                    lse, err, stream);
   if (rc != MLA_OK) return rc;
   return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, out, lse, stream, true);
 }
