@@ -116,6 +116,8 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   prm.block_table = block_table;
   prm.bt_stride = block_table_stride;
   prm.num_pages = num_pages;
+  prm.kv_rows = static_cast<const __nv_bfloat16*>(kv_cache);
+  prm.q = static_cast<const __nv_bfloat16*>(q);
   const int64_t ws_rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
   prm.ws_o = static_cast<float*>(workspace);
   prm.ws_lse = prm.ws_o + ws_rows * kDv;

@@ -215,7 +215,19 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Prefetch `bytes` (multiple of 16) of global memory into L2; no smem, no wait.
+__device__ __forceinline__ void prefetch_l2(const void* gptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------------ misc
+
+// Maximum of v over the 32 lanes of the warp, returned to every lane.
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -17,13 +17,14 @@
 // (the seesaw in the FlashMLA deep dive exists because WGMMA keeps O in
 // registers).
 //
-// Roles (416 threads):
-//   warp 0 lane 0  : producer, TMA loads of Q (once per piece) and of each
-//                    tile's 9 column chunks (two 64-token pages per chunk)
+// Roles (384 threads):
+//   warp 0 lane 0  : producer: TMA loads of Q (once per piece) and of each
+//                    tile's 9 column chunks (two 64-token pages per chunk),
+//                    plus L2 prefetches of the pages two tiles ahead
+//   warp 1         : TMEM allocation; lane 0 issues every MMA
 //   warps 4..7     : softmax warpgroup 0, query rows 0..31 of the block
 //   warps 8..11    : softmax warpgroup 1, query rows 32..63
-//   warp 12        : TMEM allocation and the single MMA-issuing thread
-//   warps 1..3     : idle
+//   warps 2..3     : idle
 //
 // Shared memory (1024-byte aligned): 9 KV chunk slots of [128 tok x 64 col]
 // bf16 (16 KB each, 128-byte swizzle), Q as 9 chunks of [64 rows x 64 col]
@@ -37,6 +38,7 @@
 #include <cstddef>
 
 #include "mla_decode.h"
+#include "mla_internal.h"
 #include "mla_ptx.cuh"
 #include "mla_schedule.cuh"
 
@@ -52,10 +54,12 @@ constexpr int kSmemSmall = kSmemQ + kChunks * kQChunkBytes;   // 221184
 constexpr int kNumBarriers = 2 * kChunks + 5;
 constexpr int kSmallBytes = 8 * kNumBarriers + 16 + 4 * 4 * 2 * 4 * 32;
 constexpr int kSmemBytes = kSmallBytes + kSmemSmall + 1024;   // + alignment slack
-constexpr int kThreads = 416;
+constexpr int kThreads = 384;
 constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kMmaWarp = 12;
+constexpr int kPageBytes = kPage * 576 * 2;   // 73728 contiguous bytes per bf16 page
+constexpr int kPrefetchTiles = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // O^T: 4 blocks of 64 columns
 constexpr uint32_t kTmemS = 256;   // S^T: 64 columns
@@ -72,7 +76,8 @@ struct SplitParams {
   const int32_t* indices;  // sparse: [n_seq, topk]
   int topk;
   int64_t s_kv;            // sparse: pool rows
-  const __nv_bfloat16* kv_rows;  // sparse: pool base
+  const __nv_bfloat16* kv_rows;  // dense: cache base (L2 prefetch); sparse: pool base
+  const __nv_bfloat16* q;        // query rows, for L2 prefetch of the next piece
   float* ws_o;
   float* ws_lse;
   __nv_bfloat16* out;
@@ -158,6 +163,43 @@ __device__ __forceinline__ void load_bcast32(const float* src, float (&dst)[32])
   }
 }
 
+// Iterates the (sequence, tile) pairs of one part in order.
+struct TileWalker {
+  PartCursor cur;
+  int q, t, t1;
+  bool valid;
+  __device__ void init(const int32_t* meta, int num_parts, int part) {
+    cur = part_cursor(meta, part);
+    int t0, split;
+    valid = next_piece(meta, num_parts, &cur, &q, &t0, &t1, &split);
+    t = t0;
+  }
+  __device__ void advance(const int32_t* meta, int num_parts) {
+    if (!valid) return;
+    if (t + 1 < t1) { ++t; return; }
+    int t0, split;
+    valid = next_piece(meta, num_parts, &cur, &q, &t0, &t1, &split);
+    t = t0;
+  }
+};
+
+// Physical page of logical page `pg` of the sequence, or -1 if out of range.
+__device__ __forceinline__ int32_t page_of(const SplitParams& p, int q, int pg) {
+  const int32_t keys = meta_seq(p.meta, p.num_parts, q)[kSKeys];
+  const int last = (keys - 1) / kPage;
+  const int32_t* bt_row = p.block_table + static_cast<int64_t>(q / p.s_q) * p.bt_stride;
+  const int32_t blk = bt_row[pg < last ? pg : last];
+  return (blk < 0 || static_cast<int64_t>(blk) >= p.num_pages) ? -1 : blk;
+}
+
+__device__ __forceinline__ void prefetch_tile(const SplitParams& p, const TileWalker& w) {
+  if (!w.valid) return;
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int32_t blk = page_of(p, w.q, 2 * w.t + h2);
+    if (blk >= 0) prefetch_l2(p.kv_rows + static_cast<int64_t>(blk) * (kPage * 576), kPageBytes);
+  }
+}
+
 template <KvMode kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_splitkv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -192,11 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.rows < kRowsPerCta) {
     // Rows [rows, 64) of every Q chunk are never written by TMA; zero them
     // once so the padded columns of S^T stay finite.
-    const int pad_bytes = (kRowsPerCta - p.rows) * 128;
-    for (int i = threadIdx.x; i < kChunks * pad_bytes / 16; i += kThreads) {
-      const int c = i / (pad_bytes / 16), k = i % (pad_bytes / 16);
-      const uint32_t a = q_base + c * kQChunkBytes + p.rows * 128 + k * 16;
-      st_shared_v4(a, 0u, 0u, 0u, 0u);
+    const int pad_units = (kRowsPerCta - p.rows) * 8;
+    for (int i = threadIdx.x; i < kChunks * pad_units; i += kThreads) {
+      const int c = i / pad_units, k = i % pad_units;
+      st_shared_v4(q_base + c * kQChunkBytes + p.rows * 128 + k * 16, 0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
   }
@@ -219,6 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
+      const bool do_prefetch = (hb == 0);
+      TileWalker ahead;
+      ahead.init(meta, p.num_parts, part);
+      for (int k = 0; k <= kPrefetchTiles; ++k) {  // tiles #0..#2 of this part
+        if (do_prefetch && k > 0) prefetch_tile(p, ahead);
+        ahead.advance(meta, p.num_parts);
+      }
       PartCursor cur = part_cursor(meta, part);
       int q, t0, t1, split;
       uint32_t tile_ctr = 0, item_ctr = 0;
@@ -233,17 +281,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q_row = q * p.h + hb * kRowsPerCta;
         for (int c = 0; c < kChunks; ++c)
           tma_load_2d(q_base + c * kQChunkBytes, &tm_q, c * 64, q_row, smem_u32(&sm->q_full), pol_q);
-        const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
-        const int b = q / p.s_q;
-        const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-        const int last_page = (keys - 1) / kPage;
+        {  // the next piece's query rows into L2
+          PartCursor nc = cur;
+          int nq, nt0, nt1, ns;
+          if (next_piece(meta, p.num_parts, &nc, &nq, &nt0, &nt1, &ns))
+            prefetch_l2(p.q + (static_cast<int64_t>(nq) * p.h + hb * kRowsPerCta) * 576,
+                        p.rows * 1152);
+        }
         for (int t = t0; t < t1 && ok; ++t) {
+          if (do_prefetch) prefetch_tile(p, ahead);
+          ahead.advance(meta, p.num_parts);
           int32_t y[2];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const int pg = min(2 * t + h2, last_page);
-            int32_t blk = bt_row[pg];
-            if (blk < 0 || static_cast<int64_t>(blk) >= p.num_pages) {
+            int32_t blk = page_of(p, q, 2 * t + h2);
+            if (blk < 0) {
               if (p.err) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
               blk = static_cast<int32_t>(p.num_pages);  // out of range: TMA fills zeros
             }
@@ -282,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q, t0, t1, split;
       uint32_t tile_ctr = 0, item_ctr = 0;
       bool ok = true;
+      const uint32_t p_base = kv_base + 8 * kChunkBytes;
       while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
         ok = mbar_wait(smem_u32(&sm->q_full), item_ctr & 1, abort_flag, p.err);
         if (!ok) break;
@@ -308,7 +361,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(smem_u32(&sm->p_full), par, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t p_base = kv_base + 8 * kChunkBytes;
           for (int m = 0; m < 4; ++m) {
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
@@ -320,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(&sm->empty[2 * m + 1]));
           }
           mma_commit(smem_u32(&sm->empty[8]));
-          mma_commit(smem_u32(&sm->o_done));
+          if (t == t1 - 1) mma_commit(smem_u32(&sm->o_done));
           ++tile_ctr;
         }
         ++item_ctr;
@@ -328,26 +380,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
     // ===================================================== softmax / epilogue
+    // Thread = one token row r of the tile (TMEM lane) x the 32 query rows of
+    // its warpgroup (TMEM columns).  Column max over the 128 tokens: warp
+    // redux, then the four warps through shared memory.  Sums stay per lane
+    // (rescaled like O) until the piece ends.
     const int g = (warp - kSoftmaxWarp0) >> 2;  // row half: rows 32g .. 32g+31
     const int wq = warp & 3;                    // TMEM lane quarter
     const int r = wq * 32 + lane;               // token row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_off + kTmemS + 32 * g;
+    const uint32_t t_o = tmem + lane_off + kTmemO + 32 * g;
     const uint32_t p_slot = kv_base + 8 * kChunkBytes;
     const float NEG_INF = -INFINITY;
+    float* red_w = &sm->red_max[g][wq][0];
+    float* bc_m = &sm->bcast[g][wq][0];
+    float* bc_a = &sm->bcast2[g][wq][0];
     PartCursor cur = part_cursor(meta, part);
     int q, t0, t1, split;
-    uint32_t tile_ctr = 0;
+    uint32_t tile_ctr = 0, item_ctr = 0;
     bool ok = true;
     while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
       const int32_t* srec = meta_seq(meta, p.num_parts, q);
       const int32_t keys = srec[kSKeys];
       const int32_t* idx_row = (kMode == KvMode::kSparseBf16)
                                    ? p.indices + static_cast<int64_t>(q) * p.topk : nullptr;
-      float m_run = NEG_INF, l_run = 0.f;  // for row 32g + lane
+      float m_run = NEG_INF;  // running max (log2 units) of row 32g + lane
+      float lp[32];           // this lane's share of the running sums
+#pragma unroll
+      for (int i = 0; i < 32; ++i) lp[i] = 0.f;
       for (int t = t0; t < t1; ++t) {
-        const uint32_t par = tile_ctr & 1;
-        ok = mbar_wait(smem_u32(&sm->s_full), par, abort_flag, p.err);
+        ok = mbar_wait(smem_u32(&sm->s_full), tile_ctr & 1, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
         float x[32];
@@ -361,23 +423,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = valid ? x[i] * p.scale_log2 : NEG_INF;
-        // row max over the 128 tokens
-        float mx = warp_reduce_scatter32<true>(x, lane);
-        sm->red_max[g][wq][lane] = mx;
-        named_barrier_sync(1 + g, 128);
-        mx = fmaxf(fmaxf(sm->red_max[g][0][lane], sm->red_max[g][1][lane]),
-                   fmaxf(sm->red_max[g][2][lane], sm->red_max[g][3][lane]));
-        const float m_new = fmaxf(m_run, mx);
-        const float m_use = (m_new == NEG_INF) ? 0.f : m_new;
-        const float alpha = fast_exp2(m_run - m_use);  // 0 for the first tile
-        sm->bcast[g][wq][lane] = m_use;
-        __syncwarp();
-        float mb[32];
-        load_bcast32(&sm->bcast[g][wq][0], mb);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = fast_exp2(x[i] - mb[i]);
-        float sum = warp_reduce_scatter32<false>(x, lane);
-        sm->red_sum[g][wq][lane] = sum;
+        for (int i = 0; i < 32; i += 4) {
+          const float w0 = warp_max_f32(x[i]), w1 = warp_max_f32(x[i + 1]);
+          const float w2 = warp_max_f32(x[i + 2]), w3 = warp_max_f32(x[i + 3]);
+          if (lane == 0) *reinterpret_cast<float4*>(red_w + i) = make_float4(w0, w1, w2, w3);
+        }
+        named_barrier_sync(1 + g, 128);
+        const float mt = fmaxf(fmaxf(sm->red_max[g][0][lane], sm->red_max[g][1][lane]),
+                               fmaxf(sm->red_max[g][2][lane], sm->red_max[g][3][lane]));
+        const float m_new = fmaxf(m_run, mt);
+        const float m_use = (m_new == NEG_INF) ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - m_use);  // 0 on the first tile
+        bc_m[lane] = m_use;
+        bc_a[lane] = alpha;
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(bc_m + i);
+          const float4 a4 = *reinterpret_cast<const float4*>(bc_a + i);
+          x[i] = fast_exp2(x[i] - m4.x);
+          x[i + 1] = fast_exp2(x[i + 1] - m4.y);
+          x[i + 2] = fast_exp2(x[i + 2] - m4.z);
+          x[i + 3] = fast_exp2(x[i + 3] - m4.w);
+          lp[i] = fmaf(lp[i], a4.x, x[i]);
+          lp[i + 1] = fmaf(lp[i + 1], a4.y, x[i + 1]);
+          lp[i + 2] = fmaf(lp[i + 2], a4.z, x[i + 2]);
+          lp[i + 3] = fmaf(lp[i + 3], a4.w, x[i + 3]);
+        }
         // P^T row r, rows 32g..32g+31 -> 16-byte units 4g..4g+3 (swizzled)
         const uint32_t prow = p_slot + r * 128;
 #pragma unroll
@@ -389,51 +462,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                        pack_bf16x2(x[8 * cu + 6], x[8 * cu + 7]));
         }
         fence_proxy_async_smem();
-        named_barrier_sync(1 + g, 128);
-        sum = (sm->red_sum[g][0][lane] + sm->red_sum[g][1][lane]) +
-              (sm->red_sum[g][2][lane] + sm->red_sum[g][3][lane]);
-        l_run = alpha * l_run + sum;
-        m_run = m_new;
-        if (t != t0) {
-          // PV of the previous tile must be complete before O^T is rescaled
-          ok = mbar_wait(smem_u32(&sm->o_done), par ^ 1, abort_flag, p.err);
-          if (!ok) break;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            sm->bcast2[g][wq][lane] = alpha;
-            __syncwarp();
-            float ab[32];
-            load_bcast32(&sm->bcast2[g][wq][0], ab);
+        // PV of the previous tile completed before s_full of this tile fired
+        // (tcgen05 operations of one thread complete in order), so O^T can be
+        // rescaled now.
+        if (t != t0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
-              float o[32];
-              const uint32_t t_o = tmem + lane_off + kTmemO + 64 * m + 32 * g;
-              tmem_ld32(t_o, o);
-              tmem_wait_ld();
+          for (int m = 0; m < 4; ++m) {
+            float o[32];
+            tmem_ld32(t_o + 64 * m, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= ab[i];
-              tmem_st32(t_o, o);
+            for (int i = 0; i < 32; i += 4) {
+              const float4 a4 = *reinterpret_cast<const float4*>(bc_a + i);
+              o[i] *= a4.x; o[i + 1] *= a4.y; o[i + 2] *= a4.z; o[i + 3] *= a4.w;
             }
-            tmem_wait_st();
+            tmem_st32(t_o + 64 * m, o);
           }
+          tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
+        m_run = m_new;
         ++tile_ctr;
       }
       if (!ok) break;
       // ---- epilogue: O^T / l -> out (one split) or fp32 partial
-      ok = mbar_wait(smem_u32(&sm->o_done), (tile_ctr - 1) & 1, abort_flag, p.err);
+      float lsum = warp_reduce_scatter32<false>(lp, lane);  // this warp's tokens, row 32g+lane
+      sm->red_sum[g][wq][lane] = lsum;
+      named_barrier_sync(1 + g, 128);
+      lsum = (sm->red_sum[g][0][lane] + sm->red_sum[g][1][lane]) +
+             (sm->red_sum[g][2][lane] + sm->red_sum[g][3][lane]);
+      ok = mbar_wait(smem_u32(&sm->o_done), item_ctr & 1, abort_flag, p.err);
       if (!ok) break;
       tc_fence_after();
-      const bool has = l_run > 0.f;
-      const float inv_l = has ? 1.f / l_run : 0.f;
-      const float lse_v = has ? (m_run + __log2f(l_run)) * 0.69314718055994531f : NEG_INF;
-      sm->bcast2[g][wq][lane] = inv_l;
+      const bool has = lsum > 0.f;
+      const float inv_l = has ? 1.f / lsum : 0.f;
+      const float lse_v = has ? (m_run + __log2f(lsum)) * 0.69314718055994531f : NEG_INF;
+      bc_a[lane] = inv_l;
       __syncwarp();
       float il[32];
-      load_bcast32(&sm->bcast2[g][wq][0], il);
+      load_bcast32(bc_a, il);
       const bool final_out = srec[kSNSplits] == 1;
       const int row0 = hb * kRowsPerCta + 32 * g;  // first head of this warpgroup
       const int split_row = srec[kSSplitOff] + split;
@@ -441,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
         float o[32];
-        tmem_ld32(tmem + lane_off + kTmemO + 64 * m + 32 * g, o);
+        tmem_ld32(t_o + 64 * m, o);
         tmem_wait_ld();
         const int d = 128 * m + 32 * wq + lane;
         if (final_out) {
@@ -462,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           p.ws_lse[static_cast<int64_t>(split_row) * p.h + row0 + lane] = lse_v;
       }
+      ++item_ctr;
     }
   }
 
