@@ -192,6 +192,42 @@ int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv, const int32_t
                       const void* metadata, int num_sm_parts, void* workspace, void* out,
                       float* lse, uint32_t* err, cudaStream_t stream);
 
+/* Size of the device scratch array that mla_decode_noalloc uses (40 MiB). */
+#define MLA_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
+
+/*
+ * mla_decode without caller-provided scratch.  The source pages have no
+ * counterpart to this entry point; it exists for callers that may launch
+ * kernels but may not allocate device memory where they call it, such as an
+ * inference engine's plugin enqueue hook that is handed only input/output
+ * pointers and a stream, or a serving loop that must not hit cudaMalloc and
+ * its implicit synchronisation.
+ *
+ * Arguments and layouts are those of mla_decode minus metadata, num_sm_parts
+ * and workspace: the schedule and the split workspace go to a library-owned
+ * device array of MLA_NOALLOC_SCRATCH_BYTES, and num_sm_parts is the
+ * current device's default (mla_num_sm_parts).  Nothing is allocated and the
+ * caller still passes every input and output.
+ *
+ *  - Limit: shapes whose metadata (rounded up to 256 bytes) plus workspace
+ *    (mla_metadata_size + mla_workspace_size) exceed the array are rejected
+ *    with MLA_ERR_SHAPE before any launch; mla_last_error() says why.  The
+ *    b=64, s_q=1, h_q=128 decode fits; use mla_decode for larger batches.
+ *  - The array exists once per device that loads this library and stays
+ *    reserved until the process exits.
+ *  - The first call on a device looks up the array's address on that device
+ *    (with the device current) and caches it; make that first call before
+ *    any stream capture.
+ *  - Every call shares the array: calls that overlap on the GPU (other
+ *    streams, other host threads on the same device) race and corrupt each
+ *    other's results.  Nothing in it needs clearing between calls.
+ */
+int mla_decode_noalloc(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
+                       const int32_t* block_table, int64_t block_table_stride,
+                       const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                       float softmax_scale, int causal, void* out, float* lse, uint32_t* err,
+                       cudaStream_t stream);
+
 /*
  * LSE combine of split partials (DeepGEMM & FlashMLA article, section 7:
  * m = max m_i, l = sum l_i e^(m_i - m), o = sum o_i l_i e^(m_i - m) / l; here

@@ -47,6 +47,8 @@ _SIGS = {
                         _vp, _vp, _vp, _vp]),
     "mla_decode_splitkv": (_i, [_vp, _vp, _i, _i64, _vp, _i64, _vp, _i, _i, _i, _f, _i, _vp, _i,
                                 _vp, _vp, _vp, _vp, _vp]),
+    "mla_decode_noalloc": (_i, [_vp, _vp, _i, _i64, _vp, _i64, _vp, _i, _i, _i, _f, _i, _vp, _vp,
+                                _vp, _vp]),
     "mla_sparse_decode": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _i, _vp, _vp, _vp,
                                _vp, _vp]),
     "mla_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
@@ -58,7 +60,7 @@ _lib = None
 class MlaError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        detail = lib().mla_last_error().decode() if status == -5 else ""
+        detail = lib().mla_last_error().decode() if status in (-2, -5) else ""
         super().__init__(f"{fn} failed with status {status}: {status_string(status)}"
                          + (f" [{detail}]" if detail else ""))
 
@@ -193,6 +195,29 @@ def mla_decode_splitkv(q, kv_cache, kv_format, block_table, cache_seqlens, softm
     """The split kernel of mla_decode alone (partials need mla_combine)."""
     _decode_call("mla_decode_splitkv", q, kv_cache, kv_format, block_table, cache_seqlens,
                  softmax_scale, causal, metadata, num_sm_parts, workspace, out, lse, err, stream)
+
+
+def mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, kv_format: int,
+                       block_table: torch.Tensor, cache_seqlens: torch.Tensor,
+                       softmax_scale: float, causal: bool, out: torch.Tensor, lse: torch.Tensor,
+                       err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """mla_decode with the schedule and split workspace in the library's fixed
+    device scratch array: the caller passes only inputs and outputs.  Calls
+    sharing that array must not overlap on the GPU."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(kv_cache, torch.bfloat16 if kv_format == MLA_KV_BF16 else torch.uint8, "kv_cache")
+    _dev(cache_seqlens, torch.int32, "cache_seqlens")
+    _dev(out, torch.bfloat16, "out")
+    _dev(lse, torch.float32, "lse")
+    if not block_table.is_cuda or block_table.dtype != torch.int32 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be a CUDA int32 tensor with unit column stride")
+    if err is not None:
+        _dev(err, torch.int32, "err")
+    b, s_q, h, d = q.shape
+    _check("mla_decode_noalloc", lib().mla_decode_noalloc(
+        _ptr(q), _ptr(kv_cache), kv_format, kv_cache.shape[0], _ptr(block_table),
+        block_table.stride(0), _ptr(cache_seqlens), b, s_q, h, float(softmax_scale),
+        int(bool(causal)), _ptr(out), _ptr(lse), _ptr(err), _stream(stream)))
 
 
 def mla_sparse_decode(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,
