@@ -152,8 +152,44 @@ extern "C" int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv,
                                  float softmax_scale, const void* metadata, int num_sm_parts,
                                  void* workspace, void* out, float* lse, uint32_t* err,
                                  cudaStream_t stream) {
-  (void)q; (void)kv; (void)s_kv; (void)indices; (void)topk; (void)batch; (void)s_q; (void)h_q;
-  (void)softmax_scale; (void)metadata; (void)num_sm_parts; (void)workspace; (void)out;
-  (void)lse; (void)err; (void)stream;
-  return MLA_ERR_UNSUPPORTED;
+  int rc = check_common(batch, s_q, h_q, num_sm_parts);
+  if (rc != MLA_OK) return rc;
+  if (!q || !kv || !indices || !metadata || !workspace || !out || !lse) return MLA_ERR_NULL;
+  if (topk <= 0 || s_kv <= 0 || s_kv > (int64_t{1} << 31) - 1) return MLA_ERR_SHAPE;
+  if (!(softmax_scale > 0.f) || !(softmax_scale < 1e30f)) return MLA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(metadata) || !aligned16(workspace) ||
+      !aligned16(out))
+    return MLA_ERR_ALIGN;
+
+  const int n_seq = batch * s_q;
+  const int rows = h_q < kRowsPerCta ? h_q : kRowsPerCta;
+  CUtensorMap tm_q, tm_kv;
+  if (!make_rows_map(&tm_q, q, static_cast<uint64_t>(n_seq) * h_q, kDqk * 2, rows))
+    return record_error("cuTensorMapEncodeTiled failed for q", MLA_ERR_CUDA);
+  // one-row boxes: each tile::gather4 fetches four arbitrary pool rows
+  if (!make_rows_map(&tm_kv, kv, static_cast<uint64_t>(s_kv), kDqk * 2, 1))
+    return record_error("cuTensorMapEncodeTiled failed for kv", MLA_ERR_CUDA);
+
+  SplitParams prm = {};
+  prm.meta = static_cast<const int32_t*>(metadata);
+  prm.indices = indices;
+  prm.topk = topk;
+  prm.s_kv = s_kv;
+  prm.kv_rows = static_cast<const __nv_bfloat16*>(kv);
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  const int64_t ws_rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
+  prm.ws_o = static_cast<float*>(workspace);
+  prm.ws_lse = prm.ws_o + ws_rows * kDv;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.err = err;
+  prm.h = h_q;
+  prm.s_q = s_q;
+  prm.num_parts = num_sm_parts;
+  prm.n_hblk = head_blocks(h_q);
+  prm.rows = rows;
+  prm.scale_log2 = softmax_scale * 1.4426950408889634f;
+  rc = launch_split<KvMode::kSparseBf16>(tm_q, tm_kv, prm, stream);
+  if (rc != MLA_OK) return rc;
+  return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, out, lse, stream, true);
 }

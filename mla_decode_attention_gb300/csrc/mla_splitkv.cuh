@@ -60,6 +60,11 @@ constexpr int kMmaWarp = 1;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kPageBytes = kPage * 576 * 2;   // 73728 contiguous bytes per bf16 page
 constexpr int kPrefetchTiles = 2;
+// With two head blocks per cluster, each CTA loads one 64-token page half of
+// every chunk and multicasts it to both CTAs, so every KV byte leaves L2 once
+// per cluster and each CTA issues half the TMA boxes.
+constexpr bool kClusterMulticast = false;
+constexpr bool kPrefetchKv = false;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // O^T: 4 blocks of 64 columns
 constexpr uint32_t kTmemS = 256;   // S^T: 64 columns
@@ -218,10 +223,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* meta = p.meta;
 
   // ---- setup: barriers, TMEM, zeroed padding rows of Q
+  const bool multicast = kClusterMulticast && p.n_hblk == 2;
   if (threadIdx.x == 0) {
     for (int c = 0; c < kChunks; ++c) {
       mbar_init(smem_u32(&sm->full[c]), 1);
-      mbar_init(smem_u32(&sm->empty[c]), 1);
+      // a slot is free once the MMA threads of every CTA writing into it
+      // have released it
+      mbar_init(smem_u32(&sm->empty[c]), multicast ? 2 : 1);
     }
     mbar_init(smem_u32(&sm->q_full), 1);
     mbar_init(smem_u32(&sm->q_empty), 1);
@@ -251,16 +259,78 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (multicast) cluster_sync();  // peers' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   volatile uint32_t* abort_flag = &sm->abort;
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp && kMode == KvMode::kSparseBf16) {
+    // ===================================================== producer (gather)
+    // Lane L gathers rows 4L..4L+3 of each 128-row tile with one tile::gather4
+    // per column chunk; lane 0 owns the barriers.  Invalid slots (-1, out of
+    // range, past topk) fetch pool row 0 and are masked by the softmax.
+    PartCursor cur = part_cursor(meta, part);
+    int q, t0, t1, split;
+    uint32_t tile_ctr = 0, item_ctr = 0;
+    int32_t issued[kChunks];  // tile counter of each slot's latest gather, -1 = none
+    for (int c = 0; c < kChunks; ++c) issued[c] = -1;
+    bool ok = true;
+    while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+      if (lane == 0) {
+        ok = mbar_wait(smem_u32(&sm->q_empty), (item_ctr & 1) ^ 1, abort_flag, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(smem_u32(&sm->q_full), kChunks * p.rows * 128);
+          const int q_row = q * p.h + hb * kRowsPerCta;
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(q_base + c * kQChunkBytes, &tm_q, c * 64, q_row, smem_u32(&sm->q_full),
+                        l2_policy_evict_last());
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
+      for (int t = t0; t < t1 && ok; ++t) {
+        int32_t rid[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int slot = t * kTileTokens + 4 * lane + i;
+          const int32_t id = slot < p.topk ? idx_row[slot] : -1;
+          const bool valid = id >= 0 && static_cast<int64_t>(id) < p.s_kv;
+          if (!valid && id != -1 && p.err) atomicOr(p.err, MLA_DEVERR_BAD_INDEX);
+          rid[i] = valid ? id : 0;
+        }
+        const uint32_t par = (tile_ctr & 1) ^ 1;
+        for (int c = 0; c < kChunks; ++c) {
+          if (lane == 0) {
+            ok = mbar_wait(smem_u32(&sm->empty[c]), par, abort_flag, p.err);
+            if (ok) mbar_arrive_expect_tx(smem_u32(&sm->full[c]), kChunkBytes);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tma_gather4(kv_base + c * kChunkBytes + 4 * lane * 128, &tm_kv, c * 64, rid[0], rid[1],
+                      rid[2], rid[3], smem_u32(&sm->full[c]));
+          issued[c] = static_cast<int32_t>(tile_ctr);
+        }
+        ++tile_ctr;
+      }
+      ++item_ctr;
+    }
+    if (!ok && lane == 0) {
+      // Let gathers already in flight land before the CTA exits.
+      for (int c = 0; c < kChunks; ++c) {
+        if (issued[c] < 0) continue;
+        const uint64_t t_start = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&sm->full[c]), static_cast<uint32_t>(issued[c]) & 1u) &&
+               globaltimer_ns() - t_start < 1000000ull) {
+        }
+      }
+    }
+  } else if (warp == kProducerWarp) {
     // ===================================================== producer (TMA)
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
-      const bool do_prefetch = (hb == 0);
+      const bool do_prefetch = kPrefetchKv && hb == 0;
       TileWalker ahead;
       ahead.init(meta, p.num_parts, part);
       for (int k = 0; k <= kPrefetchTiles; ++k) {  // tiles #0..#2 of this part
@@ -308,8 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bar = smem_u32(&sm->full[c]);
             mbar_arrive_expect_tx(bar, kChunkBytes);
             const uint32_t dst = kv_base + c * kChunkBytes;
-            tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol_kv);
-            tma_load_2d(dst + kChunkBytes / 2, &tm_kv, c * 64, y[1], bar, pol_kv);
+            if (multicast) {
+              tma_load_2d_multicast(dst + hb * (kChunkBytes / 2), &tm_kv, c * 64, y[hb], bar,
+                                    static_cast<uint16_t>(0x3), pol_kv);
+            } else {
+              tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol_kv);
+              tma_load_2d(dst + kChunkBytes / 2, &tm_kv, c * 64, y[1], bar, pol_kv);
+            }
             issued[c] = static_cast<int32_t>(tile_ctr);
           }
           ++tile_ctr;
@@ -368,10 +443,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t bp = sw128_desc(p_base + 2048 * s, kChunkBytes, 1024);
               mma_bf16_ss(tmem + kTmemO + 64 * m, a, bp, kIdescPV, (t != t0 || s != 0) ? 1u : 0u);
             }
-            mma_commit(smem_u32(&sm->empty[2 * m]));
-            mma_commit(smem_u32(&sm->empty[2 * m + 1]));
+            if (multicast) {
+              mma_commit_multicast(smem_u32(&sm->empty[2 * m]), 0x3);
+              mma_commit_multicast(smem_u32(&sm->empty[2 * m + 1]), 0x3);
+            } else {
+              mma_commit(smem_u32(&sm->empty[2 * m]));
+              mma_commit(smem_u32(&sm->empty[2 * m + 1]));
+            }
           }
-          mma_commit(smem_u32(&sm->empty[8]));
+          if (multicast) mma_commit_multicast(smem_u32(&sm->empty[8]), 0x3);
+          else mma_commit(smem_u32(&sm->empty[8]));
           if (t == t1 - 1) mma_commit(smem_u32(&sm->o_done));
           ++tile_ctr;
         }
@@ -538,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown
   tc_fence_before();
   __syncthreads();
+  if (multicast) cluster_sync();  // no peer still writes into this CTA's smem
   pdl_launch_dependents();
   if (warp == kMmaWarp) {
     tc_fence_after();

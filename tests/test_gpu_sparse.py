@@ -1,0 +1,146 @@
+"""GPU parity of DSA top-k sparse decode against the fp64 oracle (through the C ABI).
+
+Order invariance follows the flash-attention sparse-MLA article's test design:
+the same top-k set with the dominant key first and last; each order's
+coherent row gain (<out - ref, ref> / <ref, ref> per row) must stay within 2x
+that of the ideal bf16 output.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_decode_attention_gb300 import binding, workloads
+from tests._util import assert_parity, bf16_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    from mla_decode_attention_gb300 import build
+    if not os.path.exists(binding.LIB_PATH):
+        build.build()
+    return binding.lib()
+
+
+def run_sparse(inp, num_sm_parts=None):
+    q = inp["q"].to(DEV)
+    kv = inp["kv"].to(DEV)
+    idx = inp["indices"].to(DEV)
+    b, s_q, h, _ = q.shape
+    topk = idx.shape[-1]
+    buf = binding.DecodeBuffers(b, s_q, h, DEV, num_sm_parts)
+    binding.mla_get_metadata(None, b, s_q, False, topk, buf.num_sm_parts, buf.metadata)
+    binding.mla_sparse_decode(q, kv, idx, inp["softmax_scale"], buf.metadata, buf.num_sm_parts,
+                              buf.workspace, buf.out, buf.lse, buf.err)
+    torch.cuda.synchronize()
+    return buf.out.float().cpu().numpy(), buf.lse.cpu().numpy(), int(buf.err.item())
+
+
+def oracle_sparse(inp, rows=None):
+    return oracle.sparse_decode(bf16_np(inp["q"]), bf16_np(inp["kv"]), inp["indices"].numpy(),
+                                inp["softmax_scale"], rows)
+
+
+def small(seed, b=2, s_q=1, h=16, s_kv=1000, topk=300, invalid=17):
+    w = workloads.Workload("sp", "sparse", b=b, s_q=s_q, h=h, s_kv=s_kv, topk=topk,
+                           invalid_per_row=invalid, seed=seed)
+    return workloads.make_inputs(w)
+
+
+def test_small_sparse_parity():
+    inp = small(31)
+    out, lse, err = run_sparse(inp)
+    ref_o, ref_l = oracle_sparse(inp)
+    assert_parity(out, ref_o, lse, ref_l, "sparse small")
+    assert err == 0
+
+
+@pytest.mark.parametrize("topk,parts", [(1, None), (127, None), (129, 3), (640, 1)])
+def test_sparse_ragged_topk(topk, parts):
+    inp = small(32 + topk, b=3, h=64, s_kv=3000, topk=topk, invalid=min(5, topk - 1))
+    out, lse, err = run_sparse(inp, parts)
+    ref_o, ref_l = oracle_sparse(inp)
+    assert_parity(out, ref_o, lse, ref_l, f"sparse topk={topk}")
+
+
+def test_sparse_h128_peaked_rows_and_s_q2():
+    inp = small(40, b=3, s_q=2, h=128, s_kv=9000, topk=1000, invalid=50)
+    out, lse, err = run_sparse(inp)
+    ref_o, ref_l = oracle_sparse(inp)
+    assert_parity(out, ref_o, lse, ref_l, "sparse h128")
+
+
+def _row_gain(out, ref):
+    o = out.reshape(-1, out.shape[-1])
+    r = ref.reshape(-1, ref.shape[-1])
+    return np.sum((o - r) * r, axis=1) / np.sum(r * r, axis=1)
+
+
+def test_sparse_index_order_invariance_row_gain():
+    inp = small(41, b=2, h=128, s_kv=20000, topk=2048, invalid=0)
+    ref_o, ref_l = oracle_sparse(inp)
+    ideal = torch.from_numpy(ref_o).to(torch.bfloat16).double().numpy()
+    floor = np.sqrt(np.mean(_row_gain(ideal, ref_o) ** 2))
+    first = inp
+    last = dict(inp)
+    idx = inp["indices"].clone()
+    last["indices"] = torch.cat([idx[..., 1:], idx[..., :1]], dim=-1)  # dominant key last
+    for name, case in (("dominant first", first), ("dominant last", last)):
+        out, lse, err = run_sparse(case)
+        assert_parity(out, ref_o, lse, ref_l, name)
+        gain = np.sqrt(np.mean(_row_gain(out, ref_o) ** 2))
+        assert gain <= 2.0 * floor + 1e-6, (name, gain, floor)
+
+
+def test_sparse_bad_and_all_invalid_indices():
+    inp = small(42, b=2, h=32, s_kv=500, topk=200, invalid=3)
+    inp["indices"][0, 0, 5] = 500          # == s_kv: out of range
+    inp["indices"][0, 0, 9] = -7
+    inp["indices"][1, 0, :] = -1           # nothing valid
+    out, lse, err = run_sparse(inp)
+    assert err & binding.MLA_DEVERR_BAD_INDEX
+    ref_o, ref_l = oracle_sparse(inp)
+    assert_parity(out[0], ref_o[0], lse[0], ref_l[0], "bad indices skipped")
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
+
+
+def test_dense_equals_sparse_on_the_same_rows():
+    w = workloads.Workload("ds", "dense", b=2, s_q=1, h=128, seqlens=(700, 129), extra_pages=4,
+                           seed=43)
+    inp = workloads.make_inputs(w)
+    q = inp["q"].to(DEV)
+    kv = inp["kv_cache"].to(DEV)
+    bt, sl = inp["block_table"].to(DEV), inp["cache_seqlens"].to(DEV)
+    buf = binding.DecodeBuffers(2, 1, 128, DEV)
+    binding.mla_get_metadata(sl, 2, 1, True, 0, buf.num_sm_parts, buf.metadata)
+    binding.mla_decode(q, kv, binding.MLA_KV_BF16, bt, sl, inp["softmax_scale"], True,
+                       buf.metadata, buf.num_sm_parts, buf.workspace, buf.out, buf.lse)
+    torch.cuda.synchronize()
+    dense_o, dense_l = buf.out.float().cpu().numpy(), buf.lse.cpu().numpy()
+    topk = 700
+    idx = torch.full((2, 1, topk), -1, dtype=torch.int32)
+    btn = inp["block_table"].numpy()
+    for b, L in enumerate((700, 129)):
+        t = np.arange(L)
+        idx[b, 0, :L] = torch.from_numpy((btn[b][t // 64] * 64 + t % 64).astype(np.int32))
+    sp = dict(q=inp["q"], kv=inp["kv_cache"].reshape(-1, 576), indices=idx,
+              softmax_scale=inp["softmax_scale"])
+    out, lse, err = run_sparse(sp)
+    assert_parity(out, dense_o, lse, dense_l, "sparse vs dense (GPU)")
+
+
+def test_full_size_dsa_sampled_rows():
+    w = workloads.WORKLOADS["dsa"]
+    inp = workloads.make_inputs(w)
+    out, lse, err = run_sparse(inp)
+    rows = [(0, 0), (9, 0), (33, 0), (63, 0)]
+    ref_o, ref_l = oracle_sparse(inp, rows=rows)
+    for b, j in rows:
+        assert_parity(out[b, j], ref_o[b, j], lse[b, :, j], ref_l[b, :, j], f"dsa row {b}")
+    assert err == 0 and np.all(np.isfinite(out))
