@@ -42,6 +42,21 @@ bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t str
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor [rows, cols] whose rows start `stride_bytes` apart; boxes of
+// [box_rows x 64 columns] with 128-byte swizzle.
+bool make_strided_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                      uint64_t stride_bytes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), rows};
+  const cuuint64_t strides[1] = {stride_bytes};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <KvMode kMode>
 int configure_kernel() {
   static int state = 0;  // 0 unset, 1 ok, -1 failed
@@ -93,7 +108,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   if (rc != MLA_OK) return rc;
   if (!q || !kv_cache || !block_table || !cache_seqlens || !metadata || !workspace || !out || !lse)
     return MLA_ERR_NULL;
-  if (kv_format != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
+  if (kv_format != MLA_KV_BF16 && kv_format != MLA_KV_FP8_656) return MLA_ERR_UNSUPPORTED;
   if (num_pages <= 0 || num_pages > (int64_t{1} << 25) || block_table_stride <= 0)
     return MLA_ERR_SHAPE;
   if (!(softmax_scale > 0.f) || !(softmax_scale < 1e30f)) return MLA_ERR_SHAPE;
@@ -108,8 +123,18 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   CUtensorMap tm_q, tm_kv;
   if (!make_rows_map(&tm_q, q, static_cast<uint64_t>(n_seq) * h_q, kDqk * 2, rows))
     return record_error("cuTensorMapEncodeTiled failed for q", MLA_ERR_CUDA);
-  if (!make_rows_map(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kDqk * 2, kPage))
-    return record_error("cuTensorMapEncodeTiled failed for kv_cache", MLA_ERR_CUDA);
+  const bool fp8 = kv_format == MLA_KV_FP8_656;
+  if (!fp8) {
+    if (!make_rows_map(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kDqk * 2, kPage))
+      return record_error("cuTensorMapEncodeTiled failed for kv_cache", MLA_ERR_CUDA);
+  } else {
+    // the bf16 RoPE tail of every 656-byte token: 64 columns at byte 528,
+    // row stride 656 bytes (both multiples of 16)
+    const void* rope = static_cast<const uint8_t*>(kv_cache) + kFp8RopeOffset;
+    if (!make_strided_map(&tm_kv, rope, static_cast<uint64_t>(num_pages) * kPage, 64,
+                          kFp8TokenBytes, kPage))
+      return record_error("cuTensorMapEncodeTiled failed for the FP8 RoPE columns", MLA_ERR_CUDA);
+  }
 
   SplitParams prm = {};
   prm.meta = static_cast<const int32_t*>(metadata);
@@ -117,6 +142,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   prm.bt_stride = block_table_stride;
   prm.num_pages = num_pages;
   prm.kv_rows = static_cast<const __nv_bfloat16*>(kv_cache);
+  prm.kv_fp8 = static_cast<const uint8_t*>(kv_cache);
   prm.q = static_cast<const __nv_bfloat16*>(q);
   const int64_t ws_rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
   prm.ws_o = static_cast<float*>(workspace);
@@ -130,7 +156,8 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   prm.n_hblk = n_hblk;
   prm.rows = rows;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
-  return launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);
+  return fp8 ? launch_split<KvMode::kPagedFp8>(tm_q, tm_kv, prm, stream)
+             : launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);
 }
 
 extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,

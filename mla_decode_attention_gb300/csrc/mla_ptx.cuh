@@ -260,6 +260,21 @@ __device__ __forceinline__ void prefetch_l2(const void* gptr, uint32_t bytes) {
 
 // ------------------------------------------------------------------ misc
 
+// Two float8 e4m3 values (low byte first) -> two exact fp16 values.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v) {
+  float2 f;
+  asm("{ .reg .f16 lo, hi; mov.b32 {lo, hi}, %2; cvt.f32.f16 %0, lo; cvt.f32.f16 %1, hi; }"
+      : "=f"(f.x), "=f"(f.y)
+      : "r"(v));
+  return f;
+}
+
 // Maximum of v over the 32 lanes of the warp, returned to every lane.
 __device__ __forceinline__ float warp_max_f32(float v) {
   float r;

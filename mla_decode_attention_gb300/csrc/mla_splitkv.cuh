@@ -71,7 +71,15 @@ constexpr uint32_t kTmemS = 256;   // S^T: 64 columns
 constexpr uint32_t kIdescQK = idesc_bf16(128, kRowsPerCta, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, kRowsPerCta, true, true);
 
-enum class KvMode : int { kPagedBf16 = 0, kSparseBf16 = 1 };
+enum class KvMode : int { kPagedBf16 = 0, kSparseBf16 = 1, kPagedFp8 = 2 };
+
+// FP8 cache token: 512 e4m3 codes, 4 fp32 scales (one per 128 latent
+// channels), 64 bf16 RoPE values (FlashMLA "Hopper FP8 sparse decode" note,
+// "The FP8 KVCache Format").
+constexpr int kFp8TokenBytes = 656;
+constexpr int kFp8ScaleOffset = 512;
+constexpr int kFp8RopeOffset = 528;
+constexpr int kDequantWarps = 3;  // warps 0, 2, 3 (warp 1 issues the MMAs)
 
 struct SplitParams {
   const int32_t* meta;
@@ -83,6 +91,7 @@ struct SplitParams {
   int64_t s_kv;            // sparse: pool rows
   const __nv_bfloat16* kv_rows;  // dense: cache base (L2 prefetch); sparse: pool base
   const __nv_bfloat16* q;        // query rows, for L2 prefetch of the next piece
+  const uint8_t* kv_fp8;         // FP8 cache base ([pages, 64, 656] bytes)
   float* ws_o;
   float* ws_lse;
   __nv_bfloat16* out;
@@ -226,7 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool multicast = kClusterMulticast && p.n_hblk == 2;
   if (threadIdx.x == 0) {
     for (int c = 0; c < kChunks; ++c) {
-      mbar_init(smem_u32(&sm->full[c]), 1);
+      // FP8: latent chunks are filled by the three dequantising warps
+      mbar_init(smem_u32(&sm->full[c]),
+                (kMode == KvMode::kPagedFp8 && c < kChunks - 1) ? kDequantWarps : 1);
       // a slot is free once the MMA threads of every CTA writing into it
       // have released it
       mbar_init(smem_u32(&sm->empty[c]), multicast ? 2 : 1);
@@ -264,7 +275,90 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm->tmem_base;
   volatile uint32_t* abort_flag = &sm->abort;
 
-  if (warp == kProducerWarp && kMode == KvMode::kSparseBf16) {
+  if (kMode == KvMode::kPagedFp8 && (warp == 0 || warp == 2 || warp == 3)) {
+    // ===================================================== producer (FP8)
+    // Warp 0 lane 0 loads Q and the bf16 RoPE columns (chunk 8) by TMA.  The
+    // latent chunks 0..7 are dequantised by warps 0, 2, 3 chunk by chunk:
+    // 8 tokens per warp step, lane = (token, 16-code unit); value =
+    // bf16(e4m3 * scale[c / 2]) written into the 128-byte-swizzled slot.
+    const int dw = warp == 0 ? 0 : warp - 1;  // dequant warp index 0..2
+    const int unit = lane & 3;                 // 16-code unit of the 64-column chunk
+    const int tsub = lane >> 2;                // token within a group of 8
+    PartCursor cur = part_cursor(meta, part);
+    int q, t0, t1, split;
+    uint32_t tile_ctr = 0, item_ctr = 0;
+    bool ok = true;
+    while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+      if (warp == 0 && lane == 0) {
+        ok = mbar_wait(smem_u32(&sm->q_empty), (item_ctr & 1) ^ 1, abort_flag, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(smem_u32(&sm->q_full), kChunks * p.rows * 128);
+          const int q_row = q * p.h + hb * kRowsPerCta;
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(q_base + c * kQChunkBytes, &tm_q, c * 64, q_row, smem_u32(&sm->q_full),
+                        l2_policy_evict_last());
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      for (int t = t0; t < t1 && ok; ++t) {
+        int32_t blk[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          blk[h2] = page_of(p, q, 2 * t + h2);
+          if (blk[h2] < 0) {
+            if (p.err && lane == 0 && warp == 0) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
+            blk[h2] = 0;  // read a valid page; the bad page's keys are wrong but finite
+          }
+        }
+        const uint32_t par = (tile_ctr & 1) ^ 1;
+        if (warp == 0 && lane == 0) {  // RoPE chunk by TMA
+          ok = mbar_wait(smem_u32(&sm->empty[kChunks - 1]), par, abort_flag, p.err);
+          if (ok) {
+            const uint32_t bar = smem_u32(&sm->full[kChunks - 1]);
+            mbar_arrive_expect_tx(bar, kChunkBytes);
+            const uint32_t dst = kv_base + (kChunks - 1) * kChunkBytes;
+            tma_load_2d(dst, &tm_kv, 0, blk[0] * kPage, bar, l2_policy_evict_first());
+            tma_load_2d(dst + kChunkBytes / 2, &tm_kv, 0, blk[1] * kPage, bar,
+                        l2_policy_evict_first());
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        for (int c = 0; c < kChunks - 1; ++c) {
+          if (lane == 0) ok = mbar_wait(smem_u32(&sm->empty[c]), par, abort_flag, p.err);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          const uint32_t slot = kv_base + c * kChunkBytes;
+          for (int grp = dw; grp < kTileTokens / 8; grp += kDequantWarps) {
+            const int r = grp * 8 + tsub;  // token row of the tile
+            const uint8_t* tok = p.kv_fp8 +
+                                 (static_cast<int64_t>(blk[r >> 6]) * kPage + (r & 63)) * kFp8TokenBytes;
+            const uint4 codes = __ldg(reinterpret_cast<const uint4*>(tok + c * 64 + unit * 16));
+            const float sc = __ldg(reinterpret_cast<const float*>(tok + kFp8ScaleOffset) + (c >> 1));
+            const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+            uint32_t packed[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xFFFFu)));
+              const float2 b2 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16)));
+              packed[2 * k] = pack_bf16x2(a.x * sc, a.y * sc);
+              packed[2 * k + 1] = pack_bf16x2(b2.x * sc, b2.y * sc);
+            }
+            const uint32_t row = slot + r * 128;
+            st_shared_v4(row + ((2 * unit) ^ (r & 7)) * 16, packed[0], packed[1], packed[2], packed[3]);
+            st_shared_v4(row + ((2 * unit + 1) ^ (r & 7)) * 16, packed[4], packed[5], packed[6],
+                         packed[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->full[c]));
+        }
+        ++tile_ctr;
+      }
+      ++item_ctr;
+    }
+  } else if (warp == kProducerWarp && kMode == KvMode::kSparseBf16) {
     // ===================================================== producer (gather)
     // Lane L gathers rows 4L..4L+3 of each 128-row tile with one tile::gather4
     // per column chunk; lane 0 owns the barriers.  Invalid slots (-1, out of

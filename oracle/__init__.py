@@ -25,8 +25,11 @@ What it computes (one "row" = one query token of one head):
   (page * page_size + offset), -1 marks an invalid slot (FlashMLA README,
   "indices Tensor").
 * FP8 cache: 656 bytes per token = 512 e4m3 codes, 4 fp32 scales (one per 128
-  channels), 64 bf16 RoPE values; a latent value is e4m3(code) * scale
-  (FlashMLA "Hopper FP8 sparse decode" note, "The FP8 KVCache Format").
+  channels), 64 bf16 RoPE values (FlashMLA "Hopper FP8 sparse decode" note,
+  "The FP8 KVCache Format").  The kernel dequantises the codes into bf16
+  before its bf16 MMAs (same note: convert e4m3 to bf16, multiply by the fp32
+  scale; "we first dequantize ... into 512 bfloat16s"), so a key's latent value
+  is bf16(e4m3(code) * scale): the exact product rounded once to bf16.
 
 Readings where the pages are silent (each is listed in the design notes):
 
@@ -34,8 +37,8 @@ Readings where the pages are silent (each is listed in the design notes):
   tokens, so query j of request b sees positions 0 .. L_b - s_q + j.
 * An empty key set gives out = 0 and lse = -inf.
 * An index outside [0, s_kv) other than -1 is treated as invalid.
-* The FP8 value is the exact product fp64(e4m3) * fp64(scale); the oracle
-  does not round it to bf16.
+* The FP8 dequantised value is the exact product e4m3 * scale rounded once to
+  the nearest bf16 (ties to even).
 
 Every array here is numpy float64 unless stated.  bf16 inputs may be passed
 as uint16 bit patterns and are widened exactly (``widen``).
@@ -98,6 +101,25 @@ def fp8_tokens_to_f64(raw: np.ndarray) -> np.ndarray:
     rope_bits = raw[..., 528:656].copy().view("<u2")                  # [..., 64]
     lat = e4m3_to_f64(codes).reshape(*lead, 4, 128) * scales[..., :, None]
     return np.concatenate([lat.reshape(*lead, 512), bf16_bits_to_f64(rope_bits)], axis=-1)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Nearest bfloat16 value (8 significant bits, ties to even), as float64.
+
+    x = m * 2^e with 0.5 <= |m| < 1; keep 8 bits of m by rounding m * 2^8 to
+    the nearest integer (numpy's rint rounds halves to even).  Values in the
+    bf16 normal range only (enough for dequantised cache values).
+    """
+    m, e = np.frexp(np.asarray(x, dtype=np.float64))
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def fp8_tokens_to_keys(raw: np.ndarray) -> np.ndarray:
+    """656-byte FP8 tokens -> the bf16 keys the method attends over, as float64:
+    latent = bf16(e4m3 * scale), RoPE = the stored bf16 values."""
+    x = fp8_tokens_to_f64(raw)
+    x[..., :512] = round_to_bf16(x[..., :512])
+    return x
 
 
 # ---------------------------------------------------------------------------
@@ -178,13 +200,13 @@ def visible_length(seqlen: int, s_q: int, j: int, causal: bool) -> int:
 
 def widen(x: np.ndarray) -> np.ndarray:
     """float64 view of an input array: uint16 arrays are bf16 bit patterns,
-    uint8 arrays with a last dimension of 656 are FP8 cache tokens, anything
-    else is converted with ``astype``."""
+    uint8 arrays with a last dimension of 656 are FP8 cache tokens (decoded
+    to their bf16 keys), anything else is converted with ``astype``."""
     x = np.asarray(x)
     if x.dtype == np.uint16:
         return bf16_bits_to_f64(x)
     if x.dtype == np.uint8 and x.shape[-1] == FP8_TOKEN_BYTES:
-        return fp8_tokens_to_f64(x)
+        return fp8_tokens_to_keys(x)
     return x.astype(np.float64)
 
 
@@ -235,7 +257,7 @@ def dense_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
 def fp8_dense_decode(q, kv_raw, block_table, cache_seqlens, softmax_scale,
                      causal=True, rows=None):
     """Paged decode over the 656-byte FP8 cache; each gathered token is decoded
-    exactly by ``fp8_tokens_to_f64`` before the dense definition applies."""
+    to its bf16 key by ``fp8_tokens_to_keys`` before the dense definition applies."""
     kv_raw = np.asarray(kv_raw, dtype=np.uint8)
     assert kv_raw.shape[-1] == FP8_TOKEN_BYTES
     return dense_decode(q, kv_raw, block_table, cache_seqlens, softmax_scale, causal, rows)

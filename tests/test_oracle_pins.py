@@ -99,6 +99,25 @@ def test_fp8_quantise_decode_error_bound():
     assert np.array_equal(dec[:, 512:], rope_ref)
 
 
+def test_round_to_bf16_matches_torch_on_fp32_values():
+    x = rng(40).standard_normal(50000).astype(np.float32) * np.exp2(rng(41).integers(-20, 20, 50000))
+    x = x.astype(np.float32)
+    x[:6] = [0.0, 1.0, 1.00390625, 1.01171875, -3.0078125, 2.0 ** -100]  # ties and exact values
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_to_bf16(x.astype(np.float64)), ref)
+
+
+def test_fp8_keys_are_bf16_rounded_dequantised_values():
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(16, 576, generator=g)
+    raw = workloads.quantize_fp8_tokens(x).numpy()
+    exact = oracle.fp8_tokens_to_f64(raw)
+    keys = oracle.fp8_tokens_to_keys(raw)
+    assert np.array_equal(keys[:, 512:], exact[:, 512:])
+    assert np.array_equal(keys[:, :512], oracle.round_to_bf16(exact[:, :512]))
+    assert np.all(np.abs(keys[:, :512] - exact[:, :512]) <= 2.0 ** -8 * np.abs(exact[:, :512]))
+
+
 def test_fp8_representable_roundtrip_exact():
     """Values already on the e4m3 grid times a power-of-two scale survive."""
     codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
