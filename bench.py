@@ -164,8 +164,9 @@ def run_ours(args, rank, world, local_rank):
     # two input sets (each > L2), pinned host copies for the end-to-end leg
     sets_host = [workloads.make_inputs(w, seed=w.seed + 1000 * rank + k) for k in range(2)]
     for s in sets_host:
-        for key in ("q", "kv_cache", "block_table", "cache_seqlens"):
-            s[key] = s[key].pin_memory()
+        for key, v in list(s.items()):
+            if torch.is_tensor(v):
+                s[key] = v.pin_memory()
     sets = [{k: (v.to(dev) if hasattr(v, "to") and hasattr(v, "pin_memory") else v)
              for k, v in s.items()} for s in sets_host]
     b, s_q, h = w.b, w.s_q, w.h
@@ -174,16 +175,26 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.Stream(device=dev)
     scale = workloads.SOFTMAX_SCALE
 
+    sparse = w.kind == "sparse"
+    fmt = binding.MLA_KV_FP8_656 if w.kind == "fp8" else binding.MLA_KV_BF16
+    in_keys = ("q", "kv", "indices") if sparse else ("q", "kv_cache", "block_table",
+                                                      "cache_seqlens")
+
     def step(k, split_only=False):
         s, buf = sets[k % 2], bufs[k % 2]
-        if not split_only:
+        if sparse:
+            if not split_only:
+                binding.mla_get_metadata(None, b, s_q, False, w.topk, parts, buf.metadata, stream)
+            binding.mla_sparse_decode(s["q"], s["kv"], s["indices"], scale, buf.metadata, parts,
+                                      buf.workspace, buf.out, buf.lse, buf.err, stream)
+        elif not split_only:
             binding.mla_get_metadata(s["cache_seqlens"], b, s_q, True, 0, parts, buf.metadata,
                                      stream)
-            binding.mla_decode(s["q"], s["kv_cache"], binding.MLA_KV_BF16, s["block_table"],
+            binding.mla_decode(s["q"], s["kv_cache"], fmt, s["block_table"],
                                s["cache_seqlens"], scale, True, buf.metadata, parts,
                                buf.workspace, buf.out, buf.lse, buf.err, stream)
         else:
-            binding.mla_decode_splitkv(s["q"], s["kv_cache"], binding.MLA_KV_BF16,
+            binding.mla_decode_splitkv(s["q"], s["kv_cache"], fmt,
                                        s["block_table"], s["cache_seqlens"], scale, True,
                                        buf.metadata, parts, buf.workspace, buf.out, buf.lse,
                                        buf.err, stream)
@@ -272,15 +283,14 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end through the public API with host buffers
     n_e2e = max(3, min(args.steps, 50))
-    h2d = sum(sets_host[0][k].numel() * sets_host[0][k].element_size()
-              for k in ("q", "kv_cache", "block_table", "cache_seqlens"))
+    h2d = sum(sets_host[0][k].numel() * sets_host[0][k].element_size() for k in in_keys)
     d2h = bufs[0].out.numel() * 2 + bufs[0].lse.numel() * 4
     out_host = [torch.empty(bufs[0].out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     lse_host = [torch.empty(bufs[0].lse.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
 
     def e2e_step(k):
         s_h, s_d, buf = sets_host[k % 2], sets[k % 2], bufs[k % 2]
-        for key in ("q", "kv_cache", "block_table", "cache_seqlens"):
+        for key in in_keys:
             s_d[key].copy_(s_h[key], non_blocking=True)
         step(k)
         out_host[k % 2].copy_(buf.out, non_blocking=True)
@@ -306,8 +316,16 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = float(t.item())
 
     # ---- accounting
-    seqlens = sets_host[0]["cache_seqlens"].tolist()
-    flops, bytes_, kv_bytes = roofline.dense_counts(seqlens, s_q, h, causal=True)
+    flops_nominal = None
+    if sparse:
+        idx = sets_host[0]["indices"]
+        valid = ((idx >= 0) & (idx < w.s_kv)).sum(dim=-1).flatten().tolist()
+        flops, flops_nominal, bytes_, kv_bytes = roofline.sparse_counts(valid, h, w.topk)
+        seqlens = [w.topk] * b
+    else:
+        seqlens = sets_host[0]["cache_seqlens"].tolist()
+        flops, bytes_, kv_bytes = roofline.dense_counts(seqlens, s_q, h, causal=True,
+                                                        fp8=(w.kind == "fp8"))
     tflops = flops / (ms_per_step * 1e-3) / 1e12 * world
     kv_gbs = kv_bytes / (ms_per_step * 1e-3) / 1e9 * world
     ai = flops / bytes_
@@ -324,18 +342,22 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(tflops, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 q and latent cache, shuffled page table)",
+        "data": "synthetic (seeded N(0,1) bf16 q and latent cache, shuffled page table)"
+                if not sparse else "synthetic (seeded N(0,1) pool, top-k indices, peaked rows)",
         "config": {"workload": WORKLOAD if args.config == WORKLOAD else args.config,
                    "batch": b, "s_q": s_q, "h_q": h, "d_qk": 576, "d_v": 512,
                    "seqlen": seqlens[0] if len(set(seqlens)) == 1 else "mixed",
                    "page_block": 64, "num_sm_parts": parts,
-                   "l2": "inputs larger than L2 (302 MB KV per set, two sets alternate)",
+                   "l2": ("inputs larger than L2 (KV per set > 129 MB, two sets alternate)"
+                          if kv_bytes > 129e6 else
+                          "KV working set fits in L2 (two sets alternate); effective GB/s may exceed HBM"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_gbs": round(kv_gbs, 1),
         "roofline_fraction": round(tflops / world / roof_tf, 4),
         "roofline_tflops": round(roof_tf, 1),
         "arithmetic_intensity": round(ai, 1),
-        "algorithmic": {"flops": flops, "bytes": bytes_, "kv_bytes": kv_bytes},
+        "algorithmic": {"flops": flops, "bytes": bytes_, "kv_bytes": kv_bytes,
+                        "flops_nominal_topk": flops_nominal},
         "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "mla_splitkv_kernel", "kernel_ms": round(split_ms, 5),
@@ -343,7 +365,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
-                "note": "all call inputs (q, KV cache, page table, lengths) copied from pinned "
+                "note": "all call inputs (" + ", ".join(in_keys) + ") copied from pinned "
                         "host memory and out+lse copied back every step"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,

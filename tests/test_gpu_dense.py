@@ -174,3 +174,16 @@ def test_full_size_dense_v3_sampled_rows():
                       f"dense_v3 row {b}")
     assert res["err"] == 0
     assert np.all(np.isfinite(res["out"]))
+
+
+def test_full_size_spec_decode_sampled_rows():
+    """b=128, s_q=2 causal, lengths U[1024, 16384]: sampled query tokens of both positions."""
+    w = workloads.WORKLOADS["spec"]
+    inp = workloads.make_inputs(w)
+    res = run_dense(inp, causal=True)
+    rows = [(0, 0), (0, 1), (47, 1), (90, 0), (127, 1)]
+    ref_o, ref_l = oracle_dense(inp, causal=True, rows=rows)
+    for b, j in rows:
+        assert_parity(res["out"][b, j], ref_o[b, j], res["lse"][b, :, j], ref_l[b, :, j],
+                      f"spec row {b},{j}")
+    assert res["err"] == 0 and np.all(np.isfinite(res["out"]))
