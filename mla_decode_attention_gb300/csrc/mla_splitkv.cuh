@@ -17,14 +17,13 @@
 // (the seesaw in the FlashMLA deep dive exists because WGMMA keeps O in
 // registers).
 //
-// Roles (384 threads):
+// Roles (640 threads):
 //   warp 0 lane 0  : producer: TMA loads of Q (once per piece) and of each
 //                    tile's 9 column chunks (two 64-token pages per chunk),
 //                    plus L2 prefetches of the pages two tiles ahead
 //   warp 1         : TMEM allocation; lane 0 issues every MMA
-//   warps 4..7     : softmax warpgroup 0, query rows 0..31 of the block
-//   warps 8..11    : softmax warpgroup 1, query rows 32..63
-//   warps 2..3     : idle
+//   warps 4..19    : four softmax warpgroups, query rows 16g .. 16g+15 each
+//   warps 2..3     : idle (dequantisers, with warp 0, for the FP8 cache)
 //
 // Shared memory (1024-byte aligned): 9 KV chunk slots of [128 tok x 64 col]
 // bf16 (16 KB each, 128-byte swizzle), Q as 9 chunks of [64 rows x 64 col]
@@ -52,9 +51,11 @@ constexpr int kSmemKv = 0;
 constexpr int kSmemQ = kChunks * kChunkBytes;                 // 147456
 constexpr int kSmemSmall = kSmemQ + kChunks * kQChunkBytes;   // 221184
 constexpr int kNumBarriers = 2 * kChunks + 5;
-constexpr int kSmallBytes = 8 * kNumBarriers + 16 + 4 * 4 * 2 * 4 * 32;
+constexpr int kSmallBytes = 8 * kNumBarriers + 16 + 5 * 4 * 4 * 4 * 16;
 constexpr int kSmemBytes = kSmallBytes + kSmemSmall + 1024;   // + alignment slack
-constexpr int kThreads = 384;
+constexpr int kSoftmaxGroups = 4;                  // warpgroups on the softmax
+constexpr int kRowsPerGroup = kRowsPerCta / kSoftmaxGroups;  // 16 query rows each
+constexpr int kThreads = 128 * (1 + kSoftmaxGroups);
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kSoftmaxWarp0 = 4;
@@ -65,6 +66,9 @@ constexpr int kPrefetchTiles = 2;
 // per cluster and each CTA issues half the TMA boxes.
 constexpr bool kClusterMulticast = false;
 constexpr bool kPrefetchKv = false;
+// A later tile moves the softmax reference only when a score exceeds it by
+// more than this (log2 units): probabilities stay <= 2^8, exact in range.
+constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // O^T: 4 blocks of 64 columns
 constexpr uint32_t kTmemS = 256;   // S^T: 64 columns
@@ -108,10 +112,11 @@ struct SplitParams {
 struct SmemSmall {
   // float arrays first: each row of 32 floats is read back as float4 vectors,
   // so every row must start on a 16-byte boundary.
-  alignas(16) float red_max[2][4][32];
-  alignas(16) float red_sum[2][4][32];
-  alignas(16) float bcast[2][4][32];
-  alignas(16) float bcast2[2][4][32];
+  alignas(16) float red_max[kSoftmaxGroups][4][kRowsPerGroup];
+  alignas(16) float red_sum[kSoftmaxGroups][4][kRowsPerGroup];
+  alignas(16) float red_bsum[kSoftmaxGroups][4][kRowsPerGroup];
+  alignas(16) float bcast[kSoftmaxGroups][4][kRowsPerGroup];
+  alignas(16) float bcast2[kSoftmaxGroups][4][kRowsPerGroup];
   uint64_t full[kChunks];
   uint64_t empty[kChunks];
   uint64_t q_full, q_empty, s_full, p_full, o_done;
@@ -167,6 +172,39 @@ __device__ __forceinline__ float warp_reduce_scatter32(const float (&v)[32], int
   const float keep = hi ? d[1] : d[0];
   const float r = __shfl_xor_sync(0xffffffffu, send, 1);
   return kMax ? fmaxf(keep, r) : keep + r;
+}
+
+// Sum of 16 per-thread values (one per query row of the warpgroup) over the
+// warp's 32 lanes; lanes l and l + 16 both end with the sum for row l & 15.
+__device__ __forceinline__ float warp_sum_scatter16(const float (&v)[16], int lane) {
+  float a[16], b[8], c[4], d[2];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = v[i] + __shfl_xor_sync(0xffffffffu, v[i], 16);
+  bool hi = lane & 8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = hi ? a[i] : a[i + 8];
+    const float keep = hi ? a[i + 8] : a[i];
+    b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  hi = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = hi ? b[i] : b[i + 4];
+    const float keep = hi ? b[i + 4] : b[i];
+    c[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  hi = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = hi ? c[i] : c[i + 2];
+    const float keep = hi ? c[i + 2] : c[i];
+    d[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  hi = lane & 1;
+  const float send = hi ? d[0] : d[1];
+  const float keep = hi ? d[1] : d[0];
+  return keep + __shfl_xor_sync(0xffffffffu, send, 1);
 }
 
 __device__ __forceinline__ void load_bcast32(const float* src, float (&dst)[32]) {
@@ -245,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm->q_full), 1);
     mbar_init(smem_u32(&sm->q_empty), 1);
     mbar_init(smem_u32(&sm->s_full), 1);
-    mbar_init(smem_u32(&sm->p_full), 8);  // one arrive per softmax warp
+    mbar_init(smem_u32(&sm->p_full), 4 * kSoftmaxGroups);  // one arrive per softmax warp
     mbar_init(smem_u32(&sm->o_done), 1);
     sm->abort = 0;
     fence_mbarrier_init();
@@ -553,19 +591,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++item_ctr;
       }
     }
-  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
+  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4 * kSoftmaxGroups) {
     // ===================================================== softmax / epilogue
-    // Thread = one token row r of the tile (TMEM lane) x the 32 query rows of
-    // its warpgroup (TMEM columns).  Column max over the 128 tokens: warp
-    // redux, then the four warps through shared memory.  Sums stay per lane
-    // (rescaled like O) until the piece ends.
-    const int g = (warp - kSoftmaxWarp0) >> 2;  // row half: rows 32g .. 32g+31
+    // Thread = one token row r of the tile (TMEM lane) x the 16 query rows of
+    // its warpgroup (TMEM columns).  Probabilities are taken against a per-row
+    // reference max m (log2 units).  The first tile of a piece sets m to the
+    // exact column max.  A later tile keeps m unless one of its scores exceeds
+    // the smallest reference by more than kRescaleLog2 (one warp max and one
+    // barrier vote decide); then every row's m moves to its exact running max
+    // and O^T and the sums are rescaled.  Two running sums per row: of the
+    // fp32 probabilities (for the LSE) and of their bf16 roundings, i.e. the
+    // weights the PV MMA multiplies (to normalise O), so a stale reference
+    // leaves no coherent gain error on the output (flash-attention sparse-MLA
+    // article: summing the bf16-rounded p brings the row gain to the noise
+    // floor).  Sums stay per lane until the piece ends.
+    constexpr int R = kRowsPerGroup;
+    const int g = (warp - kSoftmaxWarp0) >> 2;  // rows R*g .. R*g + R-1
     const int wq = warp & 3;                    // TMEM lane quarter
     const int r = wq * 32 + lane;               // token row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + kTmemS + 32 * g;
-    const uint32_t t_o = tmem + lane_off + kTmemO + 32 * g;
+    const uint32_t t_s = tmem + lane_off + kTmemS + R * g;
+    const uint32_t t_o = tmem + lane_off + kTmemO + R * g;
     const uint32_t p_slot = kv_base + 8 * kChunkBytes;
+    const uint32_t bar_id = 1 + g;
     const float NEG_INF = -INFINITY;
     float* red_w = &sm->red_max[g][wq][0];
     float* bc_m = &sm->bcast[g][wq][0];
@@ -579,16 +627,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t keys = srec[kSKeys];
       const int32_t* idx_row = (kMode == KvMode::kSparseBf16)
                                    ? p.indices + static_cast<int64_t>(q) * p.topk : nullptr;
-      float m_run = NEG_INF;  // running max (log2 units) of row 32g + lane
-      float lp[32];           // this lane's share of the running sums
+      float m_true = NEG_INF;  // running max of row R*g + (lane & 15) (-inf: no key yet)
+      float m_use = 0.f;       // reference the probabilities are taken against
+      float m_low = NEG_INF;   // smallest m_true over the warpgroup's rows
+      float lp[R];             // this lane's share of sum p (fp32)
+      float lb[R];             // this lane's share of sum bf16(p)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) lp[i] = 0.f;
+      for (int i = 0; i < R; ++i) { lp[i] = 0.f; lb[i] = 0.f; }
       for (int t = t0; t < t1; ++t) {
         ok = mbar_wait(smem_u32(&sm->s_full), tile_ctr & 1, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
-        float x[32];
-        tmem_ld32(t_s, x);
+        float x[R];
+        tmem_ld16(t_s, x);
         tmem_wait_ld();
         const int tok = t * kTileTokens + r;
         bool valid = tok < keys;
@@ -596,90 +647,125 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t id = idx_row[tok];
           valid = id >= 0 && static_cast<int64_t>(id) < p.s_kv;
         }
+        const float mul = valid ? p.scale_log2 : 0.f;
+        const float add = valid ? 0.f : NEG_INF;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = valid ? x[i] * p.scale_log2 : NEG_INF;
+        for (int i = 0; i < R; ++i) x[i] = fmaf(x[i], mul, add);
+        bool full = true;
+        if (t != t0) {
+          float u = x[0];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float w0 = warp_max_f32(x[i]), w1 = warp_max_f32(x[i + 1]);
-          const float w2 = warp_max_f32(x[i + 2]), w3 = warp_max_f32(x[i + 3]);
-          if (lane == 0) *reinterpret_cast<float4*>(red_w + i) = make_float4(w0, w1, w2, w3);
+          for (int i = 1; i < R; ++i) u = fmaxf(u, x[i]);
+          u = warp_max_f32(u);
+          full = named_barrier_or(bar_id, 128, u > m_low + kRescaleLog2);
         }
-        named_barrier_sync(1 + g, 128);
-        const float mt = fmaxf(fmaxf(sm->red_max[g][0][lane], sm->red_max[g][1][lane]),
-                               fmaxf(sm->red_max[g][2][lane], sm->red_max[g][3][lane]));
-        const float m_new = fmaxf(m_run, mt);
-        const float m_use = (m_new == NEG_INF) ? 0.f : m_new;
-        const float alpha = fast_exp2(m_run - m_use);  // 0 on the first tile
-        bc_m[lane] = m_use;
-        bc_a[lane] = alpha;
-        __syncwarp();
+        if (full) {
+          // exact column max of this tile over the 128 tokens
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(bc_m + i);
-          const float4 a4 = *reinterpret_cast<const float4*>(bc_a + i);
-          x[i] = fast_exp2(x[i] - m4.x);
-          x[i + 1] = fast_exp2(x[i + 1] - m4.y);
-          x[i + 2] = fast_exp2(x[i + 2] - m4.z);
-          x[i + 3] = fast_exp2(x[i + 3] - m4.w);
-          lp[i] = fmaf(lp[i], a4.x, x[i]);
-          lp[i + 1] = fmaf(lp[i + 1], a4.y, x[i + 1]);
-          lp[i + 2] = fmaf(lp[i + 2], a4.z, x[i + 2]);
-          lp[i + 3] = fmaf(lp[i + 3], a4.w, x[i + 3]);
+          for (int i = 0; i < R; i += 4) {
+            const float w0 = warp_max_f32(x[i]), w1 = warp_max_f32(x[i + 1]);
+            const float w2 = warp_max_f32(x[i + 2]), w3 = warp_max_f32(x[i + 3]);
+            if (lane == 0) *reinterpret_cast<float4*>(red_w + i) = make_float4(w0, w1, w2, w3);
+          }
+          named_barrier_sync(bar_id, 128);
+          const int row = lane & (R - 1);
+          const float mt = fmaxf(fmaxf(sm->red_max[g][0][row], sm->red_max[g][1][row]),
+                                 fmaxf(sm->red_max[g][2][row], sm->red_max[g][3][row]));
+          const float m_new = fmaxf(m_true, mt);
+          const float m_use_new = (m_new == NEG_INF) ? 0.f : m_new;
+          const float alpha = (t == t0) ? 1.f : fast_exp2(m_use - m_use_new);
+          m_true = m_new;
+          m_use = m_use_new;
+          m_low = warp_min_f32(m_true);
+          if (lane < R) {
+            bc_m[lane] = m_use;
+            bc_a[lane] = alpha;
+          }
+          __syncwarp();
+          if (t != t0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < R; i += 4) {
+              const float4 a4 = *reinterpret_cast<const float4*>(bc_a + i);
+              lp[i] *= a4.x; lp[i + 1] *= a4.y; lp[i + 2] *= a4.z; lp[i + 3] *= a4.w;
+              lb[i] *= a4.x; lb[i + 1] *= a4.y; lb[i + 2] *= a4.z; lb[i + 3] *= a4.w;
+            }
+            // PV of the previous tile completed before s_full of this tile
+            // fired (one thread's tcgen05 operations complete in order)
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
+              float o[R];
+              tmem_ld16(t_o + 64 * m, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < R; i += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(bc_a + i);
+                o[i] *= a4.x; o[i + 1] *= a4.y; o[i + 2] *= a4.z; o[i + 3] *= a4.w;
+              }
+              tmem_st16(t_o + 64 * m, o);
+            }
+            tmem_wait_st();
+          }
         }
-        // P^T row r, rows 32g..32g+31 -> 16-byte units 4g..4g+3 (swizzled)
+        // probabilities against the reference; P^T row r, rows R*g .. R*g+R-1
+        // -> 16-byte units 2g, 2g+1 (swizzled)
         const uint32_t prow = p_slot + r * 128;
 #pragma unroll
-        for (int cu = 0; cu < 4; ++cu) {
-          const uint32_t unit = static_cast<uint32_t>((4 * g + cu) ^ (r & 7));
-          st_shared_v4(prow + unit * 16, pack_bf16x2(x[8 * cu + 0], x[8 * cu + 1]),
-                       pack_bf16x2(x[8 * cu + 2], x[8 * cu + 3]),
-                       pack_bf16x2(x[8 * cu + 4], x[8 * cu + 5]),
-                       pack_bf16x2(x[8 * cu + 6], x[8 * cu + 7]));
+        for (int cu = 0; cu < 2; ++cu) {
+          const float4 m0 = *reinterpret_cast<const float4*>(bc_m + 8 * cu);
+          const float4 m1 = *reinterpret_cast<const float4*>(bc_m + 8 * cu + 4);
+          float e[8];
+          e[0] = fast_exp2(x[8 * cu + 0] - m0.x); e[1] = fast_exp2(x[8 * cu + 1] - m0.y);
+          e[2] = fast_exp2(x[8 * cu + 2] - m0.z); e[3] = fast_exp2(x[8 * cu + 3] - m0.w);
+          e[4] = fast_exp2(x[8 * cu + 4] - m1.x); e[5] = fast_exp2(x[8 * cu + 5] - m1.y);
+          e[6] = fast_exp2(x[8 * cu + 6] - m1.z); e[7] = fast_exp2(x[8 * cu + 7] - m1.w);
+          uint32_t pk[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            pk[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
+            lp[8 * cu + 2 * k] += e[2 * k];
+            lp[8 * cu + 2 * k + 1] += e[2 * k + 1];
+            lb[8 * cu + 2 * k] += __uint_as_float(pk[k] << 16);
+            lb[8 * cu + 2 * k + 1] += __uint_as_float(pk[k] & 0xFFFF0000u);
+          }
+          const uint32_t unit = static_cast<uint32_t>((2 * g + cu) ^ (r & 7));
+          st_shared_v4(prow + unit * 16, pk[0], pk[1], pk[2], pk[3]);
         }
         fence_proxy_async_smem();
-        // PV of the previous tile completed before s_full of this tile fired
-        // (tcgen05 operations of one thread complete in order), so O^T can be
-        // rescaled now.
-        if (t != t0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
-            float o[32];
-            tmem_ld32(t_o + 64 * m, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 a4 = *reinterpret_cast<const float4*>(bc_a + i);
-              o[i] *= a4.x; o[i + 1] *= a4.y; o[i + 2] *= a4.z; o[i + 3] *= a4.w;
-            }
-            tmem_st32(t_o + 64 * m, o);
-          }
-          tmem_wait_st();
-        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
-        m_run = m_new;
         ++tile_ctr;
       }
       if (!ok) break;
-      // ---- epilogue: O^T / l -> out (one split) or fp32 partial
-      float lsum = warp_reduce_scatter32<false>(lp, lane);  // this warp's tokens, row 32g+lane
-      sm->red_sum[g][wq][lane] = lsum;
-      named_barrier_sync(1 + g, 128);
-      lsum = (sm->red_sum[g][0][lane] + sm->red_sum[g][1][lane]) +
-             (sm->red_sum[g][2][lane] + sm->red_sum[g][3][lane]);
+      // ---- epilogue: O^T / sum bf16(p) -> out (one split) or fp32 partial
+      const int row = lane & (R - 1);
+      float lsum = warp_sum_scatter16(lp, lane);  // this warp's tokens, row R*g + row
+      float bsum = warp_sum_scatter16(lb, lane);
+      if (lane < R) {
+        sm->red_sum[g][wq][lane] = lsum;
+        sm->red_bsum[g][wq][lane] = bsum;
+      }
+      named_barrier_sync(bar_id, 128);
+      lsum = (sm->red_sum[g][0][row] + sm->red_sum[g][1][row]) +
+             (sm->red_sum[g][2][row] + sm->red_sum[g][3][row]);
+      bsum = (sm->red_bsum[g][0][row] + sm->red_bsum[g][1][row]) +
+             (sm->red_bsum[g][2][row] + sm->red_bsum[g][3][row]);
       ok = mbar_wait(smem_u32(&sm->o_done), item_ctr & 1, abort_flag, p.err);
       if (!ok) break;
       tc_fence_after();
-      const bool has = lsum > 0.f;
-      const float inv_l = has ? 1.f / lsum : 0.f;
-      const float lse_v = has ? (m_run + __log2f(lsum)) * 0.69314718055994531f : NEG_INF;
-      bc_a[lane] = inv_l;
+      const bool has = lsum > 0.f && bsum > 0.f;
+      const float inv_l = has ? 1.f / bsum : 0.f;
+      const float lse_v = has ? (m_use + __log2f(lsum)) * 0.69314718055994531f : NEG_INF;
+      if (lane < R) bc_a[lane] = inv_l;
       __syncwarp();
-      float il[32];
-      load_bcast32(bc_a, il);
+      float il[R];
+#pragma unroll
+      for (int i = 0; i < R; i += 4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(bc_a + i);
+        il[i] = t4.x; il[i + 1] = t4.y; il[i + 2] = t4.z; il[i + 3] = t4.w;
+      }
       const bool final_out = srec[kSNSplits] == 1;
-      const int row0 = hb * kRowsPerCta + 32 * g;  // first head of this warpgroup
+      const int row0 = hb * kRowsPerCta + R * g;  // first head of this warpgroup
       const int split_row = srec[kSSplitOff] + split;
       const int b = q / p.s_q, j = q % p.s_q;
 #pragma unroll 1
@@ -691,16 +777,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (final_out) {
           __nv_bfloat16* dst = p.out + (static_cast<int64_t>(q) * p.h + row0) * kDv + d;
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < R; ++i)
             if (row0 + i < p.h) dst[static_cast<int64_t>(i) * kDv] = __float2bfloat16_rn(o[i] * il[i]);
         } else {
           float* dst = p.ws_o + (static_cast<int64_t>(split_row) * p.h + row0) * kDv + d;
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < R; ++i)
             if (row0 + i < p.h) dst[static_cast<int64_t>(i) * kDv] = o[i] * il[i];
         }
       }
-      if (wq == 0 && row0 + lane < p.h) {
+      if (wq == 0 && lane < R && row0 + lane < p.h) {
         if (final_out)
           p.lse[(static_cast<int64_t>(b) * p.h + row0 + lane) * p.s_q + j] = lse_v;
         else
