@@ -8,6 +8,7 @@
 #include "mla_decode.h"
 #include "mla_internal.h"
 #include "mla_splitkv.cuh"
+#include "mla_pair.cuh"
 
 namespace mla {
 
@@ -92,6 +93,35 @@ int launch_split(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const SplitP
   return e == cudaSuccess ? MLA_OK : record_cuda_error("split kernel launch", e);
 }
 
+int launch_pair(const CUtensorMap& tm_kv, const SplitParams& prm, cudaStream_t stream) {
+  static int state = 0;  // 0 unset, 1 ok, -1 failed
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (state == 0) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          pair::mla_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes);
+      state = e == cudaSuccess ? 1 : -1;
+      if (e != cudaSuccess) return record_cuda_error("cudaFuncSetAttribute(pair kernel)", e);
+    }
+    if (state != 1) return record_error("pair kernel configuration failed earlier", MLA_ERR_CUDA);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(prm.num_parts * 2, 1, 1);
+  cfg.blockDim = dim3(pair::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = pair::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::mla_pair_kernel, tm_kv, prm);
+  return e == cudaSuccess ? MLA_OK : record_cuda_error("pair kernel launch", e);
+}
+
 }  // namespace
 
 }  // namespace mla
@@ -156,8 +186,10 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   prm.n_hblk = n_hblk;
   prm.rows = rows;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
-  return fp8 ? launch_split<KvMode::kPagedFp8>(tm_q, tm_kv, prm, stream)
-             : launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);
+  if (fp8) return launch_split<KvMode::kPagedFp8>(tm_q, tm_kv, prm, stream);
+  // 128 query rows: the two-SM kernel (scores and softmax on one SM, P.V on the other)
+  if (h_q == pair::kRows) return launch_pair(tm_kv, prm, stream);
+  return launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);
 }
 
 extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,

@@ -1,0 +1,636 @@
+// Paired-CTA MLA decode kernel for 128 query rows per query token (sm_103a).
+//
+// A cluster of two CTAs on two SMs shares one schedule part.  Per 128-key tile:
+//
+//   score CTA (rank 0):  S[128 rows x 128 tokens] = Q[128 x 576] . K_tile^T
+//                        (tcgen05, A = Q resident in TMEM, B = K tile in smem,
+//                        N = 128), then the online softmax with one thread per
+//                        query row; P (bf16) and the per-row rescale factors go
+//                        to the output CTA by a shared-memory bulk copy.
+//   output CTA (rank 1): O[128 rows x 512] += P[128 x 128] . V_tile[128 x 512]
+//                        (tcgen05, both operands in smem, N = 128 per d quarter),
+//                        O in TMEM (all 512 columns); it writes the output rows.
+//
+// Both CTAs read the same cached rows (the score CTA all 576 columns, the
+// output CTA the first 512: V is the latent part of the same row, FlashMLA
+// deep dive, "Theoretical Analysis").  Splitting the two products over two SMs
+// lets each issue MMAs of 128 x 128 x 16 (full tensor rate) and keeps keys
+// loading while the previous tile is multiplied.  Score CTA TMEM: Q's 512
+// latent columns (256 columns of bf16 pairs) and two S buffers, so QK of tile
+// t + 1 runs while the softmax still reads tile t; Q's 64 RoPE columns sit in
+// shared memory and enter QK through one smem-smem MMA chunk.  The softmax
+// makes two passes over S in TMEM (row max, then probabilities), 32 columns
+// at a time, so its code stays small.
+//
+// Roles (256 threads, both CTAs; two warps per SM sub-partition, so each
+// thread may hold 224 registers):
+//   warps 0, 2 lane 0    : TMA issuers (chunk c of a tile by issuer c mod 2 in
+//                          the score CTA; chunk n of the V stream by n mod 2)
+//   warp 1               : TMEM owner; lane 0 issues every MMA
+//   warp 3               : score CTA: issues the P bulk copies (named barriers 1, 2
+//                          with warps 4..7 around the staging buffer);
+//                          output CTA: hands consumed P buffers back
+//   warps 4..7           : row threads, thread r = query row r = TMEM lane r
+//
+// Waits are bounded (mbar_wait*); after an abort every role keeps walking its
+// schedule without waiting, so the named barriers between warps 4..8 stay
+// matched and every thread reaches the final cluster barrier.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstddef>
+
+#include "mla_decode.h"
+#include "mla_internal.h"
+#include "mla_ptx.cuh"
+#include "mla_schedule.cuh"
+#include "mla_splitkv.cuh"
+
+namespace mla {
+namespace pair {
+
+constexpr int kThreads = 256;
+constexpr int kRows = 128;                         // query rows per cluster = TMEM lanes
+constexpr int kChunk = kTileTokens * 64 * 2;       // 16 KB: [128 tokens x 64 columns] bf16
+// score CTA
+constexpr int kKGroups = 3;                        // K ring: 3 groups of 3 chunks
+constexpr int kKGroupBytes = 3 * kChunk;           // 48 KB
+constexpr int kQRope = kKGroups * kKGroupBytes;    // 147456: Q RoPE columns [128 x 64] bf16
+constexpr int kStage = kQRope + kChunk;            // 163840: P staging
+constexpr int kPBytes = kRows * kTileTokens * 2;   // 32768: P[128 rows x 128 tokens] bf16
+constexpr int kSideAlpha = kPBytes;                // float alpha[128]
+constexpr int kSideInvL = kPBytes + 512;           // float inv_l[128] (last tile of a piece)
+constexpr int kSideFlags = kPBytes + 1024;         // uint32 per row warp: any alpha != 1
+constexpr int kXferBytes = kPBytes + 1040;         // 33808 bytes per tile
+// output CTA
+constexpr int kVGroups = 4;                        // V ring: 128-wide d quarters
+constexpr int kVGroupBytes = 2 * kChunk;           // 32 KB
+constexpr int kPBuf0 = kVGroups * kVGroupBytes;    // 131072
+constexpr int kPBufStride = 34816;                 // kXferBytes rounded up to 1 KB
+constexpr int kBarOffset = kPBuf0 + 2 * kPBufStride;  // 200704 (score CTA ends at 197648)
+// TMEM columns
+constexpr uint32_t kQCol = 0;                      // score CTA: Q latent part, 256 columns
+constexpr uint32_t kSCol = 256;                    // score CTA: S buffers at 256 and 384
+constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
+constexpr uint32_t kXferNamedThreads = 160;        // warps 3..7
+
+struct Bars {
+  uint64_t kfull[kKGroups], kempty[kKGroups];      // score CTA K ring
+  uint64_t vfull[kVGroups], vempty[kVGroups];      // output CTA V ring
+  uint64_t q_full, q_free, s_full[2], s_free[2];   // score CTA
+  uint64_t p_free[2];                              // score CTA, arrived by the output CTA
+  uint64_t p_full[2];                              // output CTA, completed by bulk copies
+  uint64_t pv_done[2], o_full, o_free, o_drained, o_rescaled;  // output CTA
+  uint64_t side_read[2];                           // output CTA: row threads read P's side data
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+constexpr int kSmemBytes = kBarOffset + static_cast<int>(sizeof(Bars)) + 1024;
+static_assert(kBarOffset % 16 == 0, "barrier block alignment");
+static_assert(kStage + kXferBytes <= kBarOffset, "score CTA layout");
+static_assert(kXferBytes <= kPBufStride && kXferBytes % 16 == 0, "P transfer size");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+// One CTA per SM (shared memory); up to 224 registers per thread (8 warps, two
+// per sub-partition), so each row thread's 128 scores stay in registers.
+__global__ void __maxnreg__(224)
+    mla_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ SplitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + kBarOffset);
+  const uint32_t base = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int part = blockIdx.x >> 1;
+  const int32_t* meta = p.meta;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kKGroups; ++i) {
+      mbar_init(smem_u32(&bars->kfull[i]), 3);  // three chunks per group
+      mbar_init(smem_u32(&bars->kempty[i]), 1);
+    }
+    for (int i = 0; i < kVGroups; ++i) {
+      mbar_init(smem_u32(&bars->vfull[i]), 2);  // two chunks per d quarter
+      mbar_init(smem_u32(&bars->vempty[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->q_full), 4);
+    mbar_init(smem_u32(&bars->q_free), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->s_full[b]), 1);
+      mbar_init(smem_u32(&bars->s_free[b]), 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->p_free[b]), 1);
+      mbar_init(smem_u32(&bars->p_full[b]), 1);
+      mbar_init(smem_u32(&bars->pv_done[b]), 1);
+      mbar_init(smem_u32(&bars->side_read[b]), 4);
+    }
+    mbar_init(smem_u32(&bars->o_full), 1);
+    mbar_init(smem_u32(&bars->o_free), 4);
+    mbar_init(smem_u32(&bars->o_drained), 1);
+    mbar_init(smem_u32(&bars->o_rescaled), 4);
+    bars->abort = 0;
+    fence_mbarrier_init();
+    if (rank == 1) {  // both P buffers start empty and armed for their first copy
+      mbar_arrive_expect_tx(smem_u32(&bars->p_full[0]), kXferBytes);
+      mbar_arrive_expect_tx(smem_u32(&bars->p_full[1]), kXferBytes);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before any remote operation
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile uint32_t* abort_flag = &bars->abort;
+
+  if (rank == 0) {
+    // ================================================================ score CTA
+    if (warp == 0 || warp == 2) {
+      // ---------------------------------------------------- K tile producers
+      if (lane == 0) {
+        const int pw = warp >> 1;
+        const uint64_t pol = l2_policy_evict_first();
+        PartCursor cur = part_cursor(meta, part);
+        int q, t0, t1, split;
+        uint32_t tc = 0;
+        int32_t issued[kKGroups];  // ring round of this issuer's last load per group slot
+        for (int i = 0; i < kKGroups; ++i) issued[i] = -1;
+        bool ok = true;
+        while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+          for (int t = t0; t < t1; ++t, ++tc) {
+            if (!ok) continue;
+            int32_t y[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              int32_t blk = page_of(p, q, 2 * t + h2);
+              if (blk < 0) {
+                if (p.err && pw == 0) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
+                blk = static_cast<int32_t>(p.num_pages);  // out of range: TMA fills zeros
+              }
+              y[h2] = blk * kPage;
+            }
+            for (int c = pw; c < kChunks && ok; c += 2) {
+              const int g = c / 3;
+              const uint32_t slot = g, round = tc;  // one ring round per tile
+              ok = mbar_wait(smem_u32(&bars->kempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
+              if (!ok) break;
+              const uint32_t bar = smem_u32(&bars->kfull[slot]);
+              mbar_arrive_expect_tx(bar, kChunk);
+              const uint32_t dst = base + slot * kKGroupBytes + (c - 3 * g) * kChunk;
+              tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol);
+              tma_load_2d(dst + kChunk / 2, &tm_kv, c * 64, y[1], bar, pol);
+              issued[slot] = static_cast<int32_t>(round);
+            }
+          }
+        }
+        if (!ok) {  // let this issuer's copies in flight land before the CTA exits
+          for (int s = 0; s < kKGroups; ++s) {
+            if (issued[s] < 0) continue;
+            const uint64_t t_start = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&bars->kfull[s]), static_cast<uint32_t>(issued[s]) & 1u) &&
+                   globaltimer_ns() - t_start < 1000000ull) {
+            }
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------- S = Q . K^T
+      if (lane == 0) {
+        PartCursor cur = part_cursor(meta, part);
+        int q, t0, t1, split;
+        uint32_t tc = 0, item = 0;
+        bool ok = true;
+        while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+          if (ok) ok = mbar_wait(smem_u32(&bars->q_full), item & 1, abort_flag, p.err);
+          const uint64_t rope_desc = sw128_desc(base + kQRope, 16, 1024);
+          for (int t = t0; t < t1; ++t, ++tc) {
+            if (!ok) continue;
+            const uint32_t sb = tc & 1;
+            ok = mbar_wait(smem_u32(&bars->s_free[sb]), ((tc >> 1) & 1) ^ 1, abort_flag, p.err);
+            if (!ok) continue;
+            tc_fence_after();
+            const uint32_t d = tmem + kSCol + 128 * sb;
+#pragma unroll
+            for (int g = 0; g < 3; ++g) {
+              const uint32_t slot = g;  // group g of every tile lives in slot g
+              ok = mbar_wait(smem_u32(&bars->kfull[slot]), tc & 1, abort_flag, p.err);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t bdesc = sw128_desc(base + slot * kKGroupBytes, 16, 1024);
+#pragma unroll
+              for (int cc = 0; cc < 3; ++cc)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t b = bdesc + static_cast<uint64_t>((cc * kChunk + 32 * k) >> 4);
+                  const uint32_t acc = (g | cc | k) != 0 ? 1u : 0u;
+                  if (3 * g + cc < 8)  // latent columns: A = Q in TMEM
+                    mma_bf16_ts(d, tmem + kQCol + 8 * (4 * (3 * g + cc) + k), b, kIdescS, acc);
+                  else  // RoPE columns: A = Q RoPE part in smem
+                    mma_bf16_ss(d, rope_desc + static_cast<uint64_t>((32 * k) >> 4), b, kIdescS, acc);
+                }
+              mma_commit(smem_u32(&bars->kempty[slot]));
+            }
+            if (!ok) continue;
+            mma_commit(smem_u32(&bars->s_full[sb]));
+            if (t == t1 - 1) mma_commit(smem_u32(&bars->q_free));
+          }
+          ++item;
+        }
+      }
+    } else if (warp >= 4 && warp < 8) {
+      // ---------------------------------------------------- Q load, softmax, P
+      // Thread r owns query row r: its scores are TMEM lane r, so the row max
+      // and sums need no cross-thread exchange.  Probabilities are taken
+      // against a per-row reference m (log2 units): the first tile of a piece
+      // sets it to that tile's row max; a later tile moves it only when a
+      // score exceeds it by more than kRescaleLog2, and then O and the sums
+      // are rescaled by alpha = 2^(m_old - m_new).  Two running sums: of the
+      // fp32 probabilities (for the LSE) and of their bf16 roundings, which
+      // are the weights the PV product multiplies (to normalise O).
+      const int r = threadIdx.x - 128;
+      const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+      const uint32_t t_q = tmem + lane_off + kQCol;
+      const uint32_t stage = base + kStage;
+      const uint32_t prow = stage + (r >> 3) * 1024 + (r & 7) * 128;
+      const uint32_t qrope_row = base + kQRope + (r >> 3) * 1024 + (r & 7) * 128;
+      const float sc = p.scale_log2;
+      PartCursor cur = part_cursor(meta, part);
+      int q, t0, t1, split;
+      uint32_t tc = 0, item = 0;
+      bool ok = true;
+      while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+        const int32_t* srec = meta_seq(meta, p.num_parts, q);
+        const int32_t keys = srec[kSKeys];
+        // Q row r of token q: 512 latent columns -> TMEM (bf16 pairs, even k in
+        // the low half), 64 RoPE columns -> smem (128-byte swizzled row r)
+        if (ok) ok = mbar_wait(smem_u32(&bars->q_free), (item & 1) ^ 1, abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          tc_fence_after();
+          const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(q) * kRows + r) * kDqk);
+#pragma unroll 1
+          for (int blk = 0; blk < kDv / 64; ++blk) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint4 v = ldg_nc_v4(qrow + blk * 8 + i);
+              w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+            }
+            tmem_st32u(t_q + 32 * blk, w);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 v = ldg_nc_v4(qrow + kDv / 8 + u);
+            st_shared_v4(qrope_row + ((u ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+          }
+          tmem_wait_st();
+          fence_proxy_async_smem();
+          tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->q_full));
+        float m_use = 0.f, lsum = 0.f, bsum = 0.f;
+        for (int t = t0; t < t1; ++t, ++tc) {
+          const uint32_t sb = tc & 1;
+          const uint32_t t_s = tmem + lane_off + kSCol + 128 * sb;
+          if (ok) ok = mbar_wait(smem_u32(&bars->s_full[sb]), (tc >> 1) & 1, abort_flag, p.err);
+          ok = __all_sync(0xffffffffu, ok);
+          const int n_valid = keys - t * kTileTokens;  // >= 1; < 128 only on the last tile
+          const bool full = n_valid >= kTileTokens;
+          // pass 1: row max of the raw scores (the scale is positive)
+          float u = -INFINITY;
+          if (ok) {
+            tc_fence_after();
+            float u2 = -INFINITY;
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+              float v[32];
+              tmem_ld32(t_s + 32 * i, v);
+              tmem_wait_ld();
+              if (!full) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 32 * i + j < n_valid ? v[j] : -INFINITY;
+              }
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                u = fmaxf(u, v[j]);
+                u2 = fmaxf(u2, v[j + 1]);
+              }
+            }
+            u = fmaxf(u, u2);
+          }
+          u *= sc;
+          float alpha = 1.f;
+          if (t == t0) {
+            m_use = u == -INFINITY ? 0.f : u;
+          } else if (u > m_use + kRescaleLog2) {
+            alpha = fast_exp2(m_use - u);
+            m_use = u;
+            lsum *= alpha;
+            bsum *= alpha;
+          }
+          const float neg_m = -m_use;
+          const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
+          // pass 2: p = 2^(s * scale - m) -> bf16 P row r in the staging buffer
+          // (two 64-token chunks, 128-byte swizzle), and the two sums
+          named_barrier_sync(1, kXferNamedThreads);  // the previous copy has read the staging
+          float ls = 0.f, bs = 0.f;
+          if (ok) {
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+              float v[32];
+              tmem_ld32(t_s + 32 * i, v);
+              tmem_wait_ld();
+              if (!full) {  // keys past the end: s = -inf, p = 2^-inf = 0
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 32 * i + j < n_valid ? v[j] : -INFINITY;
+              }
+              uint32_t pk[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float e0 = fast_exp2(fmaf(v[2 * j], sc, neg_m));
+                const float e1 = fast_exp2(fmaf(v[2 * j + 1], sc, neg_m));
+                pk[j] = pack_bf16x2(e0, e1);
+                ls += e0 + e1;
+                bs += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
+              }
+              const uint32_t chunk = prow + (i >> 1) * 16384;
+#pragma unroll
+              for (int uu = 0; uu < 4; ++uu)
+                st_shared_v4(chunk + ((((i & 1) * 4 + uu) ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1],
+                             pk[4 * uu + 2], pk[4 * uu + 3]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[sb]));  // S buffer sb may be rewritten
+          lsum += ls;
+          bsum += bs;
+          st_shared_f32(stage + kSideAlpha + 4 * r, alpha);
+          if (t == t1 - 1) st_shared_f32(stage + kSideInvL + 4 * r, bsum > 0.f ? 1.f / bsum : 0.f);
+          if (lane == 0) st_shared_u32(stage + kSideFlags + 4 * (warp - 4), any);
+          fence_proxy_async_smem();
+          named_barrier_arrive(2, kXferNamedThreads);  // staging full
+        }
+        // LSE of row r for this piece
+        const float lse_v = (lsum > 0.f && bsum > 0.f) ? (m_use + __log2f(lsum)) * 0.69314718055994531f
+                                                       : -INFINITY;
+        if (ok) {
+          if (srec[kSNSplits] == 1) {
+            const int b = q / p.s_q, j = q % p.s_q;
+            p.lse[(static_cast<int64_t>(b) * kRows + r) * p.s_q + j] = lse_v;
+          } else {
+            p.ws_lse[static_cast<int64_t>(srec[kSSplitOff] + split) * kRows + r] = lse_v;
+          }
+        }
+        ++item;
+      }
+    } else if (warp == 3) {
+      // ---------------------------------------------------- P transfers
+      PartCursor cur = part_cursor(meta, part);
+      int q, t0, t1, split;
+      uint32_t tc = 0;
+      bool ok = true;
+      while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+        for (int t = t0; t < t1; ++t, ++tc) {
+          if (lane == 0 && tc > 0) bulk_wait_read_all();
+          __syncwarp();
+          named_barrier_arrive(1, kXferNamedThreads);  // staging free
+          named_barrier_sync(2, kXferNamedThreads);    // staging full
+          if (lane == 0 && ok) {
+            const uint32_t b = tc & 1;
+            ok = mbar_wait_cluster(smem_u32(&bars->p_free[b]), ((tc >> 1) & 1) ^ 1, abort_flag, p.err);
+            if (ok) {
+              bulk_copy_to_peer(mapa_shared(base + kPBuf0 + b * kPBufStride, 1), base + kStage, kXferBytes,
+                                mapa_shared(smem_u32(&bars->p_full[b]), 1));
+              bulk_commit_group();
+            }
+          }
+          __syncwarp();
+        }
+      }
+      if (lane == 0) bulk_wait_all();
+    }
+  } else {
+    // ================================================================ output CTA
+    if (warp == 0 || warp == 2) {
+      // ---------------------------------------------------- V tile producers
+      if (lane == 0) {
+        const int pw = warp >> 1;
+        const uint64_t pol = l2_policy_evict_first();
+        PartCursor cur = part_cursor(meta, part);
+        int q, t0, t1, split;
+        uint32_t tc = 0;
+        int32_t issued[kVGroups];
+        for (int i = 0; i < kVGroups; ++i) issued[i] = -1;
+        bool ok = true;
+        while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+          for (int t = t0; t < t1; ++t, ++tc) {
+            if (!ok) continue;
+            int32_t y[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              int32_t blk = page_of(p, q, 2 * t + h2);
+              if (blk < 0) blk = static_cast<int32_t>(p.num_pages);
+              y[h2] = blk * kPage;
+            }
+            for (int c = pw; c < 8 && ok; c += 2) {
+              const uint32_t gv = 4 * tc + (c >> 1), slot = gv % kVGroups, round = gv / kVGroups;
+              ok = mbar_wait(smem_u32(&bars->vempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
+              if (!ok) break;
+              const uint32_t bar = smem_u32(&bars->vfull[slot]);
+              mbar_arrive_expect_tx(bar, kChunk);
+              const uint32_t dst = base + slot * kVGroupBytes + (c & 1) * kChunk;
+              tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol);
+              tma_load_2d(dst + kChunk / 2, &tm_kv, c * 64, y[1], bar, pol);
+              issued[slot] = static_cast<int32_t>(round);
+            }
+          }
+        }
+        if (!ok) {
+          for (int s = 0; s < kVGroups; ++s) {
+            if (issued[s] < 0) continue;
+            const uint64_t t_start = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&bars->vfull[s]), static_cast<uint32_t>(issued[s]) & 1u) &&
+                   globaltimer_ns() - t_start < 1000000ull) {
+            }
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------- O += P . V
+      if (lane == 0) {
+        PartCursor cur = part_cursor(meta, part);
+        int q, t0, t1, split;
+        uint32_t tc = 0, item = 0, rc = 0;
+        bool ok = true;
+        while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+          for (int t = t0; t < t1; ++t, ++tc) {
+            if (!ok) continue;
+            const uint32_t b = tc & 1;
+            const uint32_t pbuf = base + kPBuf0 + b * kPBufStride;
+            ok = mbar_wait_cluster(smem_u32(&bars->p_full[b]), (tc >> 1) & 1, abort_flag, p.err);
+            if (!ok) continue;
+            if (t == t0) {
+              ok = mbar_wait(smem_u32(&bars->o_free), (item & 1) ^ 1, abort_flag, p.err);
+            } else {
+              const uint4 f = ld_shared_v4(pbuf + kSideFlags);
+              if ((f.x | f.y | f.z | f.w) != 0u) {
+                mma_commit(smem_u32(&bars->o_drained));
+                ok = mbar_wait(smem_u32(&bars->o_rescaled), rc & 1, abort_flag, p.err);
+                ++rc;
+              }
+            }
+            if (!ok) continue;
+            tc_fence_after();
+            const uint64_t pdesc = sw128_desc(pbuf, 16, 1024);
+            for (int qd = 0; qd < 4 && ok; ++qd) {
+              const uint32_t gv = 4 * tc + qd, slot = gv % kVGroups;
+              ok = mbar_wait(smem_u32(&bars->vfull[slot]), (gv / kVGroups) & 1, abort_flag, p.err);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t vdesc = sw128_desc(base + slot * kVGroupBytes, kChunk, 1024);
+#pragma unroll
+              for (int s = 0; s < 8; ++s)
+                mma_bf16_ss(tmem + 128 * qd,
+                            pdesc + static_cast<uint64_t>(((s >> 2) * 16384 + (s & 3) * 32) >> 4),
+                            vdesc + static_cast<uint64_t>((2048 * s) >> 4), kIdescO,
+                            (t != t0 || s != 0) ? 1u : 0u);
+              mma_commit(smem_u32(&bars->vempty[slot]));
+            }
+            if (!ok) continue;
+            mma_commit(smem_u32(&bars->pv_done[b]));
+            if (t == t1 - 1) mma_commit(smem_u32(&bars->o_full));
+          }
+          ++item;
+        }
+      }
+    } else if (warp >= 4 && warp < 8) {
+      // ---------------------------------------------------- rescale, epilogue
+      const int r = threadIdx.x - 128;
+      const uint32_t t_o = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16);
+      PartCursor cur = part_cursor(meta, part);
+      int q, t0, t1, split;
+      uint32_t tc = 0, item = 0, rc = 0;
+      bool ok = true;
+      while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+        const int32_t* srec = meta_seq(meta, p.num_parts, q);
+        float inv_l = 0.f;
+        for (int t = t0; t < t1; ++t, ++tc) {
+          const uint32_t b = tc & 1;
+          const uint32_t side = base + kPBuf0 + b * kPBufStride;
+          if (ok) ok = mbar_wait_cluster(smem_u32(&bars->p_full[b]), (tc >> 1) & 1, abort_flag, p.err);
+          ok = __all_sync(0xffffffffu, ok);
+          float alpha = 1.f;
+          uint32_t any = 0;
+          if (ok) {
+            alpha = ld_shared_f32(side + kSideAlpha + 4 * r);
+            const uint4 f = ld_shared_v4(side + kSideFlags);
+            any = f.x | f.y | f.z | f.w;
+            if (t == t1 - 1) inv_l = ld_shared_f32(side + kSideInvL + 4 * r);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->side_read[b]));  // done with the side data
+          if (ok && t != t0 && any != 0u) {
+            ok = mbar_wait(smem_u32(&bars->o_drained), rc & 1, abort_flag, p.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+              tc_fence_after();
+              if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                for (int blk = 0; blk < kDv / 32; ++blk) {
+                  float v[32];
+                  tmem_ld32(t_o + 32 * blk, v);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                  tmem_st32(t_o + 32 * blk, v);
+                }
+                tmem_wait_st();
+              }
+              tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->o_rescaled));
+            ++rc;
+          }
+        }
+        // epilogue: O row r / sum of bf16(p) -> out (single split) or fp32 partial
+        if (ok) ok = mbar_wait(smem_u32(&bars->o_full), item & 1, abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          tc_fence_after();
+          const bool final_out = srec[kSNSplits] == 1;
+          const int64_t row = final_out ? static_cast<int64_t>(q) * kRows + r
+                                        : static_cast<int64_t>(srec[kSSplitOff] + split) * kRows + r;
+#pragma unroll 1
+          for (int blk = 0; blk < kDv / 32; ++blk) {
+            float v[32];
+            tmem_ld32(t_o + 32 * blk, v);
+            tmem_wait_ld();
+            if (final_out) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDv + 32 * blk);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack_bf16x2(v[8 * i] * inv_l, v[8 * i + 1] * inv_l),
+                                    pack_bf16x2(v[8 * i + 2] * inv_l, v[8 * i + 3] * inv_l),
+                                    pack_bf16x2(v[8 * i + 4] * inv_l, v[8 * i + 5] * inv_l),
+                                    pack_bf16x2(v[8 * i + 6] * inv_l, v[8 * i + 7] * inv_l));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(p.ws_o + row * kDv + 32 * blk);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(v[4 * i] * inv_l, v[4 * i + 1] * inv_l, v[4 * i + 2] * inv_l,
+                                     v[4 * i + 3] * inv_l);
+            }
+          }
+          tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));
+        ++item;
+      }
+    } else if (warp == 3) {
+      // ---------------------------------------------------- P buffer hand-back
+      PartCursor cur = part_cursor(meta, part);
+      int q, t0, t1, split;
+      uint32_t tc = 0;
+      bool ok = true;
+      while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+        for (int t = t0; t < t1; ++t, ++tc) {
+          if (lane == 0 && ok) {
+            const uint32_t b = tc & 1;
+            ok = mbar_wait(smem_u32(&bars->side_read[b]), (tc >> 1) & 1, abort_flag, p.err);
+            if (ok) ok = mbar_wait(smem_u32(&bars->pv_done[b]), (tc >> 1) & 1, abort_flag, p.err);
+            if (ok) {
+              mbar_arrive_expect_tx(smem_u32(&bars->p_full[b]), kXferBytes);  // armed for tile tc + 2
+              mbar_remote_arrive(mapa_shared(smem_u32(&bars->p_free[b]), 0));
+            }
+          }
+          __syncwarp();
+        }
+      }
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no peer still copies into or arrives on this CTA's smem
+  pdl_launch_dependents();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace pair
+}  // namespace mla
