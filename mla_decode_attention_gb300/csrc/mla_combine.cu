@@ -13,69 +13,87 @@ namespace mla {
 
 namespace {
 
-constexpr int kCombineThreads = 128;  // 4 output columns per thread
-constexpr int kMaxSplitsCached = 64;
+constexpr int kCombineWarps = 8;  // one output row (query token, head) per warp
+constexpr int kCombineThreads = 32 * kCombineWarps;
 
+// Lane l of a warp owns output columns [16 l, 16 l + 16): each split row is read
+// as 2 KB contiguous per warp, and the bf16 row is written as 1 KB contiguous.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const int32_t* __restrict__ meta, int h, int s_q, int num_parts, const float* __restrict__ ws_o,
     const float* __restrict__ ws_lse, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  // The split kernel's writes are visible only after the primary grid is done.
-  pdl_wait_primary();
-  const int q = blockIdx.x, head = blockIdx.y;
+  const int q = blockIdx.x;
+  const int head = blockIdx.y * kCombineWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  // The schedule was written before the split kernel started; only the
+  // partials need the split kernel to be done.
   const int32_t* s = meta_seq(meta, num_parts, q);
   const int n_splits = s[kSNSplits];
-  if (n_splits == 1) return;
+  const int off = s[kSSplitOff];
+  pdl_wait_primary();
+  if (head >= h || n_splits == 1) return;  // single split: written by the split kernel
   const int b = q / s_q, j = q % s_q;
-  __nv_bfloat16* orow = out + (static_cast<int64_t>(q) * h + head) * kDv;
+  __nv_bfloat16* orow = out + (static_cast<int64_t>(q) * h + head) * kDv + 16 * lane;
   float* lse_out = lse + (static_cast<int64_t>(b) * h + head) * s_q + j;
-  const int d = threadIdx.x * 4;
   if (n_splits == 0) {  // no visible key: out = 0, lse = -inf
-    const __nv_bfloat162 z = __floats2bfloat162_rn(0.f, 0.f);
-    reinterpret_cast<__nv_bfloat162*>(orow + d)[0] = z;
-    reinterpret_cast<__nv_bfloat162*>(orow + d)[1] = z;
-    if (threadIdx.x == 0) *lse_out = -INFINITY;
+    reinterpret_cast<uint4*>(orow)[0] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(orow)[1] = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) *lse_out = -INFINITY;
     return;
   }
-  const int off = s[kSSplitOff];
-  __shared__ float w_sm[kMaxSplitsCached];
-  __shared__ float lse_sm;
-  if (threadIdx.x < 32) {
-    float mx = -INFINITY;
-    for (int i = threadIdx.x; i < n_splits; i += 32)
-      mx = fmaxf(mx, ws_lse[static_cast<int64_t>(off + i) * h + head]);
+  // merged lse = ref + ln sum_i exp(lse_i - ref), ref = max_i lse_i
+  float mx = -INFINITY;
+  for (int i = lane; i < n_splits; i += 32) mx = fmaxf(mx, ws_lse[static_cast<int64_t>(off + i) * h + head]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float ref = (mx == -INFINITY) ? 0.f : mx;
-    float sum = 0.f;
-    for (int i = threadIdx.x; i < n_splits; i += 32) {
-      const float e = __expf(ws_lse[static_cast<int64_t>(off + i) * h + head] - ref);
-      sum += e;
-      if (i < kMaxSplitsCached) w_sm[i] = e;
-    }
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float ref = (mx == -INFINITY) ? 0.f : mx;
+  float my_e = 0.f, sum = 0.f;
+  for (int i = lane; i < n_splits; i += 32) {
+    const float e = __expf(ws_lse[static_cast<int64_t>(off + i) * h + head] - ref);
+    if (i < 32) my_e = e;
+    sum += e;
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float total_lse = sum > 0.f ? ref + __logf(sum) : -INFINITY;
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    for (int i = threadIdx.x; i < n_splits && i < kMaxSplitsCached; i += 32) w_sm[i] *= inv;
-    if (threadIdx.x == 0) lse_sm = total_lse;
-  }
-  __syncthreads();
-  const float tl = lse_sm;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = 0; i < n_splits; ++i) {
-    float w;
-    if (i < kMaxSplitsCached) {
-      w = w_sm[i];
-    } else {
-      const float li = ws_lse[static_cast<int64_t>(off + i) * h + head];
-      w = tl == -INFINITY ? 0.f : __expf(li - tl);
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float total_lse = sum > 0.f ? ref + __logf(sum) : -INFINITY;
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  const float* base = ws_o + (static_cast<int64_t>(off) * h + head) * kDv + 16 * lane;
+  const int64_t split_stride = static_cast<int64_t>(h) * kDv;
+  for (int i0 = 0; i0 < n_splits; i0 += 4) {
+    float4 o[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u < n_splits) {
+        const float4* src = reinterpret_cast<const float4*>(base + (i0 + u) * split_stride);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[u][c] = src[c];
+      }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u;
+      if (i >= n_splits) break;
+      float w;
+      if (i < 32) {
+        w = __shfl_sync(0xffffffffu, my_e, i) * inv;
+      } else {
+        const float li = ws_lse[static_cast<int64_t>(off + i) * h + head];
+        w = __expf(li - ref) * inv;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        acc[4 * c] += w * o[u][c].x; acc[4 * c + 1] += w * o[u][c].y;
+        acc[4 * c + 2] += w * o[u][c].z; acc[4 * c + 3] += w * o[u][c].w;
+      }
     }
-    const float4 o = *reinterpret_cast<const float4*>(ws_o + (static_cast<int64_t>(off + i) * h + head) * kDv + d);
-    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
   }
-  reinterpret_cast<__nv_bfloat162*>(orow + d)[0] = __floats2bfloat162_rn(acc.x, acc.y);
-  reinterpret_cast<__nv_bfloat162*>(orow + d)[1] = __floats2bfloat162_rn(acc.z, acc.w);
-  if (threadIdx.x == 0) *lse_out = tl;
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+  reinterpret_cast<uint4*>(orow)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  reinterpret_cast<uint4*>(orow)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  if (lane == 0) *lse_out = total_lse;
 }
 
 }  // namespace
@@ -86,7 +104,7 @@ int launch_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm
   const float* ws_o = static_cast<const float*>(workspace);
   const float* ws_lse = ws_o + rows * kDv;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(batch * s_q, h_q, 1);
+  cfg.gridDim = dim3(batch * s_q, (h_q + kCombineWarps - 1) / kCombineWarps, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -70,6 +70,7 @@ constexpr int kVGroupBytes = 2 * kChunk;           // 32 KB
 constexpr int kPBuf0 = kVGroups * kVGroupBytes;    // 131072
 constexpr int kPBufStride = 34816;                 // kXferBytes rounded up to 1 KB
 constexpr int kBarOffset = kPBuf0 + 2 * kPBufStride;  // 200704 (score CTA ends at 197648)
+constexpr int kEpi = kBarOffset + 1024;            // output CTA: 4 KB per row warp for the epilogue
 // TMEM columns
 constexpr uint32_t kQCol = 0;                      // score CTA: Q latent part, 256 columns
 constexpr uint32_t kSCol = 256;                    // score CTA: S buffers at 256 and 384
@@ -88,8 +89,9 @@ struct Bars {
   uint32_t tmem_base;
   uint32_t abort;
 };
-constexpr int kSmemBytes = kBarOffset + static_cast<int>(sizeof(Bars)) + 1024;
+constexpr int kSmemBytes = kEpi + 4 * 4096 + 1024;
 static_assert(kBarOffset % 16 == 0, "barrier block alignment");
+static_assert(sizeof(Bars) <= 1024, "barrier block size");
 static_assert(kStage + kXferBytes <= kBarOffset, "score CTA layout");
 static_assert(kXferBytes <= kPBufStride && kXferBytes % 16 == 0, "P transfer size");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -276,20 +278,37 @@ __global__ void __maxnreg__(224)
         if (ok) {
           tc_fence_after();
           const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(q) * kRows + r) * kDqk);
-#pragma unroll 1
-          for (int blk = 0; blk < kDv / 64; ++blk) {
-            uint32_t w[32];
+          // 72 16-byte units = nine blocks of 8 (blocks 0..7 latent, block 8 RoPE),
+          // read three blocks per round so that 24 loads are in flight at once
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint4 v = ldg_nc_v4(qrow + blk * 8 + i);
-              w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+          for (int rnd = 0; rnd < 3; ++rnd) {
+            uint4 v[24];
+#pragma unroll
+            for (int i = 0; i < 24; ++i) v[i] = ldg_nc_v4(qrow + 24 * rnd + i);
+#pragma unroll
+            for (int bb = 0; bb < 3; ++bb) {
+              const int blk = 3 * rnd + bb;
+              if (blk < kDv / 64) {
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  w[4 * i] = v[8 * bb + i].x; w[4 * i + 1] = v[8 * bb + i].y;
+                  w[4 * i + 2] = v[8 * bb + i].z; w[4 * i + 3] = v[8 * bb + i].w;
+                }
+                tmem_st32u(t_q + 32 * blk, w);
+              } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  st_shared_v4(qrope_row + ((u ^ (r & 7)) << 4), v[8 * bb + u].x, v[8 * bb + u].y,
+                               v[8 * bb + u].z, v[8 * bb + u].w);
+              }
             }
-            tmem_st32u(t_q + 32 * blk, w);
           }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 v = ldg_nc_v4(qrow + kDv / 8 + u);
-            st_shared_v4(qrope_row + ((u ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+          if (r == 0) {  // the next piece's query rows (147 KB, contiguous) start towards L2
+            PartCursor nc = cur;
+            int nq, nt0, nt1, nsplit;
+            if (next_piece(meta, p.num_parts, &nc, &nq, &nt0, &nt1, &nsplit))
+              prefetch_l2(p.q + static_cast<int64_t>(nq) * kRows * kDqk, kRows * kDqk * 2);
           }
           tmem_wait_st();
           fence_proxy_async_smem();
@@ -568,28 +587,58 @@ __global__ void __maxnreg__(224)
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
           tc_fence_after();
+          // Thread r holds row r of O; each 128-byte slice of the warp's 32 rows
+          // goes through a swizzled 4 KB staging area so that every global
+          // store instruction writes four whole 128-byte row segments.
           const bool final_out = srec[kSNSplits] == 1;
-          const int64_t row = final_out ? static_cast<int64_t>(q) * kRows + r
-                                        : static_cast<int64_t>(srec[kSSplitOff] + split) * kRows + r;
+          const int64_t row0 = (final_out ? static_cast<int64_t>(q) : static_cast<int64_t>(srec[kSSplitOff] + split)) *
+                                   kRows + 32 * (warp - 4);
+          const uint32_t stg = base + kEpi + (warp - 4) * 4096;
+          const int rr0 = lane >> 3, uu = lane & 7;
+          if (final_out) {
 #pragma unroll 1
-          for (int blk = 0; blk < kDv / 32; ++blk) {
-            float v[32];
-            tmem_ld32(t_o + 32 * blk, v);
-            tmem_wait_ld();
-            if (final_out) {
-              uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDv + 32 * blk);
+            for (int blk = 0; blk < kDv / 64; ++blk) {  // 64 bf16 columns = 128 bytes per row
+              uint32_t pk[32];
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(pack_bf16x2(v[8 * i] * inv_l, v[8 * i + 1] * inv_l),
-                                    pack_bf16x2(v[8 * i + 2] * inv_l, v[8 * i + 3] * inv_l),
-                                    pack_bf16x2(v[8 * i + 4] * inv_l, v[8 * i + 5] * inv_l),
-                                    pack_bf16x2(v[8 * i + 6] * inv_l, v[8 * i + 7] * inv_l));
-            } else {
-              float4* dst = reinterpret_cast<float4*>(p.ws_o + row * kDv + 32 * blk);
+              for (int h2 = 0; h2 < 2; ++h2) {
+                float v[32];
+                tmem_ld32(t_o + 64 * blk + 32 * h2, v);
+                tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(v[4 * i] * inv_l, v[4 * i + 1] * inv_l, v[4 * i + 2] * inv_l,
-                                     v[4 * i + 3] * inv_l);
+                for (int i = 0; i < 16; ++i) pk[16 * h2 + i] = pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                             pk[4 * u + 3]);
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int rr = 4 * j + rr0;
+                const uint4 x = ld_shared_v4(stg + rr * 128 + ((uu ^ (rr & 7)) << 4));
+                *reinterpret_cast<uint4*>(p.out + (row0 + rr) * kDv + 64 * blk + 8 * uu) = x;
+              }
+              __syncwarp();
+            }
+          } else {
+#pragma unroll 1
+            for (int blk = 0; blk < kDv / 32; ++blk) {  // 32 fp32 columns = 128 bytes per row
+              float v[32];
+              tmem_ld32(t_o + 32 * blk, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) << 4), __float_as_uint(v[4 * u] * inv_l),
+                             __float_as_uint(v[4 * u + 1] * inv_l), __float_as_uint(v[4 * u + 2] * inv_l),
+                             __float_as_uint(v[4 * u + 3] * inv_l));
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int rr = 4 * j + rr0;
+                const uint4 x = ld_shared_v4(stg + rr * 128 + ((uu ^ (rr & 7)) << 4));
+                *reinterpret_cast<uint4*>(p.ws_o + (row0 + rr) * kDv + 32 * blk + 4 * uu) = x;
+              }
+              __syncwarp();
             }
           }
           tc_fence_before();
