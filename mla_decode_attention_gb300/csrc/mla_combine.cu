@@ -18,7 +18,9 @@ constexpr int kCombineThreads = 32 * kCombineWarps;
 
 // Lane l of a warp owns output columns [16 l, 16 l + 16): each split row is read
 // as 2 KB contiguous per warp, and the bf16 row is written as 1 KB contiguous.
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+// At most 64 registers per thread: four CTAs (32 warps) per SM, so that one
+// or two waves cover the rows of a typical batch.
+__global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(
     const int32_t* __restrict__ meta, int h, int s_q, int num_parts, const float* __restrict__ ws_o,
     const float* __restrict__ ws_lse, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   const int q = blockIdx.x;
@@ -40,52 +42,48 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     if (lane == 0) *lse_out = -INFINITY;
     return;
   }
-  // merged lse = ref + ln sum_i exp(lse_i - ref), ref = max_i lse_i
-  float mx = -INFINITY;
-  for (int i = lane; i < n_splits; i += 32) mx = fmaxf(mx, ws_lse[static_cast<int64_t>(off + i) * h + head]);
+  const float4* src = reinterpret_cast<const float4*>(ws_o + (static_cast<int64_t>(off) * h + head) * kDv) + 4 * lane;
+  const int64_t split_stride = static_cast<int64_t>(h) * kDv / 4;  // in float4
+  // split 0's row is requested before the weights are known; split i + 1's
+  // while split i is accumulated
+  float4 cur[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  for (int c = 0; c < 4; ++c) cur[c] = src[c];
+  // merged lse = ref + ln sum_i exp(lse_i - ref), ref = max_i lse_i
+  const float* lrow = ws_lse + static_cast<int64_t>(off) * h + head;
+  float mx = -INFINITY;
+  for (int i = lane; i < n_splits; i += 32) mx = fmaxf(mx, lrow[static_cast<int64_t>(i) * h]);
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
   const float ref = (mx == -INFINITY) ? 0.f : mx;
   float my_e = 0.f, sum = 0.f;
   for (int i = lane; i < n_splits; i += 32) {
-    const float e = __expf(ws_lse[static_cast<int64_t>(off + i) * h + head] - ref);
+    const float e = __expf(lrow[static_cast<int64_t>(i) * h] - ref);
     if (i < 32) my_e = e;
     sum += e;
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
   const float total_lse = sum > 0.f ? ref + __logf(sum) : -INFINITY;
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  const float* base = ws_o + (static_cast<int64_t>(off) * h + head) * kDv + 16 * lane;
-  const int64_t split_stride = static_cast<int64_t>(h) * kDv;
-  for (int i0 = 0; i0 < n_splits; i0 += 4) {
-    float4 o[4][4];
+  for (int i = 0; i < n_splits; ++i) {
+    float4 nxt[4];
+    if (i + 1 < n_splits) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (i0 + u < n_splits) {
-        const float4* src = reinterpret_cast<const float4*>(base + (i0 + u) * split_stride);
+      for (int c = 0; c < 4; ++c) nxt[c] = src[(i + 1) * split_stride + c];
+    }
+    const float w = (i < 32 ? __shfl_sync(0xffffffffu, my_e, i & 31) : __expf(lrow[static_cast<int64_t>(i) * h] - ref)) * inv;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) o[u][c] = src[c];
-      }
+    for (int c = 0; c < 4; ++c) {
+      acc[4 * c] += w * cur[c].x; acc[4 * c + 1] += w * cur[c].y;
+      acc[4 * c + 2] += w * cur[c].z; acc[4 * c + 3] += w * cur[c].w;
+    }
+    if (i + 1 < n_splits) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u;
-      if (i >= n_splits) break;
-      float w;
-      if (i < 32) {
-        w = __shfl_sync(0xffffffffu, my_e, i) * inv;
-      } else {
-        const float li = ws_lse[static_cast<int64_t>(off + i) * h + head];
-        w = __expf(li - ref) * inv;
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        acc[4 * c] += w * o[u][c].x; acc[4 * c + 1] += w * o[u][c].y;
-        acc[4 * c + 2] += w * o[u][c].z; acc[4 * c + 3] += w * o[u][c].w;
-      }
+      for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
     }
   }
   uint32_t pk[8];

@@ -111,13 +111,17 @@ int launch_pair(const CUtensorMap& tm_kv, const SplitParams& prm, cudaStream_t s
   cfg.blockDim = dim3(pair::kThreads, 1, 1);
   cfg.dynamicSmemBytes = pair::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // the kernel's prologue overlaps the previous kernel (e.g. the schedule);
+  // it waits for that kernel's results before reading any input
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::mla_pair_kernel, tm_kv, prm);
   return e == cudaSuccess ? MLA_OK : record_cuda_error("pair kernel launch", e);
 }

@@ -5,6 +5,7 @@
 
 #include "mla_decode.h"
 #include "mla_internal.h"
+#include "mla_ptx.cuh"
 #include "mla_schedule.cuh"
 
 namespace mla {
@@ -47,6 +48,9 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
                                                                 int s_q, int causal, int topk,
                                                                 int num_parts, int32_t* meta) {
   __shared__ int64_t warp_sums[32];
+  // a decode kernel launched next may start its prologue; it waits for this
+  // grid to complete before it reads the schedule
+  pdl_launch_dependents();
   const int n_seq = batch * s_q;
   const int chunk = (n_seq + kMetaThreads - 1) / kMetaThreads;
   const int q0 = threadIdx.x * chunk;

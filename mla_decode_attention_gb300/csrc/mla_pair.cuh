@@ -150,6 +150,10 @@ __global__ void __maxnreg__(224)
   __syncthreads();
   cluster_sync();  // the peer's barriers exist before any remote operation
   tc_fence_after();
+  // Everything above overlaps the previous kernel of the stream (programmatic
+  // dependent launch); its results (the schedule, the inputs) are read below.
+  pdl_wait_primary();
+  pdl_launch_dependents();  // the combine may launch now; it waits for this grid to finish
   const uint32_t tmem = bars->tmem_base;
   volatile uint32_t* abort_flag = &bars->abort;
 
@@ -674,7 +678,6 @@ __global__ void __maxnreg__(224)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no peer still copies into or arrives on this CTA's smem
-  pdl_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
