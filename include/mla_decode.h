@@ -101,7 +101,7 @@ int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes);
  *   dense, non-causal:  cache_seqlens[b]
  *   sparse (topk > 0):  topk   (cache_seqlens ignored, may be NULL)
  * Sequences are cut into 128-key tiles and the tiles are dealt out as
- * contiguous ranges of balanced cost (tiles + 1 per sequence piece) to the
+ * contiguous ranges of balanced cost (tiles + 2 per sequence piece) to the
  * parts; a sequence cut between parts becomes several splits that the
  * combine step merges.  Layout of `metadata` (int32):
  *   [0,16)                    header: magic 0x4D4C4131, version, n_seq,

@@ -154,6 +154,12 @@ __global__ void __maxnreg__(224)
   // dependent launch); its results (the schedule, the inputs) are read below.
   pdl_wait_primary();
   pdl_launch_dependents();  // the combine may launch now; it waits for this grid to finish
+  if (threadIdx.x == 0 && rank == 0) {  // the first piece's query rows start towards L2
+    PartCursor c0 = part_cursor(meta, part);
+    int q0, a0, b0, s0;
+    if (next_piece(meta, p.num_parts, &c0, &q0, &a0, &b0, &s0))
+      prefetch_l2(p.q + static_cast<int64_t>(q0) * kRows * kDqk, kRows * kDqk * 2);
+  }
   const uint32_t tmem = bars->tmem_base;
   volatile uint32_t* abort_flag = &bars->abort;
 

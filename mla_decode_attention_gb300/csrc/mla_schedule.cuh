@@ -20,7 +20,7 @@
 namespace mla {
 
 constexpr int kTileTokens = 128;
-constexpr int kFixedCost = 1;
+constexpr int kFixedCost = 2;  // a piece switch (Q load, epilogue) costs about two tiles
 constexpr int32_t kMetaMagic = 0x4D4C4131;  // "MLA1"
 constexpr int32_t kMetaVersion = 1;
 
