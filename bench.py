@@ -185,8 +185,9 @@ def run_ours(args, rank, world, local_rank):
         if sparse:
             if not split_only:
                 binding.mla_get_metadata(None, b, s_q, False, w.topk, parts, buf.metadata, stream)
-            binding.mla_sparse_decode(s["q"], s["kv"], s["indices"], scale, buf.metadata, parts,
-                                      buf.workspace, buf.out, buf.lse, buf.err, stream)
+            fn = binding.mla_sparse_decode_splitkv if split_only else binding.mla_sparse_decode
+            fn(s["q"], s["kv"], s["indices"], scale, buf.metadata, parts, buf.workspace, buf.out,
+               buf.lse, buf.err, stream)
         elif not split_only:
             binding.mla_get_metadata(s["cache_seqlens"], b, s_q, True, 0, parts, buf.metadata,
                                      stream)
@@ -337,7 +338,7 @@ def run_ours(args, rank, world, local_rank):
     else:
         achieved, peak, unit = flops / (split_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     # the split kernel the library dispatches to: two-SM kernel for 128 bf16 query rows
-    kernel_name = "mla_pair_kernel" if (w.kind == "dense" and h == 128) else "mla_splitkv_kernel"
+    kernel_name = "mla_pair_kernel" if (w.kind in ("dense", "sparse") and h == 128) else "mla_splitkv_kernel"
     traffic = recorded_traffic(kernel_name, args.config)
 
     result = {

@@ -192,6 +192,17 @@ int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv, const int32_t
                       const void* metadata, int num_sm_parts, void* workspace, void* out,
                       float* lse, uint32_t* err, cudaStream_t stream);
 
+/*
+ * The split-KV kernel of mla_sparse_decode alone (the sparse counterpart of
+ * mla_decode_splitkv).  Same arguments and layouts; rows whose keys were cut
+ * into several splits need a following mla_combine on the same metadata and
+ * workspace.
+ */
+int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv, const int32_t* indices,
+                              int topk, int batch, int s_q, int h_q, float softmax_scale,
+                              const void* metadata, int num_sm_parts, void* workspace, void* out,
+                              float* lse, uint32_t* err, cudaStream_t stream);
+
 /* Size of the device scratch array that mla_decode_noalloc uses (40 MiB). */
 #define MLA_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
 

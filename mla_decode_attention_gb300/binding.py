@@ -51,6 +51,8 @@ _SIGS = {
                                 _vp, _vp]),
     "mla_sparse_decode": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _i, _vp, _vp, _vp,
                                _vp, _vp]),
+    "mla_sparse_decode_splitkv": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _i, _vp, _vp, _vp,
+                               _vp, _vp]),
     "mla_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
 }
 
@@ -220,11 +222,10 @@ def mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, kv_format: int,
         int(bool(causal)), _ptr(out), _ptr(lse), _ptr(err), _stream(stream)))
 
 
-def mla_sparse_decode(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,
-                      softmax_scale: float, metadata: torch.Tensor, num_sm_parts: int,
-                      workspace: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
-                      err: Optional[torch.Tensor] = None, stream=None) -> None:
-    """q [b, s_q, h, 576] bf16; kv [s_kv, 576] bf16; indices [b, s_q, topk] int32."""
+def _sparse_call(name, q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,
+                 softmax_scale: float, metadata: torch.Tensor, num_sm_parts: int,
+                 workspace: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+                 err: Optional[torch.Tensor] = None, stream=None) -> None:
     _dev(q, torch.bfloat16, "q")
     _dev(kv, torch.bfloat16, "kv")
     _dev(indices, torch.int32, "indices")
@@ -235,11 +236,25 @@ def mla_sparse_decode(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,
         _dev(err, torch.int32, "err")
     b, s_q, h, d = q.shape
     topk = indices.shape[-1]
-    _check("mla_sparse_decode",
-           lib().mla_sparse_decode(_ptr(q), _ptr(kv), kv.shape[0], _ptr(indices), topk, b, s_q,
-                                   h, float(softmax_scale), _ptr(metadata), num_sm_parts,
-                                   _ptr(workspace), _ptr(out), _ptr(lse), _ptr(err),
-                                   _stream(stream)))
+    _check(name,
+           getattr(lib(), name)(_ptr(q), _ptr(kv), kv.shape[0], _ptr(indices), topk, b, s_q,
+                                h, float(softmax_scale), _ptr(metadata), num_sm_parts,
+                                _ptr(workspace), _ptr(out), _ptr(lse), _ptr(err),
+                                _stream(stream)))
+
+
+def mla_sparse_decode(q, kv, indices, softmax_scale, metadata, num_sm_parts, workspace, out, lse,
+                      err=None, stream=None) -> None:
+    """q [b, s_q, h, 576] bf16; kv [s_kv, 576] bf16; indices [b, s_q, topk] int32."""
+    _sparse_call("mla_sparse_decode", q, kv, indices, softmax_scale, metadata, num_sm_parts,
+                 workspace, out, lse, err, stream)
+
+
+def mla_sparse_decode_splitkv(q, kv, indices, softmax_scale, metadata, num_sm_parts, workspace,
+                              out, lse, err=None, stream=None) -> None:
+    """The split kernel of mla_sparse_decode alone (partials need mla_combine)."""
+    _sparse_call("mla_sparse_decode_splitkv", q, kv, indices, softmax_scale, metadata,
+                 num_sm_parts, workspace, out, lse, err, stream)
 
 
 def mla_combine(metadata: torch.Tensor, batch: int, s_q: int, h_q: int, num_sm_parts: int,

@@ -93,14 +93,15 @@ int launch_split(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const SplitP
   return e == cudaSuccess ? MLA_OK : record_cuda_error("split kernel launch", e);
 }
 
+template <bool kSparse>
 int launch_pair(const CUtensorMap& tm_kv, const SplitParams& prm, cudaStream_t stream) {
-  static int state = 0;  // 0 unset, 1 ok, -1 failed
+  static int state = 0;  // 0 unset, 1 ok, -1 failed (per instantiation)
   static std::mutex mu;
   {
     std::lock_guard<std::mutex> lock(mu);
     if (state == 0) {
       const cudaError_t e = cudaFuncSetAttribute(
-          pair::mla_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes);
+          pair::mla_pair_kernel<kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes);
       state = e == cudaSuccess ? 1 : -1;
       if (e != cudaSuccess) return record_cuda_error("cudaFuncSetAttribute(pair kernel)", e);
     }
@@ -122,7 +123,7 @@ int launch_pair(const CUtensorMap& tm_kv, const SplitParams& prm, cudaStream_t s
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::mla_pair_kernel, tm_kv, prm);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::mla_pair_kernel<kSparse>, tm_kv, prm);
   return e == cudaSuccess ? MLA_OK : record_cuda_error("pair kernel launch", e);
 }
 
@@ -192,7 +193,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
   if (fp8) return launch_split<KvMode::kPagedFp8>(tm_q, tm_kv, prm, stream);
   // 128 query rows: the two-SM kernel (scores and softmax on one SM, P.V on the other)
-  if (h_q == pair::kRows) return launch_pair(tm_kv, prm, stream);
+  if (h_q == pair::kRows) return launch_pair<false>(tm_kv, prm, stream);
   return launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);
 }
 
@@ -210,11 +211,11 @@ extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, in
   return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, out, lse, stream, true);
 }
 
-extern "C" int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv,
-                                 const int32_t* indices, int topk, int batch, int s_q, int h_q,
-                                 float softmax_scale, const void* metadata, int num_sm_parts,
-                                 void* workspace, void* out, float* lse, uint32_t* err,
-                                 cudaStream_t stream) {
+extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv,
+                                         const int32_t* indices, int topk, int batch, int s_q,
+                                         int h_q, float softmax_scale, const void* metadata,
+                                         int num_sm_parts, void* workspace, void* out, float* lse,
+                                         uint32_t* err, cudaStream_t stream) {
   int rc = check_common(batch, s_q, h_q, num_sm_parts);
   if (rc != MLA_OK) return rc;
   if (!q || !kv || !indices || !metadata || !workspace || !out || !lse) return MLA_ERR_NULL;
@@ -252,7 +253,19 @@ extern "C" int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv,
   prm.n_hblk = head_blocks(h_q);
   prm.rows = rows;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
-  rc = launch_split<KvMode::kSparseBf16>(tm_q, tm_kv, prm, stream);
+  // 128 query rows: the two-SM kernel with gathered keys
+  return h_q == pair::kRows ? launch_pair<true>(tm_kv, prm, stream)
+                            : launch_split<KvMode::kSparseBf16>(tm_q, tm_kv, prm, stream);
+}
+
+extern "C" int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv,
+                                 const int32_t* indices, int topk, int batch, int s_q, int h_q,
+                                 float softmax_scale, const void* metadata, int num_sm_parts,
+                                 void* workspace, void* out, float* lse, uint32_t* err,
+                                 cudaStream_t stream) {
+  const int rc = mla_sparse_decode_splitkv(q, kv, s_kv, indices, topk, batch, s_q, h_q,
+                                           softmax_scale, metadata, num_sm_parts, workspace, out,
+                                           lse, err, stream);
   if (rc != MLA_OK) return rc;
   return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, out, lse, stream, true);
 }

@@ -98,6 +98,10 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // One CTA per SM (shared memory); up to 224 registers per thread (8 warps, two
 // per sub-partition), so each row thread's 128 scores stay in registers.
+// kSparse: keys are pool rows named by p.indices (DSA top-k, -1 = none), read
+// with tile::gather4 (the tensor map's box is one row); otherwise pages of the
+// block table, read as [64 rows x 64 columns] boxes.
+template <bool kSparse>
 __global__ void __maxnreg__(224)
     mla_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -167,7 +171,10 @@ __global__ void __maxnreg__(224)
     // ================================================================ score CTA
     if (warp == 0 || warp == 2) {
       // ---------------------------------------------------- K tile producers
-      if (lane == 0) {
+      // Dense: lane 0 loads each chunk as two page boxes.  Sparse: lane L
+      // gathers rows 4L..4L+3 of the tile for each chunk (invalid slots fetch
+      // pool row 0; the softmax gives them zero weight); lane 0 owns the barriers.
+      if (lane == 0 || kSparse) {
         const int pw = warp >> 1;
         const uint64_t pol = l2_policy_evict_first();
         PartCursor cur = part_cursor(meta, part);
@@ -179,31 +186,50 @@ __global__ void __maxnreg__(224)
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
-            int32_t y[2];
+            int32_t y[4];
+            if constexpr (kSparse) {
+              const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              int32_t blk = page_of(p, q, 2 * t + h2);
-              if (blk < 0) {
-                if (p.err && pw == 0) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
-                blk = static_cast<int32_t>(p.num_pages);  // out of range: TMA fills zeros
+              for (int i = 0; i < 4; ++i) {
+                const int slot = t * kTileTokens + 4 * lane + i;
+                const int32_t id = slot < p.topk ? idx_row[slot] : -1;
+                const bool valid = id >= 0 && static_cast<int64_t>(id) < p.s_kv;
+                if (!valid && id != -1 && p.err && pw == 0) atomicOr(p.err, MLA_DEVERR_BAD_INDEX);
+                y[i] = valid ? id : 0;
               }
-              y[h2] = blk * kPage;
+            } else {
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                int32_t blk = page_of(p, q, 2 * t + h2);
+                if (blk < 0) {
+                  if (p.err && pw == 0) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
+                  blk = static_cast<int32_t>(p.num_pages);  // out of range: TMA fills zeros
+                }
+                y[h2] = blk * kPage;
+              }
             }
             for (int c = pw; c < kChunks && ok; c += 2) {
               const int g = c / 3;
               const uint32_t slot = g, round = tc;  // one ring round per tile
-              ok = mbar_wait(smem_u32(&bars->kempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
+              if (lane == 0) {
+                ok = mbar_wait(smem_u32(&bars->kempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
+                if (ok) mbar_arrive_expect_tx(smem_u32(&bars->kfull[slot]), kChunk);
+              }
+              if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
               if (!ok) break;
               const uint32_t bar = smem_u32(&bars->kfull[slot]);
-              mbar_arrive_expect_tx(bar, kChunk);
               const uint32_t dst = base + slot * kKGroupBytes + (c - 3 * g) * kChunk;
-              tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol);
-              tma_load_2d(dst + kChunk / 2, &tm_kv, c * 64, y[1], bar, pol);
+              if constexpr (kSparse) {
+                tma_gather4(dst + 4 * lane * 128, &tm_kv, c * 64, y[0], y[1], y[2], y[3], bar);
+              } else {
+                tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol);
+                tma_load_2d(dst + kChunk / 2, &tm_kv, c * 64, y[1], bar, pol);
+              }
               issued[slot] = static_cast<int32_t>(round);
             }
           }
         }
-        if (!ok) {  // let this issuer's copies in flight land before the CTA exits
+        if (!ok && lane == 0) {  // let this issuer's copies in flight land before the CTA exits
           for (int s = 0; s < kKGroups; ++s) {
             if (issued[s] < 0) continue;
             const uint64_t t_start = globaltimer_ns();
@@ -330,10 +356,24 @@ __global__ void __maxnreg__(224)
         for (int t = t0; t < t1; ++t, ++tc) {
           const uint32_t sb = tc & 1;
           const uint32_t t_s = tmem + lane_off + kSCol + 128 * sb;
+          // sparse: bit L of vm[k] = key slot t * 128 + 32 k + L names a pool row
+          uint32_t vm[4] = {~0u, ~0u, ~0u, ~0u};
+          if constexpr (kSparse) {
+            const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
+            int32_t id[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int slot = t * kTileTokens + 32 * k + lane;
+              id[k] = slot < p.topk ? idx_row[slot] : -1;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              vm[k] = __ballot_sync(0xffffffffu, id[k] >= 0 && static_cast<int64_t>(id[k]) < p.s_kv);
+          }
           if (ok) ok = mbar_wait(smem_u32(&bars->s_full[sb]), (tc >> 1) & 1, abort_flag, p.err);
           ok = __all_sync(0xffffffffu, ok);
           const int n_valid = keys - t * kTileTokens;  // >= 1; < 128 only on the last tile
-          const bool full = n_valid >= kTileTokens;
+          const bool full = kSparse || n_valid >= kTileTokens;
           // pass 1: row max of the raw scores (the scale is positive)
           float u = -INFINITY;
           if (ok) {
@@ -347,6 +387,11 @@ __global__ void __maxnreg__(224)
               if (!full) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 32 * i + j < n_valid ? v[j] : -INFINITY;
+              }
+              if constexpr (kSparse) {
+                const uint32_t w = vm[0] * (i == 0) | vm[1] * (i == 1) | vm[2] * (i == 2) | vm[3] * (i == 3);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = (w >> j) & 1u ? v[j] : -INFINITY;
               }
 #pragma unroll
               for (int j = 0; j < 32; j += 2) {
@@ -381,6 +426,11 @@ __global__ void __maxnreg__(224)
               if (!full) {  // keys past the end: s = -inf, p = 2^-inf = 0
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 32 * i + j < n_valid ? v[j] : -INFINITY;
+              }
+              if constexpr (kSparse) {  // slots without a pool row: p = 0
+                const uint32_t w = vm[0] * (i == 0) | vm[1] * (i == 1) | vm[2] * (i == 2) | vm[3] * (i == 3);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = (w >> j) & 1u ? v[j] : -INFINITY;
               }
               uint32_t pk[16];
 #pragma unroll
@@ -452,7 +502,7 @@ __global__ void __maxnreg__(224)
     // ================================================================ output CTA
     if (warp == 0 || warp == 2) {
       // ---------------------------------------------------- V tile producers
-      if (lane == 0) {
+      if (lane == 0 || kSparse) {
         const int pw = warp >> 1;
         const uint64_t pol = l2_policy_evict_first();
         PartCursor cur = part_cursor(meta, part);
@@ -464,27 +514,44 @@ __global__ void __maxnreg__(224)
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
-            int32_t y[2];
+            int32_t y[4];
+            if constexpr (kSparse) {
+              const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              int32_t blk = page_of(p, q, 2 * t + h2);
-              if (blk < 0) blk = static_cast<int32_t>(p.num_pages);
-              y[h2] = blk * kPage;
+              for (int i = 0; i < 4; ++i) {
+                const int slot = t * kTileTokens + 4 * lane + i;
+                const int32_t id = slot < p.topk ? idx_row[slot] : -1;
+                y[i] = (id >= 0 && static_cast<int64_t>(id) < p.s_kv) ? id : 0;
+              }
+            } else {
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                int32_t blk = page_of(p, q, 2 * t + h2);
+                if (blk < 0) blk = static_cast<int32_t>(p.num_pages);
+                y[h2] = blk * kPage;
+              }
             }
             for (int c = pw; c < 8 && ok; c += 2) {
               const uint32_t gv = 4 * tc + (c >> 1), slot = gv % kVGroups, round = gv / kVGroups;
-              ok = mbar_wait(smem_u32(&bars->vempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
+              if (lane == 0) {
+                ok = mbar_wait(smem_u32(&bars->vempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
+                if (ok) mbar_arrive_expect_tx(smem_u32(&bars->vfull[slot]), kChunk);
+              }
+              if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
               if (!ok) break;
               const uint32_t bar = smem_u32(&bars->vfull[slot]);
-              mbar_arrive_expect_tx(bar, kChunk);
               const uint32_t dst = base + slot * kVGroupBytes + (c & 1) * kChunk;
-              tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol);
-              tma_load_2d(dst + kChunk / 2, &tm_kv, c * 64, y[1], bar, pol);
+              if constexpr (kSparse) {
+                tma_gather4(dst + 4 * lane * 128, &tm_kv, c * 64, y[0], y[1], y[2], y[3], bar);
+              } else {
+                tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol);
+                tma_load_2d(dst + kChunk / 2, &tm_kv, c * 64, y[1], bar, pol);
+              }
               issued[slot] = static_cast<int32_t>(round);
             }
           }
         }
-        if (!ok) {
+        if (!ok && lane == 0) {
           for (int s = 0; s < kVGroups; ++s) {
             if (issued[s] < 0) continue;
             const uint64_t t_start = globaltimer_ns();
