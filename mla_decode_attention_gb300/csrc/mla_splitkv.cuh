@@ -368,12 +368,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           const uint32_t slot = kv_base + c * kChunkBytes;
-          for (int grp = dw; grp < kTileTokens / 8; grp += kDequantWarps) {
+          // all of this warp's code and scale loads for the chunk are issued
+          // before the first conversion, so their latencies overlap
+          constexpr int kGroupsPerWarp = (kTileTokens / 8 + kDequantWarps - 1) / kDequantWarps;
+          uint4 codes_g[kGroupsPerWarp];
+          float sc_g[kGroupsPerWarp];
+#pragma unroll
+          for (int k = 0; k < kGroupsPerWarp; ++k) {
+            const int grp = dw + kDequantWarps * k;
+            if (grp < kTileTokens / 8) {
+              const int r = grp * 8 + tsub;
+              const uint8_t* tok = p.kv_fp8 +
+                                   (static_cast<int64_t>(blk[r >> 6]) * kPage + (r & 63)) * kFp8TokenBytes;
+              codes_g[k] = __ldg(reinterpret_cast<const uint4*>(tok + c * 64 + unit * 16));
+              sc_g[k] = __ldg(reinterpret_cast<const float*>(tok + kFp8ScaleOffset) + (c >> 1));
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < kGroupsPerWarp; ++k) {
+            const int grp = dw + kDequantWarps * k;
+            if (grp >= kTileTokens / 8) continue;
             const int r = grp * 8 + tsub;  // token row of the tile
-            const uint8_t* tok = p.kv_fp8 +
-                                 (static_cast<int64_t>(blk[r >> 6]) * kPage + (r & 63)) * kFp8TokenBytes;
-            const uint4 codes = __ldg(reinterpret_cast<const uint4*>(tok + c * 64 + unit * 16));
-            const float sc = __ldg(reinterpret_cast<const float*>(tok + kFp8ScaleOffset) + (c >> 1));
+            const uint4 codes = codes_g[k];
+            const float sc = sc_g[k];
             const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
             uint32_t packed[8];
 #pragma unroll
