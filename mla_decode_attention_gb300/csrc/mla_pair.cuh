@@ -76,7 +76,8 @@ constexpr uint32_t kQCol = 0;                      // score CTA: Q latent part, 
 constexpr uint32_t kSCol = 256;                    // score CTA: S buffers at 256 and 384
 constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
-constexpr uint32_t kXferNamedThreads = 160;        // warps 3..7
+constexpr uint32_t kRowThreads = 128;              // warps 4..7
+constexpr uint32_t kXferNamedThreads = 160;        // dense: warps 3..7
 
 struct Bars {
   uint64_t kfull[kKGroups], kempty[kKGroups];      // score CTA K ring
@@ -169,13 +170,18 @@ __global__ void __maxnreg__(224)
 
   if (rank == 0) {
     // ================================================================ score CTA
-    if (warp == 0 || warp == 2) {
+    if (warp == 0 || warp == 2 || (kSparse && warp == 3)) {
       // ---------------------------------------------------- K tile producers
-      // Dense: lane 0 loads each chunk as two page boxes.  Sparse: lane L
-      // gathers rows 4L..4L+3 of the tile for each chunk (invalid slots fetch
-      // pool row 0; the softmax gives them zero weight); lane 0 owns the barriers.
+      // Dense: lane 0 of warps 0, 2 loads each chunk as two page boxes.
+      // Sparse: warps 0, 2, 3 share the chunks (one gather4 costs its warp
+      // ~80 clk to issue, so gathers need more issuing warps); lane L gathers
+      // rows 4L..4L+3 of the tile for each chunk (invalid slots fetch pool
+      // row 0; the softmax gives them zero weight); lane 0 owns the barriers.
+      // Each group of 3 chunks has a chunk of every issuer, so each issuer
+      // waits on every slot in order.
       if (lane == 0 || kSparse) {
-        const int pw = warp >> 1;
+        constexpr int kIssuers = kSparse ? 3 : 2;
+        const int pw = warp == 0 ? 0 : warp - 1;
         const uint64_t pol = l2_policy_evict_first();
         PartCursor cur = part_cursor(meta, part);
         int q, t0, t1, split;
@@ -208,7 +214,7 @@ __global__ void __maxnreg__(224)
                 y[h2] = blk * kPage;
               }
             }
-            for (int c = pw; c < kChunks && ok; c += 2) {
+            for (int c = pw; c < kChunks && ok; c += kIssuers) {
               const int g = c / 3;
               const uint32_t slot = g, round = tc;  // one ring round per tile
               if (lane == 0) {
@@ -415,8 +421,13 @@ __global__ void __maxnreg__(224)
           const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
           // pass 2: p = 2^(s * scale - m) -> bf16 P row r in the staging buffer
           // (two 64-token chunks, 128-byte swizzle), and the two sums
-          named_barrier_sync(1, kXferNamedThreads);  // the previous copy has read the staging
-          float ls = 0.f, bs = 0.f;
+          if constexpr (kSparse) {
+            if (r == 0 && tc > 0) bulk_wait_read_all();  // the previous copy has read the staging
+            named_barrier_sync(1, kRowThreads);
+          } else {
+            named_barrier_sync(1, kXferNamedThreads);  // warp 3's previous copy has read the staging
+          }
+          float ls = 0.f, bs = 0.f, ls2 = 0.f, bs2 = 0.f;
           if (ok) {
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
@@ -432,14 +443,21 @@ __global__ void __maxnreg__(224)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = (w >> j) & 1u ? v[j] : -INFINITY;
               }
+              // packed fp32x2 FMA/adds: one instruction per key pair
               uint32_t pk[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                const float e0 = fast_exp2(fmaf(v[2 * j], sc, neg_m));
-                const float e1 = fast_exp2(fmaf(v[2 * j + 1], sc, neg_m));
+                float x0, x1;
+                asm("{ .reg .b64 a, b, c, d; mov.b64 a, {%2, %3}; mov.b64 b, {%4, %4}; mov.b64 c, {%5, %5};"
+                    " fma.rn.f32x2 d, a, b, c; mov.b64 {%0, %1}, d; }"
+                    : "=f"(x0), "=f"(x1) : "f"(v[2 * j]), "f"(v[2 * j + 1]), "f"(sc), "f"(neg_m));
+                const float e0 = fast_exp2(x0);
+                const float e1 = fast_exp2(x1);
                 pk[j] = pack_bf16x2(e0, e1);
-                ls += e0 + e1;
-                bs += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
+                asm("{ .reg .b64 a, b, c; mov.b64 a, {%0, %1}; mov.b64 b, {%4, %5}; add.rn.f32x2 c, a, b; mov.b64 {%0, %1}, c;"
+                    " mov.b64 a, {%2, %3}; mov.b64 b, {%6, %7}; add.rn.f32x2 c, a, b; mov.b64 {%2, %3}, c; }"
+                    : "+f"(ls), "+f"(ls2), "+f"(bs), "+f"(bs2)
+                    : "f"(e0), "f"(e1), "f"(__uint_as_float(pk[j] << 16)), "f"(__uint_as_float(pk[j] & 0xFFFF0000u)));
               }
               const uint32_t chunk = prow + (i >> 1) * 16384;
 #pragma unroll
@@ -451,13 +469,23 @@ __global__ void __maxnreg__(224)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[sb]));  // S buffer sb may be rewritten
-          lsum += ls;
-          bsum += bs;
+          lsum += ls + ls2;
+          bsum += bs + bs2;
           st_shared_f32(stage + kSideAlpha + 4 * r, alpha);
           if (t == t1 - 1) st_shared_f32(stage + kSideInvL + 4 * r, bsum > 0.f ? 1.f / bsum : 0.f);
           if (lane == 0) st_shared_u32(stage + kSideFlags + 4 * (warp - 4), any);
           fence_proxy_async_smem();
-          named_barrier_arrive(2, kXferNamedThreads);  // staging full
+          if constexpr (!kSparse) named_barrier_arrive(2, kXferNamedThreads);  // staging full: warp 3 copies
+          if constexpr (kSparse) named_barrier_sync(2, kRowThreads);  // staging full
+          if (kSparse && r == 0 && ok) {  // one copy of tile tc into the peer's P buffer tc mod 2
+            const uint32_t b = tc & 1;
+            ok = mbar_wait_cluster(smem_u32(&bars->p_free[b]), ((tc >> 1) & 1) ^ 1, abort_flag, p.err);
+            if (ok) {
+              bulk_copy_to_peer(mapa_shared(base + kPBuf0 + b * kPBufStride, 1), base + kStage, kXferBytes,
+                                mapa_shared(smem_u32(&bars->p_full[b]), 1));
+              bulk_commit_group();
+            }
+          }
         }
         // LSE of row r for this piece
         const float lse_v = (lsum > 0.f && bsum > 0.f) ? (m_use + __log2f(lsum)) * 0.69314718055994531f
@@ -472,8 +500,9 @@ __global__ void __maxnreg__(224)
         }
         ++item;
       }
-    } else if (warp == 3) {
-      // ---------------------------------------------------- P transfers
+      if (kSparse && r == 0) bulk_wait_all();  // the last copy has landed in the peer
+    } else if (warp == 3 && !kSparse) {
+      // ---------------------------------------------------- P transfers (dense)
       PartCursor cur = part_cursor(meta, part);
       int q, t0, t1, split;
       uint32_t tc = 0;
@@ -500,10 +529,14 @@ __global__ void __maxnreg__(224)
     }
   } else {
     // ================================================================ output CTA
-    if (warp == 0 || warp == 2) {
+    if (warp == 0 || warp == 2 || (kSparse && warp == 3)) {
       // ---------------------------------------------------- V tile producers
+      // Dense: lane 0 of warps 0, 2.  Sparse: warps 0, 2, 3 gather (chunk c by
+      // issuer c mod 3); each issuer loads into the same d quarters every tile,
+      // so it waits on those slots in order.
       if (lane == 0 || kSparse) {
-        const int pw = warp >> 1;
+        constexpr int kIssuers = kSparse ? 3 : 2;
+        const int pw = warp == 0 ? 0 : warp - 1;
         const uint64_t pol = l2_policy_evict_first();
         PartCursor cur = part_cursor(meta, part);
         int q, t0, t1, split;
@@ -531,7 +564,7 @@ __global__ void __maxnreg__(224)
                 y[h2] = blk * kPage;
               }
             }
-            for (int c = pw; c < 8 && ok; c += 2) {
+            for (int c = pw; c < 8 && ok; c += kIssuers) {
               const uint32_t gv = 4 * tc + (c >> 1), slot = gv % kVGroups, round = gv / kVGroups;
               if (lane == 0) {
                 ok = mbar_wait(smem_u32(&bars->vempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
@@ -635,6 +668,17 @@ __global__ void __maxnreg__(224)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->side_read[b]));  // done with the side data
+          if (kSparse && warp == 4 && lane == 0 && ok && tc >= 1) {
+            // hand P buffer (tc - 1) mod 2 back: every row warp has read tile
+            // tc - 1's side data and its PV has completed; armed for tile tc + 1
+            const uint32_t pb = (tc - 1) & 1, ph = ((tc - 1) >> 1) & 1;
+            ok = mbar_wait(smem_u32(&bars->side_read[pb]), ph, abort_flag, p.err);
+            if (ok) ok = mbar_wait(smem_u32(&bars->pv_done[pb]), ph, abort_flag, p.err);
+            if (ok) {
+              mbar_arrive_expect_tx(smem_u32(&bars->p_full[pb]), kXferBytes);
+              mbar_remote_arrive(mapa_shared(smem_u32(&bars->p_free[pb]), 0));
+            }
+          }
           if (ok && t != t0 && any != 0u) {
             ok = mbar_wait(smem_u32(&bars->o_drained), rc & 1, abort_flag, p.err);
             ok = __all_sync(0xffffffffu, ok);
@@ -724,7 +768,7 @@ __global__ void __maxnreg__(224)
         if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));
         ++item;
       }
-    } else if (warp == 3) {
+    } else if (warp == 3 && !kSparse) {
       // ---------------------------------------------------- P buffer hand-back
       PartCursor cur = part_cursor(meta, part);
       int q, t0, t1, split;
