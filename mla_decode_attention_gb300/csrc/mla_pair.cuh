@@ -77,6 +77,9 @@ constexpr uint32_t kSCol = 256;                    // score CTA: S buffers at 25
 constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
 constexpr uint32_t kRowThreads = 128;              // warps 4..7
+// Softmax: one pass over S per tile after a piece's first (the row max comes
+// with the probabilities; a row whose reference must move redoes the pass).
+constexpr bool kSinglePass = true;
 constexpr uint32_t kXferNamedThreads = 160;        // dense: warps 3..7
 
 struct Bars {
@@ -96,6 +99,12 @@ static_assert(sizeof(Bars) <= 1024, "barrier block size");
 static_assert(kStage + kXferBytes <= kBarOffset, "score CTA layout");
 static_assert(kXferBytes <= kPBufStride && kXferBytes % 16 == 0, "P transfer size");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 // One CTA per SM (shared memory); up to 224 registers per thread (8 warps, two
 // per sub-partition), so each row thread's 128 scores stay in registers.
@@ -380,11 +389,13 @@ __global__ void __maxnreg__(224)
           ok = __all_sync(0xffffffffu, ok);
           const int n_valid = keys - t * kTileTokens;  // >= 1; < 128 only on the last tile
           const bool full = kSparse || n_valid >= kTileTokens;
-          // pass 1: row max of the raw scores (the scale is positive)
+          // Row max (raw scores; the scale is positive).  The first tile of a
+          // piece reads S once for it (pass 1); later tiles take it from the
+          // probabilities pass, against the current reference, and redo that
+          // pass only in the rare rows whose reference has to move.
           float u = -INFINITY;
-          if (ok) {
+          if (ok && (t == t0 || !kSinglePass)) {
             tc_fence_after();
-            float u2 = -INFINITY;
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
               float v[32];
@@ -400,25 +411,19 @@ __global__ void __maxnreg__(224)
                 for (int j = 0; j < 32; ++j) v[j] = (w >> j) & 1u ? v[j] : -INFINITY;
               }
 #pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                u = fmaxf(u, v[j]);
-                u2 = fmaxf(u2, v[j + 1]);
-              }
+              for (int j = 0; j < 32; j += 2) u = fmax3(u, v[j], v[j + 1]);
             }
-            u = fmaxf(u, u2);
           }
           u *= sc;
           float alpha = 1.f;
           if (t == t0) {
             m_use = u == -INFINITY ? 0.f : u;
-          } else if (u > m_use + kRescaleLog2) {
+          } else if (!kSinglePass && u > m_use + kRescaleLog2) {
             alpha = fast_exp2(m_use - u);
             m_use = u;
             lsum *= alpha;
             bsum *= alpha;
           }
-          const float neg_m = -m_use;
-          const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
           // pass 2: p = 2^(s * scale - m) -> bf16 P row r in the staging buffer
           // (two 64-token chunks, 128-byte swizzle), and the two sums
           if constexpr (kSparse) {
@@ -427,8 +432,13 @@ __global__ void __maxnreg__(224)
           } else {
             named_barrier_sync(1, kXferNamedThreads);  // warp 3's previous copy has read the staging
           }
+          if (ok && kSinglePass && t != t0) tc_fence_after();
           float ls = 0.f, bs = 0.f, ls2 = 0.f, bs2 = 0.f;
-          if (ok) {
+          for (bool again = ok; again;) {
+            again = false;
+            const float neg_m = -m_use;
+            float xm = -INFINITY;  // raw row max seen by this pass
+            ls = 0.f; bs = 0.f; ls2 = 0.f; bs2 = 0.f;
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
               float v[32];
@@ -447,6 +457,7 @@ __global__ void __maxnreg__(224)
               uint32_t pk[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
+                if constexpr (kSinglePass) xm = fmax3(xm, v[2 * j], v[2 * j + 1]);
                 float x0, x1;
                 asm("{ .reg .b64 a, b, c, d; mov.b64 a, {%2, %3}; mov.b64 b, {%4, %4}; mov.b64 c, {%5, %5};"
                     " fma.rn.f32x2 d, a, b, c; mov.b64 {%0, %1}, d; }"
@@ -465,7 +476,18 @@ __global__ void __maxnreg__(224)
                 st_shared_v4(chunk + ((((i & 1) * 4 + uu) ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1],
                              pk[4 * uu + 2], pk[4 * uu + 3]);
             }
+            xm *= sc;
+            const bool move = kSinglePass && t != t0 && xm > m_use + kRescaleLog2;
+            if (move) {  // move the reference; the warp redoes the pass (TMEM loads are warp-wide)
+              const float a_new = fast_exp2(m_use - xm);
+              alpha *= a_new;
+              m_use = xm;
+              lsum *= a_new;
+              bsum *= a_new;
+            }
+            again = __any_sync(0xffffffffu, move);
           }
+          const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[sb]));  // S buffer sb may be rewritten
