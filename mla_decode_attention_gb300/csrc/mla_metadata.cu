@@ -13,6 +13,7 @@ namespace mla {
 namespace {
 
 constexpr int kMetaThreads = 1024;
+constexpr int kSmemPrefixes = 8192;  // sequences whose cost prefixes the schedule keeps in smem
 
 // Block-wide exclusive scan of one int64 per thread; returns the total.
 __device__ int64_t block_exclusive_scan(int64_t v, int64_t* out_excl, int64_t* warp_sums) {
@@ -48,6 +49,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
                                                                 int s_q, int causal, int topk,
                                                                 int num_parts, int32_t* meta) {
   __shared__ int64_t warp_sums[32];
+  __shared__ int32_t s_prefix[kSmemPrefixes];
   // a decode kernel launched next may start its prologue; it waits for this
   // grid to complete before it reads the schedule
   pdl_launch_dependents();
@@ -68,7 +70,11 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   }
   int64_t base;
   const int64_t total = block_exclusive_scan(local, &base, warp_sums);
-  for (int q = q0; q < q1; ++q) meta_seq(meta, num_parts, q)[kSCostPrefix] += static_cast<int32_t>(base);
+  for (int q = q0; q < q1; ++q) {
+    int32_t* sq = meta_seq(meta, num_parts, q);
+    sq[kSCostPrefix] += static_cast<int32_t>(base);
+    if (n_seq <= kSmemPrefixes) s_prefix[q] = sq[kSCostPrefix];
+  }
   __syncthreads();
   __threadfence_block();
 
@@ -94,8 +100,14 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   __syncthreads();
 
   // 3. part ranges.
-  for (int p = threadIdx.x; p < num_parts; p += kMetaThreads)
-    fill_part(meta, num_parts, n_seq, total, per_part, p);
+  // (the binary searches read the prefixes from shared memory when they fit)
+  if (n_seq <= kSmemPrefixes) {
+    for (int p = threadIdx.x; p < num_parts; p += kMetaThreads)
+      fill_part(meta, num_parts, ArrayPrefix{s_prefix}, n_seq, total, per_part, p);
+  } else {
+    for (int p = threadIdx.x; p < num_parts; p += kMetaThreads)
+      fill_part(meta, num_parts, MetaPrefix{meta, num_parts}, n_seq, total, per_part, p);
+  }
 
   if (threadIdx.x == 0) {
     meta[kHMagic] = kMetaMagic; meta[kHVersion] = kMetaVersion; meta[kHNSeq] = n_seq;
@@ -221,7 +233,8 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
     s[kSSplitOff] = static_cast<int32_t>(splits);
     splits += s[kSNSplits];
   }
-  for (int p = 0; p < num_sm_parts; ++p) fill_part(meta, num_sm_parts, n_seq, total, per_part, p);
+  for (int p = 0; p < num_sm_parts; ++p)
+    fill_part(meta, num_sm_parts, MetaPrefix{meta, num_sm_parts}, n_seq, total, per_part, p);
   meta[kHMagic] = kMetaMagic; meta[kHVersion] = kMetaVersion; meta[kHNSeq] = n_seq;
   meta[kHParts] = num_sm_parts; meta[kHTile] = kTileTokens; meta[kHSq] = s_q;
   meta[kHBatch] = batch; meta[kHCausal] = causal ? 1 : 0; meta[kHTopk] = topk;

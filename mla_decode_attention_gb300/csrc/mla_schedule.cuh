@@ -67,11 +67,24 @@ MLA_HD int64_t floordiv(int64_t a, int64_t b) {  // b > 0
   return a >= 0 ? a / b : -((-a + b - 1) / b);
 }
 
+// Cost prefix of sequence q read from the metadata's sequence records, or from
+// a copy of those prefixes (the device schedule keeps one in shared memory).
+struct MetaPrefix {
+  const int32_t* meta;
+  int num_parts;
+  MLA_HD int32_t operator()(int q) const { return meta_seq(meta, num_parts, q)[kSCostPrefix]; }
+};
+struct ArrayPrefix {
+  const int32_t* a;
+  MLA_HD int32_t operator()(int q) const { return a[q]; }
+};
+
 // Position (q, t) of cost offset x: q is the sequence whose cost range
 // [prefix[q], prefix[q] + cost[q]) contains x; t is the tile at that offset
 // (offsets inside the fixed cost map to tile 0).  x >= total maps to (n_seq, 0).
-MLA_HD void cost_position(const int32_t* meta, int num_parts, int n_seq, int64_t total, int64_t x,
-                          int* q_out, int* t_out) {
+template <class Prefix>
+MLA_HD void cost_position(const Prefix& prefix, int n_seq, int64_t total, int64_t x, int* q_out,
+                          int* t_out) {
   if (x >= total) {
     *q_out = n_seq;
     *t_out = 0;
@@ -80,9 +93,9 @@ MLA_HD void cost_position(const int32_t* meta, int num_parts, int n_seq, int64_t
   int lo = 0, hi = n_seq - 1;
   while (lo < hi) {  // largest q with prefix[q] <= x
     const int mid = (lo + hi + 1) >> 1;
-    if (meta_seq(meta, num_parts, mid)[kSCostPrefix] <= x) lo = mid; else hi = mid - 1;
+    if (prefix(mid) <= x) lo = mid; else hi = mid - 1;
   }
-  const int64_t local = x - meta_seq(meta, num_parts, lo)[kSCostPrefix];
+  const int64_t local = x - prefix(lo);
   *q_out = lo;
   *t_out = static_cast<int>(local > kFixedCost ? local - kFixedCost : 0);
 }
@@ -97,19 +110,17 @@ MLA_HD int32_t inner_boundaries(int64_t prefix, int32_t n_tiles, int64_t per_par
 }
 
 // Fills part p's record from the per-sequence cost prefixes.
-MLA_HD void fill_part(int32_t* meta, int num_parts, int n_seq, int64_t total, int64_t per_part,
-                      int p) {
+template <class Prefix>
+MLA_HD void fill_part(int32_t* meta, int num_parts, const Prefix& prefix, int n_seq, int64_t total,
+                      int64_t per_part, int p) {
   int qb, tb, qe, te;
   const int64_t xb = static_cast<int64_t>(p) * per_part;
   int64_t xe = xb + per_part;
   if (xe > total) xe = total;
-  cost_position(meta, num_parts, n_seq, total, xb, &qb, &tb);
-  cost_position(meta, num_parts, n_seq, total, xe, &qe, &te);
+  cost_position(prefix, n_seq, total, xb, &qb, &tb);
+  cost_position(prefix, n_seq, total, xe, &qe, &te);
   int32_t split_begin = 0;
-  if (qb < n_seq && tb > 0) {
-    const int64_t prefix = meta_seq(meta, num_parts, qb)[kSCostPrefix];
-    split_begin = static_cast<int32_t>(p - floordiv(prefix + kFixedCost, per_part));
-  }
+  if (qb < n_seq && tb > 0) split_begin = static_cast<int32_t>(p - floordiv(prefix(qb) + kFixedCost, per_part));
   int32_t* r = meta_part(meta, p);
   r[0] = qb; r[1] = tb; r[2] = qe; r[3] = te; r[4] = split_begin;
   r[5] = 0; r[6] = 0; r[7] = 0;
