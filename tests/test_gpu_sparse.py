@@ -144,3 +144,23 @@ def test_full_size_dsa_sampled_rows():
     for b, j in rows:
         assert_parity(out[b, j], ref_o[b, j], lse[b, :, j], ref_l[b, :, j], f"dsa row {b}")
     assert err == 0 and np.all(np.isfinite(out))
+
+
+def test_split_entry_then_combine_equals_sparse_decode():
+    """mla_sparse_decode_splitkv + mla_combine on the same metadata and
+    workspace gives the bytes mla_sparse_decode gives (128 heads: the two-SM
+    kernel; 64: the one-SM kernel), with splits forced by 76 parts."""
+    for h in (128, 64):
+        inp = small(31 + h, b=3, s_q=2, h=h, s_kv=5000, topk=700, invalid=40)
+        ref_o, ref_l, ref_e = run_sparse(inp, 76)
+        q, kv, idx = inp["q"].to(DEV), inp["kv"].to(DEV), inp["indices"].to(DEV)
+        b, s_q, _, _ = q.shape
+        buf = binding.DecodeBuffers(b, s_q, h, DEV, 76)
+        binding.mla_get_metadata(None, b, s_q, False, idx.shape[-1], 76, buf.metadata)
+        binding.mla_sparse_decode_splitkv(q, kv, idx, inp["softmax_scale"], buf.metadata, 76,
+                                          buf.workspace, buf.out, buf.lse, buf.err)
+        binding.mla_combine(buf.metadata, b, s_q, h, 76, buf.workspace, buf.out, buf.lse)
+        torch.cuda.synchronize()
+        assert int(buf.err.item()) == ref_e == 0
+        assert np.array_equal(buf.out.float().cpu().numpy(), ref_o)
+        assert np.array_equal(buf.lse.cpu().numpy(), ref_l)
