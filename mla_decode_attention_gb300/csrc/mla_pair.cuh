@@ -100,6 +100,17 @@ static_assert(kStage + kXferBytes <= kBarOffset, "score CTA layout");
 static_assert(kXferBytes <= kPBufStride && kXferBytes % 16 == 0, "P transfer size");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
+// Sparse: the index list entries of key slots 128 t + 4 lane .. + 3 of
+// sequence q (-1 past topk); validated by the caller.
+__device__ __forceinline__ void load_idx4(const SplitParams& p, int q, int t, int lane, int32_t (&id)[4]) {
+  const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int slot = t * kTileTokens + 4 * lane + i;
+    id[i] = slot < p.topk ? idx_row[slot] : -1;
+  }
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -199,18 +210,21 @@ __global__ void __maxnreg__(224)
         for (int i = 0; i < kKGroups; ++i) issued[i] = -1;
         bool ok = true;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+          int32_t nid[4];  // sparse: the next tile's indices, requested one tile ahead
+          if constexpr (kSparse) load_idx4(p, q, t0, lane, nid);
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
             int32_t y[4];
             if constexpr (kSparse) {
-              const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
+              int32_t id[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) id[i] = nid[i];
+              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, nid);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const int slot = t * kTileTokens + 4 * lane + i;
-                const int32_t id = slot < p.topk ? idx_row[slot] : -1;
-                const bool valid = id >= 0 && static_cast<int64_t>(id) < p.s_kv;
-                if (!valid && id != -1 && p.err && pw == 0) atomicOr(p.err, MLA_DEVERR_BAD_INDEX);
-                y[i] = valid ? id : 0;
+                const bool valid = id[i] >= 0 && static_cast<int64_t>(id[i]) < p.s_kv;
+                if (!valid && id[i] != -1 && p.err && pw == 0) atomicOr(p.err, MLA_DEVERR_BAD_INDEX);
+                y[i] = valid ? id[i] : 0;
               }
             } else {
 #pragma unroll
@@ -373,20 +387,22 @@ __global__ void __maxnreg__(224)
           const uint32_t t_s = tmem + lane_off + kSCol + 128 * sb;
           // sparse: bit L of vm[k] = key slot t * 128 + 32 k + L names a pool row
           uint32_t vm[4] = {~0u, ~0u, ~0u, ~0u};
+          int32_t sid[4];  // sparse: requested before the S wait, used after it
           if constexpr (kSparse) {
             const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
-            int32_t id[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int slot = t * kTileTokens + 32 * k + lane;
-              id[k] = slot < p.topk ? idx_row[slot] : -1;
+              sid[k] = slot < p.topk ? idx_row[slot] : -1;
             }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              vm[k] = __ballot_sync(0xffffffffu, id[k] >= 0 && static_cast<int64_t>(id[k]) < p.s_kv);
           }
           if (ok) ok = mbar_wait(smem_u32(&bars->s_full[sb]), (tc >> 1) & 1, abort_flag, p.err);
           ok = __all_sync(0xffffffffu, ok);
+          if constexpr (kSparse) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              vm[k] = __ballot_sync(0xffffffffu, sid[k] >= 0 && static_cast<int64_t>(sid[k]) < p.s_kv);
+          }
           const int n_valid = keys - t * kTileTokens;  // >= 1; < 128 only on the last tile
           const bool full = kSparse || n_valid >= kTileTokens;
           // Row max (raw scores; the scale is positive).  The first tile of a
@@ -567,17 +583,18 @@ __global__ void __maxnreg__(224)
         for (int i = 0; i < kVGroups; ++i) issued[i] = -1;
         bool ok = true;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+          int32_t nid[4];  // sparse: the next tile's indices, requested one tile ahead
+          if constexpr (kSparse) load_idx4(p, q, t0, lane, nid);
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
             int32_t y[4];
             if constexpr (kSparse) {
-              const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
+              int32_t id[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int slot = t * kTileTokens + 4 * lane + i;
-                const int32_t id = slot < p.topk ? idx_row[slot] : -1;
-                y[i] = (id >= 0 && static_cast<int64_t>(id) < p.s_kv) ? id : 0;
-              }
+              for (int i = 0; i < 4; ++i) id[i] = nid[i];
+              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, nid);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) y[i] = (id[i] >= 0 && static_cast<int64_t>(id[i]) < p.s_kv) ? id[i] : 0;
             } else {
 #pragma unroll
               for (int h2 = 0; h2 < 2; ++h2) {
