@@ -174,6 +174,9 @@ def run_ours(args, rank, world, local_rank):
     # One set of schedule / workspace / output buffers reused every step, as a
     # serving loop reuses them; the inputs alternate between two sets.
     bufs = [binding.DecodeBuffers(b, s_q, h, dev, parts)]
+    # the split-only timing replays the split kernel without the schedule
+    # kernel, so it keeps one schedule per input set (lengths differ per set)
+    split_meta = [torch.empty_like(bufs[0].metadata) for _ in range(2)]
     stream = torch.cuda.Stream(device=dev)
     scale = workloads.SOFTMAX_SCALE
 
@@ -184,11 +187,12 @@ def run_ours(args, rank, world, local_rank):
 
     def step(k, split_only=False):
         s, buf = sets[k % 2], bufs[0]
+        meta = split_meta[k % 2] if split_only else buf.metadata
         if sparse:
             if not split_only:
                 binding.mla_get_metadata(None, b, s_q, False, w.topk, parts, buf.metadata, stream)
             fn = binding.mla_sparse_decode_splitkv if split_only else binding.mla_sparse_decode
-            fn(s["q"], s["kv"], s["indices"], scale, buf.metadata, parts, buf.workspace, buf.out,
+            fn(s["q"], s["kv"], s["indices"], scale, meta, parts, buf.workspace, buf.out,
                buf.lse, buf.err, stream)
         elif not split_only:
             binding.mla_get_metadata(s["cache_seqlens"], b, s_q, True, 0, parts, buf.metadata,
@@ -199,11 +203,17 @@ def run_ours(args, rank, world, local_rank):
         else:
             binding.mla_decode_splitkv(s["q"], s["kv_cache"], fmt,
                                        s["block_table"], s["cache_seqlens"], scale, True,
-                                       buf.metadata, parts, buf.workspace, buf.out, buf.lse,
+                                       meta, parts, buf.workspace, buf.out, buf.lse,
                                        buf.err, stream)
 
-    # metadata once so the split-only graph has a valid schedule
+    # one schedule per input set for the split-only graph
     with torch.cuda.stream(stream):
+        for k in range(2):
+            if sparse:
+                binding.mla_get_metadata(None, b, s_q, False, w.topk, parts, split_meta[k], stream)
+            else:
+                binding.mla_get_metadata(sets[k]["cache_seqlens"], b, s_q, True, 0, parts,
+                                         split_meta[k], stream)
         for k in range(2):
             step(k)
     torch.cuda.synchronize(dev)
