@@ -492,4 +492,17 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, v
   }
 }
 
+// 16-byte store into another CTA's shared memory (distributed shared memory).
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr_cluster, uint32_t a, uint32_t b,
+                                                     uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr_cluster), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+// Orders this thread's generic-proxy writes to cluster shared memory before
+// later async-proxy accesses (a peer's tensor-core reads).
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
 }  // namespace mla

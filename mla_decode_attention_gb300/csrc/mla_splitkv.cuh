@@ -271,6 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup: barriers, TMEM, zeroed padding rows of Q
   const bool multicast = kClusterMulticast && p.n_hblk == 2;
+  // FP8 with two head blocks: each CTA dequantises half of the latent chunks
+  // (chunk c by head block c mod 2) into both CTAs' slots
+  const bool share = kMode == KvMode::kPagedFp8 && p.n_hblk == 2;
   if (threadIdx.x == 0) {
     for (int c = 0; c < kChunks; ++c) {
       // FP8: latent chunks are filled by the three dequantising warps
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (kMode == KvMode::kPagedFp8 && c < kChunks - 1) ? kDequantWarps : 1);
       // a slot is free once the MMA threads of every CTA writing into it
       // have released it
-      mbar_init(smem_u32(&sm->empty[c]), multicast ? 2 : 1);
+      mbar_init(smem_u32(&sm->empty[c]), (multicast || (share && c < kChunks - 1)) ? 2 : 1);
     }
     mbar_init(smem_u32(&sm->q_full), 1);
     mbar_init(smem_u32(&sm->q_empty), 1);
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (multicast) cluster_sync();  // peers' barriers are initialised before any remote arrive
+  if (multicast || share) cluster_sync();  // peers' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   volatile uint32_t* abort_flag = &sm->abort;
@@ -364,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         for (int c = 0; c < kChunks - 1; ++c) {
+          if (share && (c & 1) != hb) continue;  // the peer dequantises this chunk for both
           if (lane == 0) ok = mbar_wait(smem_u32(&sm->empty[c]), par, abort_flag, p.err);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
@@ -401,13 +405,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               packed[2 * k + 1] = pack_bf16x2(b2.x * sc, b2.y * sc);
             }
             const uint32_t row = slot + r * 128;
-            st_shared_v4(row + ((2 * unit) ^ (r & 7)) * 16, packed[0], packed[1], packed[2], packed[3]);
-            st_shared_v4(row + ((2 * unit + 1) ^ (r & 7)) * 16, packed[4], packed[5], packed[6],
-                         packed[7]);
+            const uint32_t a0 = row + ((2 * unit) ^ (r & 7)) * 16, a1 = row + ((2 * unit + 1) ^ (r & 7)) * 16;
+            st_shared_v4(a0, packed[0], packed[1], packed[2], packed[3]);
+            st_shared_v4(a1, packed[4], packed[5], packed[6], packed[7]);
+            if (share) {
+              st_shared_cluster_v4(mapa_shared(a0, hb ^ 1), packed[0], packed[1], packed[2], packed[3]);
+              st_shared_cluster_v4(mapa_shared(a1, hb ^ 1), packed[4], packed[5], packed[6], packed[7]);
+            }
           }
           fence_proxy_async_smem();
+          if (share) fence_proxy_async_cluster();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sm->full[c]));
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&sm->full[c]));
+            if (share) mbar_remote_arrive(mapa_shared(smem_u32(&sm->full[c]), hb ^ 1));
+          }
         }
         ++tile_ctr;
       }
@@ -592,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t bp = sw128_desc(p_base + 2048 * s, kChunkBytes, 1024);
               mma_bf16_ss(tmem + kTmemO + 64 * m, a, bp, kIdescPV, (t != t0 || s != 0) ? 1u : 0u);
             }
-            if (multicast) {
+            if (multicast || share) {  // the slot is written by both CTAs' producers
               mma_commit_multicast(smem_u32(&sm->empty[2 * m]), 0x3);
               mma_commit_multicast(smem_u32(&sm->empty[2 * m + 1]), 0x3);
             } else {
@@ -816,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (multicast) cluster_sync();  // no peer still writes into this CTA's smem
+  if (multicast || share) cluster_sync();  // no peer still writes into this CTA's smem
   pdl_launch_dependents();
   if (warp == kMmaWarp) {
     tc_fence_after();
