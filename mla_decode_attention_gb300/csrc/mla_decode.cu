@@ -58,6 +58,21 @@ bool make_strided_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte tensor [rows, cols] whose rows start `stride_bytes` apart; boxes of
+// [box_rows x box_cols bytes], not swizzled.
+bool make_byte_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint64_t stride_bytes, uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {stride_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <KvMode kMode>
 int configure_kernel() {
   static int state = 0;  // 0 unset, 1 ok, -1 failed
@@ -74,7 +89,8 @@ int configure_kernel() {
 
 template <KvMode kMode>
 int launch_split(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const SplitParams& prm,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, const CUtensorMap* tm_codes = nullptr,
+                 const CUtensorMap* tm_scales = nullptr) {
   int rc = configure_kernel<kMode>();
   if (rc != MLA_OK) return rc;
   cudaLaunchConfig_t cfg = {};
@@ -89,7 +105,10 @@ int launch_split(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const SplitP
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_splitkv_kernel<kMode>, tm_q, tm_kv, prm);
+  // the FP8 code and scale maps are read only by the FP8 instantiation
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_splitkv_kernel<kMode>, tm_q, tm_kv,
+                                           tm_codes ? *tm_codes : tm_kv,
+                                           tm_scales ? *tm_scales : tm_kv, prm);
   return e == cudaSuccess ? MLA_OK : record_cuda_error("split kernel launch", e);
 }
 
@@ -155,7 +174,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   const int n_seq = batch * s_q;
   const int n_hblk = head_blocks(h_q);
   const int rows = h_q < kRowsPerCta ? h_q : kRowsPerCta;
-  CUtensorMap tm_q, tm_kv;
+  CUtensorMap tm_q, tm_kv, tm_codes, tm_scales;
   if (!make_rows_map(&tm_q, q, static_cast<uint64_t>(n_seq) * h_q, kDqk * 2, rows))
     return record_error("cuTensorMapEncodeTiled failed for q", MLA_ERR_CUDA);
   const bool fp8 = kv_format == MLA_KV_FP8_656;
@@ -169,6 +188,13 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
     if (!make_strided_map(&tm_kv, rope, static_cast<uint64_t>(num_pages) * kPage, 64,
                           kFp8TokenBytes, kPage))
       return record_error("cuTensorMapEncodeTiled failed for the FP8 RoPE columns", MLA_ERR_CUDA);
+    // the 512 e4m3 codes (boxes of 64 tokens x 64 codes) and the 16 scale
+    // bytes at byte 512 (boxes of 64 tokens x 16 bytes) of every token
+    const uint64_t tokens = static_cast<uint64_t>(num_pages) * kPage;
+    if (!make_byte_map(&tm_codes, kv_cache, tokens, kFp8ScaleOffset, kFp8TokenBytes, 64, kPage) ||
+        !make_byte_map(&tm_scales, static_cast<const uint8_t*>(kv_cache) + kFp8ScaleOffset, tokens,
+                       16, kFp8TokenBytes, 16, kPage))
+      return record_error("cuTensorMapEncodeTiled failed for the FP8 codes or scales", MLA_ERR_CUDA);
   }
 
   SplitParams prm = {};
@@ -191,7 +217,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   prm.n_hblk = n_hblk;
   prm.rows = rows;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
-  if (fp8) return launch_split<KvMode::kPagedFp8>(tm_q, tm_kv, prm, stream);
+  if (fp8) return launch_split<KvMode::kPagedFp8>(tm_q, tm_kv, prm, stream, &tm_codes, &tm_scales);
   // 128 query rows: the two-SM kernel (scores and softmax on one SM, P.V on the other)
   if (h_q == pair::kRows) return launch_pair<false>(tm_kv, prm, stream);
   return launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);

@@ -51,6 +51,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that suspends the thread for at most about `ns` nanoseconds.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false (and
 // records MLA_DEVERR_TIMEOUT in *abort and err) if it does not complete within
 // kWaitTimeoutNs or another role of the CTA has already aborted.
@@ -118,6 +140,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// The same without an L2 cache hint.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
 
@@ -395,6 +427,14 @@ __device__ __forceinline__ void mbar_remote_arrive(uint32_t bar_cluster) {
                : "memory");
 }
 
+// Arrive once on a peer CTA's mbarrier and raise its expected transaction
+// bytes by `bytes` (release, cluster scope).
+__device__ __forceinline__ void mbar_remote_arrive_expect_tx(uint32_t bar_cluster, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;"
+               ::"r"(bar_cluster), "r"(bytes)
+               : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this
 // CTA's shared memory into a peer CTA's, completing on the peer's mbarrier.
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src,
@@ -490,19 +530,6 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, v
       }
     }
   }
-}
-
-// 16-byte store into another CTA's shared memory (distributed shared memory).
-__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr_cluster, uint32_t a, uint32_t b,
-                                                     uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr_cluster), "r"(a), "r"(b),
-               "r"(c), "r"(d)
-               : "memory");
-}
-// Orders this thread's generic-proxy writes to cluster shared memory before
-// later async-proxy accesses (a peer's tensor-core reads).
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 }  // namespace mla

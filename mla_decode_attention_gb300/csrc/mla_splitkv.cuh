@@ -50,9 +50,10 @@ constexpr int kQChunkBytes = kRowsPerCta * 64 * 2;  // 8 KB
 constexpr int kSmemKv = 0;
 constexpr int kSmemQ = kChunks * kChunkBytes;                 // 147456
 constexpr int kSmemSmall = kSmemQ + kChunks * kQChunkBytes;   // 221184
-constexpr int kNumBarriers = 2 * kChunks + 5;
+constexpr int kNumBarriers = 3 * kChunks + 4;
 constexpr int kSmallBytes = 8 * kNumBarriers + 16 + 5 * 4 * 4 * 4 * 16;
 constexpr int kSmemBytes = kSmallBytes + kSmemSmall + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 232448, "dynamic shared memory per CTA");
 constexpr int kSoftmaxGroups = 4;                  // warpgroups on the softmax
 constexpr int kRowsPerGroup = kRowsPerCta / kSoftmaxGroups;  // 16 query rows each
 constexpr int kThreads = 128 * (1 + kSoftmaxGroups);
@@ -84,6 +85,14 @@ constexpr int kFp8TokenBytes = 656;
 constexpr int kFp8ScaleOffset = 512;
 constexpr int kFp8RopeOffset = 528;
 constexpr int kDequantWarps = 3;  // warps 0, 2, 3 (warp 1 issues the MMAs)
+constexpr uint32_t kDequantBarrier = 5;  // named barrier of the three (1..4: softmax groups)
+// staging of a latent chunk's raw FP8 data inside its own 16 KB bf16 slot
+constexpr int kRawScaleOff = 4096;                  // [128 tokens][4 fp32 scales]
+constexpr int kRawScaleBytes = kTileTokens * 16;
+constexpr int kRawCodeOff = 8192;                   // [128 tokens][64 e4m3 codes]
+constexpr int kRawCodeBytes = kTileTokens * 64;
+static_assert(kRawScaleOff + kRawScaleBytes <= kRawCodeOff && kRawCodeOff + kRawCodeBytes <= kChunkBytes,
+              "staging fits in the slot");
 
 struct SplitParams {
   const int32_t* meta;
@@ -119,6 +128,7 @@ struct SmemSmall {
   alignas(16) float bcast2[kSoftmaxGroups][4][kRowsPerGroup];
   uint64_t full[kChunks];
   uint64_t empty[kChunks];
+  uint64_t raw_full[kChunks - 1];  // FP8: raw codes and scales of a latent chunk landed
   uint64_t q_full, q_empty, s_full, p_full, o_done;
   uint32_t tmem_base;
   uint32_t abort;
@@ -256,6 +266,8 @@ template <KvMode kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_splitkv_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_kv,
+                       const __grid_constant__ CUtensorMap tm_codes,
+                       const __grid_constant__ CUtensorMap tm_scales,
                        const __grid_constant__ SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -272,17 +284,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- setup: barriers, TMEM, zeroed padding rows of Q
   const bool multicast = kClusterMulticast && p.n_hblk == 2;
   // FP8 with two head blocks: each CTA dequantises half of the latent chunks
-  // (chunk c by head block c mod 2) into both CTAs' slots
+  // (chunk c by head block c mod 2) and copies them into the peer's slots
   const bool share = kMode == KvMode::kPagedFp8 && p.n_hblk == 2;
   if (threadIdx.x == 0) {
     for (int c = 0; c < kChunks; ++c) {
-      // FP8: latent chunks are filled by the three dequantising warps
+      // FP8: a latent chunk is filled by this CTA's three dequantising warps,
+      // or by one bulk copy from the peer (one remote arrive + bytes)
+      const bool from_peer = share && (c & 1) != hb;
       mbar_init(smem_u32(&sm->full[c]),
-                (kMode == KvMode::kPagedFp8 && c < kChunks - 1) ? kDequantWarps : 1);
+                (kMode == KvMode::kPagedFp8 && c < kChunks - 1 && !from_peer) ? kDequantWarps : 1);
       // a slot is free once the MMA threads of every CTA writing into it
       // have released it
       mbar_init(smem_u32(&sm->empty[c]), (multicast || (share && c < kChunks - 1)) ? 2 : 1);
     }
+    for (int c = 0; c < kChunks - 1; ++c) mbar_init(smem_u32(&sm->raw_full[c]), 1);
     mbar_init(smem_u32(&sm->q_full), 1);
     mbar_init(smem_u32(&sm->q_empty), 1);
     mbar_init(smem_u32(&sm->s_full), 1);
@@ -308,6 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
+    if (kMode == KvMode::kPagedFp8) {
+      tma_prefetch_desc(&tm_codes);
+      tma_prefetch_desc(&tm_scales);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -318,19 +337,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (kMode == KvMode::kPagedFp8 && (warp == 0 || warp == 2 || warp == 3)) {
     // ===================================================== producer (FP8)
-    // Warp 0 lane 0 loads Q and the bf16 RoPE columns (chunk 8) by TMA.  The
-    // latent chunks 0..7 are dequantised by warps 0, 2, 3 chunk by chunk:
-    // 8 tokens per warp step, lane = (token, 16-code unit); value =
-    // bf16(e4m3 * scale[c / 2]) written into the 128-byte-swizzled slot.
+    // Warp 0 lane 0 loads Q, the bf16 RoPE columns (chunk 8) and, for every
+    // latent chunk this CTA converts, the raw e4m3 codes and token scales by
+    // TMA into that chunk's own slot (codes at +8 KB, scales at +4 KB), each
+    // as soon as the slot is released.  Warps 0, 2, 3 convert a slot in
+    // place: every thread reads its codes, the three warps meet at a named
+    // barrier, and bf16(e4m3 * scale[c / 2]) is written over the staging in
+    // the 128-byte-swizzled layout.  Lane = (token within a group of 8,
+    // 16-code unit); 16 groups per tile.  With two head blocks, a converted
+    // slot is also bulk-copied into the peer CTA's slot.
+    //
+    // Every blocking wait is skipped once `ok` is false; the three warps
+    // leave their loops only on the consensus `go` taken at a named barrier,
+    // so none is ever left alone at one.
     const int dw = warp == 0 ? 0 : warp - 1;  // dequant warp index 0..2
     const int unit = lane & 3;                 // 16-code unit of the 64-column chunk
     const int tsub = lane >> 2;                // token within a group of 8
+    const int own0 = share ? hb : 0, own_step = share ? 2 : 1;
+    const int n_own = (kChunks - 1) / own_step;
     PartCursor cur = part_cursor(meta, part);
     int q, t0, t1, split;
     uint32_t tile_ctr = 0, item_ctr = 0;
-    bool ok = true;
-    while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
-      if (warp == 0 && lane == 0) {
+    bool ok = true, go = true;
+    while (go && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+      if (warp == 0 && lane == 0 && ok) {
         ok = mbar_wait(smem_u32(&sm->q_empty), (item_ctr & 1) ^ 1, abort_flag, p.err);
         if (ok) {
           mbar_arrive_expect_tx(smem_u32(&sm->q_full), kChunks * p.rows * 128);
@@ -340,86 +370,124 @@ __global__ void __launch_bounds__(kThreads, 1)
                         l2_policy_evict_last());
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      for (int t = t0; t < t1 && ok; ++t) {
-        int32_t blk[2];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          blk[h2] = page_of(p, q, 2 * t + h2);
-          if (blk[h2] < 0) {
-            if (p.err && lane == 0 && warp == 0) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
-            blk[h2] = 0;  // read a valid page; the bad page's keys are wrong but finite
-          }
-        }
+      go = !named_barrier_or(kDequantBarrier, 32 * kDequantWarps, !ok);
+      for (int t = t0; t < t1 && go; ++t) {
         const uint32_t par = (tile_ctr & 1) ^ 1;
-        if (warp == 0 && lane == 0) {  // RoPE chunk by TMA
-          ok = mbar_wait(smem_u32(&sm->empty[kChunks - 1]), par, abort_flag, p.err);
-          if (ok) {
+        int32_t blk[2] = {0, 0};
+        int issued = 0;  // requests made for this tile (warp 0 lane 0)
+        auto slot_of = [&](int i) { return i == n_own ? kChunks - 1 : own0 + own_step * i; };
+        const uint64_t pol = l2_policy_evict_first();
+        // requests 0 .. n_own - 1: raw data of the owned latent chunks;
+        // request n_own: the RoPE chunk (its slot also carries P until the
+        // previous tile's P.V is done)
+        auto issue = [&](int i) {
+          if (i == n_own) {
             const uint32_t bar = smem_u32(&sm->full[kChunks - 1]);
             mbar_arrive_expect_tx(bar, kChunkBytes);
             const uint32_t dst = kv_base + (kChunks - 1) * kChunkBytes;
-            tma_load_2d(dst, &tm_kv, 0, blk[0] * kPage, bar, l2_policy_evict_first());
-            tma_load_2d(dst + kChunkBytes / 2, &tm_kv, 0, blk[1] * kPage, bar,
-                        l2_policy_evict_first());
+            tma_load_2d(dst, &tm_kv, 0, blk[0] * kPage, bar, pol);
+            tma_load_2d(dst + kChunkBytes / 2, &tm_kv, 0, blk[1] * kPage, bar, pol);
+            return;
+          }
+          const int c = own0 + own_step * i;
+          const uint32_t bar = smem_u32(&sm->raw_full[c]);
+          const uint32_t slot = kv_base + c * kChunkBytes;
+          mbar_arrive_expect_tx(bar, kRawCodeBytes + kRawScaleBytes);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            tma_load_2d(slot + kRawCodeOff + h2 * (kRawCodeBytes / 2), &tm_codes, c * 64,
+                        blk[h2] * kPage, bar, pol);
+            tma_load_2d(slot + kRawScaleOff + h2 * (kRawScaleBytes / 2), &tm_scales, 0,
+                        blk[h2] * kPage, bar);
+          }
+        };
+        if (warp == 0 && lane == 0 && ok) {
+          for (int h2 = 0; h2 < 2; ++h2) {
+            blk[h2] = page_of(p, q, 2 * t + h2);
+            if (blk[h2] < 0) {
+              if (p.err) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
+              blk[h2] = 0;  // read a valid page; the bad page's keys are wrong but finite
+            }
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        for (int c = 0; c < kChunks - 1; ++c) {
-          if (share && (c & 1) != hb) continue;  // the peer dequantises this chunk for both
-          if (lane == 0) ok = mbar_wait(smem_u32(&sm->empty[c]), par, abort_flag, p.err);
+        for (int k = 0; k < n_own; ++k) {
+          const int c = own0 + own_step * k;
+          if (warp == 0 && lane == 0 && ok) {
+            // this chunk's request (waiting for its slot) ...
+            while (ok && issued <= k) {
+              ok = mbar_wait(smem_u32(&sm->empty[slot_of(issued)]), par, abort_flag, p.err);
+              if (ok) issue(issued++);
+            }
+            // ... then, while its data is in flight, every later request
+            // whose slot has been released
+            const uint32_t rbar = smem_u32(&sm->raw_full[c]);
+            const uint64_t t_start = globaltimer_ns();
+            while (ok && !mbar_try_wait_hint(rbar, tile_ctr & 1, 200)) {
+              while (issued <= n_own && mbar_test_wait(smem_u32(&sm->empty[slot_of(issued)]), par))
+                issue(issued++);
+              if (*abort_flag) {
+                ok = false;
+              } else if (globaltimer_ns() - t_start > kWaitTimeoutNs) {
+                *abort_flag = 1u;
+                if (p.err) atomicOr(p.err, MLA_DEVERR_TIMEOUT);
+                ok = false;
+              }
+            }
+          } else if (lane == 0 && ok) {
+            ok = mbar_wait(smem_u32(&sm->raw_full[c]), tile_ctr & 1, abort_flag, p.err);
+          }
           ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
           const uint32_t slot = kv_base + c * kChunkBytes;
-          // all of this warp's code and scale loads for the chunk are issued
-          // before the first conversion, so their latencies overlap
           constexpr int kGroupsPerWarp = (kTileTokens / 8 + kDequantWarps - 1) / kDequantWarps;
           uint4 codes_g[kGroupsPerWarp];
           float sc_g[kGroupsPerWarp];
 #pragma unroll
-          for (int k = 0; k < kGroupsPerWarp; ++k) {
-            const int grp = dw + kDequantWarps * k;
-            if (grp < kTileTokens / 8) {
-              const int r = grp * 8 + tsub;
-              const uint8_t* tok = p.kv_fp8 +
-                                   (static_cast<int64_t>(blk[r >> 6]) * kPage + (r & 63)) * kFp8TokenBytes;
-              codes_g[k] = __ldg(reinterpret_cast<const uint4*>(tok + c * 64 + unit * 16));
-              sc_g[k] = __ldg(reinterpret_cast<const float*>(tok + kFp8ScaleOffset) + (c >> 1));
-            }
+          for (int g = 0; g < kGroupsPerWarp; ++g) {
+            const int grp = dw + kDequantWarps * g;
+            const int r = (grp < kTileTokens / 8 ? grp : 0) * 8 + tsub;
+            codes_g[g] = ld_shared_v4(slot + kRawCodeOff + r * 64 + unit * 16);
+            sc_g[g] = ld_shared_f32(slot + kRawScaleOff + r * 16 + (c >> 1) * 4);
           }
+          // all staging reads are done before any bf16 write lands on it
+          go = !named_barrier_or(kDequantBarrier, 32 * kDequantWarps, !ok);
+          if (!go) break;
 #pragma unroll
-          for (int k = 0; k < kGroupsPerWarp; ++k) {
-            const int grp = dw + kDequantWarps * k;
+          for (int g = 0; g < kGroupsPerWarp; ++g) {
+            const int grp = dw + kDequantWarps * g;
             if (grp >= kTileTokens / 8) continue;
             const int r = grp * 8 + tsub;  // token row of the tile
-            const uint4 codes = codes_g[k];
-            const float sc = sc_g[k];
+            const uint4 codes = codes_g[g];
+            const float sc = sc_g[g];
             const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
             uint32_t packed[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xFFFFu)));
-              const float2 b2 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16)));
-              packed[2 * k] = pack_bf16x2(a.x * sc, a.y * sc);
-              packed[2 * k + 1] = pack_bf16x2(b2.x * sc, b2.y * sc);
+            for (int i = 0; i < 4; ++i) {
+              const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu)));
+              const float2 b2 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16)));
+              packed[2 * i] = pack_bf16x2(a.x * sc, a.y * sc);
+              packed[2 * i + 1] = pack_bf16x2(b2.x * sc, b2.y * sc);
             }
             const uint32_t row = slot + r * 128;
-            const uint32_t a0 = row + ((2 * unit) ^ (r & 7)) * 16, a1 = row + ((2 * unit + 1) ^ (r & 7)) * 16;
-            st_shared_v4(a0, packed[0], packed[1], packed[2], packed[3]);
-            st_shared_v4(a1, packed[4], packed[5], packed[6], packed[7]);
-            if (share) {
-              st_shared_cluster_v4(mapa_shared(a0, hb ^ 1), packed[0], packed[1], packed[2], packed[3]);
-              st_shared_cluster_v4(mapa_shared(a1, hb ^ 1), packed[4], packed[5], packed[6], packed[7]);
-            }
+            st_shared_v4(row + ((2 * unit) ^ (r & 7)) * 16, packed[0], packed[1], packed[2], packed[3]);
+            st_shared_v4(row + ((2 * unit + 1) ^ (r & 7)) * 16, packed[4], packed[5], packed[6],
+                         packed[7]);
           }
           fence_proxy_async_smem();
-          if (share) fence_proxy_async_cluster();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(smem_u32(&sm->full[c]));
-            if (share) mbar_remote_arrive(mapa_shared(smem_u32(&sm->full[c]), hb ^ 1));
+          if (lane == 0) mbar_arrive(smem_u32(&sm->full[c]));
+          if (share && warp == 0 && lane == 0 && ok) {
+            // once all three warps have written the slot, one bulk copy puts
+            // it into the peer's slot and completes the peer's full barrier
+            ok = mbar_wait(smem_u32(&sm->full[c]), tile_ctr & 1, abort_flag, p.err);
+            if (ok) {
+              const uint32_t peer_bar = mapa_shared(smem_u32(&sm->full[c]), hb ^ 1);
+              mbar_remote_arrive_expect_tx(peer_bar, kChunkBytes);
+              bulk_copy_to_peer(mapa_shared(slot, hb ^ 1), slot, kChunkBytes, peer_bar);
+            }
           }
+        }
+        if (go && warp == 0 && lane == 0 && ok && issued == n_own) {  // the RoPE chunk, if still due
+          ok = mbar_wait(smem_u32(&sm->empty[kChunks - 1]), par, abort_flag, p.err);
+          if (ok) issue(issued++);
         }
         ++tile_ctr;
       }
@@ -578,7 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t par = tile_ctr & 1;
           // S^T = K_tile . Q^T: A = tile chunk (K-major), B = Q chunk (K-major)
           for (int c = 0; c < kChunks; ++c) {
-            ok = mbar_wait(smem_u32(&sm->full[c]), par, abort_flag, p.err);
+            // FP8 chunks converted by the peer complete on its bulk copy
+            ok = (share && c < kChunks - 1 && (c & 1) != hb)
+                     ? mbar_wait_cluster(smem_u32(&sm->full[c]), par, abort_flag, p.err)
+                     : mbar_wait(smem_u32(&sm->full[c]), par, abort_flag, p.err);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
