@@ -84,8 +84,7 @@ enum class KvMode : int { kPagedBf16 = 0, kSparseBf16 = 1, kPagedFp8 = 2 };
 constexpr int kFp8TokenBytes = 656;
 constexpr int kFp8ScaleOffset = 512;
 constexpr int kFp8RopeOffset = 528;
-constexpr int kDequantWarps = 3;  // warps 0, 2, 3 (warp 1 issues the MMAs)
-constexpr uint32_t kDequantBarrier = 5;  // named barrier of the three (1..4: softmax groups)
+constexpr uint32_t kDequantBarrier = 5;  // FP8: all softmax warps (1..4: one softmax group each)
 // staging of a latent chunk's raw FP8 data inside its own 16 KB bf16 slot
 constexpr int kRawScaleOff = 4096;                  // [128 tokens][4 fp32 scales]
 constexpr int kRawScaleBytes = kTileTokens * 16;
@@ -288,11 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool share = kMode == KvMode::kPagedFp8 && p.n_hblk == 2;
   if (threadIdx.x == 0) {
     for (int c = 0; c < kChunks; ++c) {
-      // FP8: a latent chunk is filled by this CTA's three dequantising warps,
-      // or by one bulk copy from the peer (one remote arrive + bytes)
-      const bool from_peer = share && (c & 1) != hb;
+      // FP8: a latent chunk is filled by this CTA's softmax warps (one
+      // arrive each), or by one bulk copy from the peer (one local arm + bytes)
+      const bool from_peer = share && c < kChunks - 1 && (c & 1) != hb;
       mbar_init(smem_u32(&sm->full[c]),
-                (kMode == KvMode::kPagedFp8 && c < kChunks - 1 && !from_peer) ? kDequantWarps : 1);
+                (kMode == KvMode::kPagedFp8 && c < kChunks - 1 && !from_peer) ? 4 * kSoftmaxGroups : 1);
       // a slot is free once the MMA threads of every CTA writing into it
       // have released it
       mbar_init(smem_u32(&sm->empty[c]), (multicast || (share && c < kChunks - 1)) ? 2 : 1);
@@ -305,6 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm->o_done), 1);
     sm->abort = 0;
     fence_mbarrier_init();
+    // the first tile's arm of every chunk the peer converts (the MMA thread
+    // re-arms after each use)
+    if (share)
+      for (int c = hb ^ 1; c < kChunks - 1; c += 2) mbar_arrive_expect_tx(smem_u32(&sm->full[c]), kChunkBytes);
   }
   if (p.rows < kRowsPerCta) {
     // Rows [rows, 64) of every Q chunk are never written by TMA; zero them
@@ -335,72 +338,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm->tmem_base;
   volatile uint32_t* abort_flag = &sm->abort;
 
-  if (kMode == KvMode::kPagedFp8 && (warp == 0 || warp == 2 || warp == 3)) {
+  if (kMode == KvMode::kPagedFp8 && warp == kProducerWarp) {
     // ===================================================== producer (FP8)
-    // Warp 0 lane 0 loads Q, the bf16 RoPE columns (chunk 8) and, for every
-    // latent chunk this CTA converts, the raw e4m3 codes and token scales by
-    // TMA into that chunk's own slot (codes at +8 KB, scales at +4 KB), each
-    // as soon as the slot is released.  Warps 0, 2, 3 convert a slot in
-    // place: every thread reads its codes, the three warps meet at a named
-    // barrier, and bf16(e4m3 * scale[c / 2]) is written over the staging in
-    // the 128-byte-swizzled layout.  Lane = (token within a group of 8,
-    // 16-code unit); 16 groups per tile.  With two head blocks, a converted
-    // slot is also bulk-copied into the peer CTA's slot.
-    //
-    // Every blocking wait is skipped once `ok` is false; the three warps
-    // leave their loops only on the consensus `go` taken at a named barrier,
-    // so none is ever left alone at one.
-    const int dw = warp == 0 ? 0 : warp - 1;  // dequant warp index 0..2
-    const int unit = lane & 3;                 // 16-code unit of the 64-column chunk
-    const int tsub = lane >> 2;                // token within a group of 8
-    const int own0 = share ? hb : 0, own_step = share ? 2 : 1;
-    const int n_own = (kChunks - 1) / own_step;
-    PartCursor cur = part_cursor(meta, part);
-    int q, t0, t1, split;
-    uint32_t tile_ctr = 0, item_ctr = 0;
-    bool ok = true, go = true;
-    while (go && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
-      if (warp == 0 && lane == 0 && ok) {
+    // Lane 0 loads Q, the bf16 RoPE columns (chunk 8) and, for every latent
+    // chunk this CTA converts, the raw e4m3 codes and token scales by TMA into
+    // that chunk's own slot (codes at +8 KB, scales at +4 KB), each as soon as
+    // the slot is released; the softmax warps convert the slot in place.
+    // With two head blocks, each converted slot then goes to the peer CTA's
+    // slot by one bulk copy (the peer's MMA thread has armed its barrier).
+    if (lane == 0) {
+      const int own0 = share ? hb : 0, own_step = share ? 2 : 1;
+      const int n_own = (kChunks - 1) / own_step;
+      PartCursor cur = part_cursor(meta, part);
+      int q, t0, t1, split;
+      uint32_t tile_ctr = 0, item_ctr = 0;
+      bool ok = true;
+      const uint64_t pol = l2_policy_evict_first();
+      while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
         ok = mbar_wait(smem_u32(&sm->q_empty), (item_ctr & 1) ^ 1, abort_flag, p.err);
-        if (ok) {
-          mbar_arrive_expect_tx(smem_u32(&sm->q_full), kChunks * p.rows * 128);
-          const int q_row = q * p.h + hb * kRowsPerCta;
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(q_base + c * kQChunkBytes, &tm_q, c * 64, q_row, smem_u32(&sm->q_full),
-                        l2_policy_evict_last());
-        }
-      }
-      go = !named_barrier_or(kDequantBarrier, 32 * kDequantWarps, !ok);
-      for (int t = t0; t < t1 && go; ++t) {
-        const uint32_t par = (tile_ctr & 1) ^ 1;
-        int32_t blk[2] = {0, 0};
-        int issued = 0;  // requests made for this tile (warp 0 lane 0)
-        auto slot_of = [&](int i) { return i == n_own ? kChunks - 1 : own0 + own_step * i; };
-        const uint64_t pol = l2_policy_evict_first();
-        // requests 0 .. n_own - 1: raw data of the owned latent chunks;
-        // request n_own: the RoPE chunk (its slot also carries P until the
-        // previous tile's P.V is done)
-        auto issue = [&](int i) {
-          if (i == n_own) {
-            const uint32_t bar = smem_u32(&sm->full[kChunks - 1]);
-            mbar_arrive_expect_tx(bar, kChunkBytes);
-            const uint32_t dst = kv_base + (kChunks - 1) * kChunkBytes;
-            tma_load_2d(dst, &tm_kv, 0, blk[0] * kPage, bar, pol);
-            tma_load_2d(dst + kChunkBytes / 2, &tm_kv, 0, blk[1] * kPage, bar, pol);
-            return;
-          }
-          const int c = own0 + own_step * i;
-          const uint32_t bar = smem_u32(&sm->raw_full[c]);
-          const uint32_t slot = kv_base + c * kChunkBytes;
-          mbar_arrive_expect_tx(bar, kRawCodeBytes + kRawScaleBytes);
-          for (int h2 = 0; h2 < 2; ++h2) {
-            tma_load_2d(slot + kRawCodeOff + h2 * (kRawCodeBytes / 2), &tm_codes, c * 64,
-                        blk[h2] * kPage, bar, pol);
-            tma_load_2d(slot + kRawScaleOff + h2 * (kRawScaleBytes / 2), &tm_scales, 0,
-                        blk[h2] * kPage, bar);
-          }
-        };
-        if (warp == 0 && lane == 0 && ok) {
+        if (!ok) break;
+        mbar_arrive_expect_tx(smem_u32(&sm->q_full), kChunks * p.rows * 128);
+        const int q_row = q * p.h + hb * kRowsPerCta;
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(q_base + c * kQChunkBytes, &tm_q, c * 64, q_row, smem_u32(&sm->q_full),
+                      l2_policy_evict_last());
+        for (int t = t0; t < t1 && ok; ++t) {
+          const uint32_t par = (tile_ctr & 1) ^ 1;
+          int32_t blk[2];
           for (int h2 = 0; h2 < 2; ++h2) {
             blk[h2] = page_of(p, q, 2 * t + h2);
             if (blk[h2] < 0) {
@@ -408,20 +372,43 @@ __global__ void __launch_bounds__(kThreads, 1)
               blk[h2] = 0;  // read a valid page; the bad page's keys are wrong but finite
             }
           }
-        }
-        for (int k = 0; k < n_own; ++k) {
-          const int c = own0 + own_step * k;
-          if (warp == 0 && lane == 0 && ok) {
-            // this chunk's request (waiting for its slot) ...
+          // requests 0 .. n_own - 1: raw data of the owned latent chunks;
+          // request n_own: the RoPE chunk (its slot also carries P until the
+          // previous tile's P.V is done)
+          int issued = 0;
+          auto slot_of = [&](int i) { return i == n_own ? kChunks - 1 : own0 + own_step * i; };
+          auto issue = [&](int i) {
+            if (i == n_own) {
+              const uint32_t bar = smem_u32(&sm->full[kChunks - 1]);
+              mbar_arrive_expect_tx(bar, kChunkBytes);
+              const uint32_t dst = kv_base + (kChunks - 1) * kChunkBytes;
+              tma_load_2d(dst, &tm_kv, 0, blk[0] * kPage, bar, pol);
+              tma_load_2d(dst + kChunkBytes / 2, &tm_kv, 0, blk[1] * kPage, bar, pol);
+              return;
+            }
+            const int c = own0 + own_step * i;
+            const uint32_t bar = smem_u32(&sm->raw_full[c]);
+            const uint32_t slot = kv_base + c * kChunkBytes;
+            mbar_arrive_expect_tx(bar, kRawCodeBytes + kRawScaleBytes);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              tma_load_2d(slot + kRawCodeOff + h2 * (kRawCodeBytes / 2), &tm_codes, c * 64,
+                          blk[h2] * kPage, bar, pol);
+              tma_load_2d(slot + kRawScaleOff + h2 * (kRawScaleBytes / 2), &tm_scales, 0,
+                          blk[h2] * kPage, bar);
+            }
+          };
+          for (int k = 0; k < n_own && ok; ++k) {
             while (ok && issued <= k) {
               ok = mbar_wait(smem_u32(&sm->empty[slot_of(issued)]), par, abort_flag, p.err);
               if (ok) issue(issued++);
             }
-            // ... then, while its data is in flight, every later request
-            // whose slot has been released
-            const uint32_t rbar = smem_u32(&sm->raw_full[c]);
+            if (!share || !ok) continue;
+            // chunk k converted: copy it to the peer; while waiting, make
+            // every later request whose slot has been released
+            const int c = own0 + own_step * k;
+            const uint32_t fbar = smem_u32(&sm->full[c]);
             const uint64_t t_start = globaltimer_ns();
-            while (ok && !mbar_try_wait_hint(rbar, tile_ctr & 1, 200)) {
+            while (ok && !mbar_try_wait_hint(fbar, tile_ctr & 1, 200)) {
               while (issued <= n_own && mbar_test_wait(smem_u32(&sm->empty[slot_of(issued)]), par))
                 issue(issued++);
               if (*abort_flag) {
@@ -432,66 +419,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
               }
             }
-          } else if (lane == 0 && ok) {
-            ok = mbar_wait(smem_u32(&sm->raw_full[c]), tile_ctr & 1, abort_flag, p.err);
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          const uint32_t slot = kv_base + c * kChunkBytes;
-          constexpr int kGroupsPerWarp = (kTileTokens / 8 + kDequantWarps - 1) / kDequantWarps;
-          uint4 codes_g[kGroupsPerWarp];
-          float sc_g[kGroupsPerWarp];
-#pragma unroll
-          for (int g = 0; g < kGroupsPerWarp; ++g) {
-            const int grp = dw + kDequantWarps * g;
-            const int r = (grp < kTileTokens / 8 ? grp : 0) * 8 + tsub;
-            codes_g[g] = ld_shared_v4(slot + kRawCodeOff + r * 64 + unit * 16);
-            sc_g[g] = ld_shared_f32(slot + kRawScaleOff + r * 16 + (c >> 1) * 4);
-          }
-          // all staging reads are done before any bf16 write lands on it
-          go = !named_barrier_or(kDequantBarrier, 32 * kDequantWarps, !ok);
-          if (!go) break;
-#pragma unroll
-          for (int g = 0; g < kGroupsPerWarp; ++g) {
-            const int grp = dw + kDequantWarps * g;
-            if (grp >= kTileTokens / 8) continue;
-            const int r = grp * 8 + tsub;  // token row of the tile
-            const uint4 codes = codes_g[g];
-            const float sc = sc_g[g];
-            const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-            uint32_t packed[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu)));
-              const float2 b2 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16)));
-              packed[2 * i] = pack_bf16x2(a.x * sc, a.y * sc);
-              packed[2 * i + 1] = pack_bf16x2(b2.x * sc, b2.y * sc);
-            }
-            const uint32_t row = slot + r * 128;
-            st_shared_v4(row + ((2 * unit) ^ (r & 7)) * 16, packed[0], packed[1], packed[2], packed[3]);
-            st_shared_v4(row + ((2 * unit + 1) ^ (r & 7)) * 16, packed[4], packed[5], packed[6],
-                         packed[7]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sm->full[c]));
-          if (share && warp == 0 && lane == 0 && ok) {
-            // once all three warps have written the slot, one bulk copy puts
-            // it into the peer's slot and completes the peer's full barrier
-            ok = mbar_wait(smem_u32(&sm->full[c]), tile_ctr & 1, abort_flag, p.err);
             if (ok) {
-              const uint32_t peer_bar = mapa_shared(smem_u32(&sm->full[c]), hb ^ 1);
-              mbar_remote_arrive_expect_tx(peer_bar, kChunkBytes);
-              bulk_copy_to_peer(mapa_shared(slot, hb ^ 1), slot, kChunkBytes, peer_bar);
+              const uint32_t slot = kv_base + c * kChunkBytes;
+              bulk_copy_to_peer(mapa_shared(slot, hb ^ 1), slot, kChunkBytes,
+                                mapa_shared(fbar, hb ^ 1));
             }
           }
+          while (ok && issued <= n_own) {  // the RoPE chunk, if still due
+            ok = mbar_wait(smem_u32(&sm->empty[slot_of(issued)]), par, abort_flag, p.err);
+            if (ok) issue(issued++);
+          }
+          ++tile_ctr;
         }
-        if (go && warp == 0 && lane == 0 && ok && issued == n_own) {  // the RoPE chunk, if still due
-          ok = mbar_wait(smem_u32(&sm->empty[kChunks - 1]), par, abort_flag, p.err);
-          if (ok) issue(issued++);
-        }
-        ++tile_ctr;
+        ++item_ctr;
       }
-      ++item_ctr;
     }
   } else if (warp == kProducerWarp && kMode == KvMode::kSparseBf16) {
     // ===================================================== producer (gather)
@@ -647,10 +588,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S^T = K_tile . Q^T: A = tile chunk (K-major), B = Q chunk (K-major)
           for (int c = 0; c < kChunks; ++c) {
             // FP8 chunks converted by the peer complete on its bulk copy
-            ok = (share && c < kChunks - 1 && (c & 1) != hb)
-                     ? mbar_wait_cluster(smem_u32(&sm->full[c]), par, abort_flag, p.err)
-                     : mbar_wait(smem_u32(&sm->full[c]), par, abort_flag, p.err);
+            const bool from_peer = share && c < kChunks - 1 && (c & 1) != hb;
+            ok = from_peer ? mbar_wait_cluster(smem_u32(&sm->full[c]), par, abort_flag, p.err)
+                           : mbar_wait(smem_u32(&sm->full[c]), par, abort_flag, p.err);
             if (!ok) break;
+            // next tile's arm: this phase is complete, so the arrive counts
+            // toward the next one, before the peer can start its copy
+            if (from_peer) mbar_arrive_expect_tx(smem_u32(&sm->full[c]), kChunkBytes);
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -714,6 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_o = tmem + lane_off + kTmemO + R * g;
     const uint32_t p_slot = kv_base + 8 * kChunkBytes;
     const uint32_t bar_id = 1 + g;
+    const int dq_r = (threadIdx.x - 32 * kSoftmaxWarp0) >> 2;  // FP8 conversion: token
+    const int dq_u = threadIdx.x & 3;                           // and 16-code unit
     const float NEG_INF = -INFINITY;
     float* red_w = &sm->red_max[g][wq][0];
     float* bc_m = &sm->bcast[g][wq][0];
@@ -735,7 +681,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < R; ++i) { lp[i] = 0.f; lb[i] = 0.f; }
       for (int t = t0; t < t1; ++t) {
+        if constexpr (kMode == KvMode::kPagedFp8) {
+          // ---- FP8: convert this tile's owned latent chunks in place.  Thread
+          // = (token dq_r, 16-code unit dq_u); reads of the staging finish at
+          // the named barrier before any bf16 write lands on it.  Every exit
+          // is decided at a barrier, so all 16 warps leave together.
+          const int own0 = share ? hb : 0, own_step = share ? 2 : 1;
+          for (int c = own0; c < kChunks - 1; c += own_step) {
+            if (lane == 0 && ok) ok = mbar_wait(smem_u32(&sm->raw_full[c]), tile_ctr & 1, abort_flag, p.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            const uint32_t slot = kv_base + c * kChunkBytes;
+            const uint4 codes = ld_shared_v4(slot + kRawCodeOff + dq_r * 64 + dq_u * 16);
+            const float sc = ld_shared_f32(slot + kRawScaleOff + dq_r * 16 + (c >> 1) * 4);
+            ok = !named_barrier_or(kDequantBarrier, 128 * kSoftmaxGroups, !ok);
+            if (!ok) break;
+            const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+            uint32_t packed[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu)));
+              const float2 b2 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16)));
+              packed[2 * i] = pack_bf16x2(a.x * sc, a.y * sc);
+              packed[2 * i + 1] = pack_bf16x2(b2.x * sc, b2.y * sc);
+            }
+            const uint32_t row = slot + dq_r * 128;
+            st_shared_v4(row + ((2 * dq_u) ^ (dq_r & 7)) * 16, packed[0], packed[1], packed[2], packed[3]);
+            st_shared_v4(row + ((2 * dq_u + 1) ^ (dq_r & 7)) * 16, packed[4], packed[5], packed[6], packed[7]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm->full[c]));
+          }
+          if (!ok) break;
+        }
         ok = mbar_wait(smem_u32(&sm->s_full), tile_ctr & 1, abort_flag, p.err);
+        if constexpr (kMode == KvMode::kPagedFp8)  // leave together (the barrier above)
+          ok = !named_barrier_or(kDequantBarrier, 128 * kSoftmaxGroups, !ok);
         if (!ok) break;
         tc_fence_after();
         float x[R];
@@ -851,6 +831,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bsum = (sm->red_bsum[g][0][row] + sm->red_bsum[g][1][row]) +
              (sm->red_bsum[g][2][row] + sm->red_bsum[g][3][row]);
       ok = mbar_wait(smem_u32(&sm->o_done), item_ctr & 1, abort_flag, p.err);
+      if constexpr (kMode == KvMode::kPagedFp8)  // the next piece starts at a shared barrier
+        ok = !named_barrier_or(kDequantBarrier, 128 * kSoftmaxGroups, !ok);
       if (!ok) break;
       tc_fence_after();
       const bool has = lsum > 0.f && bsum > 0.f;
