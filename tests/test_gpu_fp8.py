@@ -69,8 +69,12 @@ def test_fp8_h128_spec_ragged(parts):
     assert_parity(out, ref_o, lse, ref_l, f"fp8 spec parts={parts}")
 
 
-def test_fp8_single_key_rows_are_the_dequantised_row():
-    inp = fp8_case(53, 4, 1, 64, (1, 1, 1, 1), extra_pages=8)
+@pytest.mark.parametrize("h", [64, 128])
+def test_fp8_single_key_rows_are_the_dequantised_row(h):
+    # one visible key: the output row is that key's dequantised latent part
+    # (h = 128: the two head-block CTAs of a cluster each convert half of the
+    # latent chunks and copy them to the other)
+    inp = fp8_case(53, 4, 1, h, (1, 1, 1, 1), extra_pages=8)
     out, lse, err = run_fp8(inp)
     dec = oracle.fp8_tokens_to_f64(inp["kv_cache"].numpy())
     bt = inp["block_table"].numpy()
