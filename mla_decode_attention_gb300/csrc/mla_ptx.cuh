@@ -427,14 +427,6 @@ __device__ __forceinline__ void mbar_remote_arrive(uint32_t bar_cluster) {
                : "memory");
 }
 
-// Arrive once on a peer CTA's mbarrier and raise its expected transaction
-// bytes by `bytes` (release, cluster scope).
-__device__ __forceinline__ void mbar_remote_arrive_expect_tx(uint32_t bar_cluster, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;"
-               ::"r"(bar_cluster), "r"(bytes)
-               : "memory");
-}
-
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this
 // CTA's shared memory into a peer CTA's, completing on the peer's mbarrier.
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src,

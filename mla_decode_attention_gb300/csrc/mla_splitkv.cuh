@@ -19,11 +19,17 @@
 //
 // Roles (640 threads):
 //   warp 0 lane 0  : producer: TMA loads of Q (once per piece) and of each
-//                    tile's 9 column chunks (two 64-token pages per chunk),
-//                    plus L2 prefetches of the pages two tiles ahead
+//                    tile's 9 column chunks (two 64-token pages per chunk);
+//                    FP8 cache: the raw codes and scales of the latent chunks
+//                    (staged inside their slots) and the bf16 RoPE chunk, and
+//                    with two head blocks the copy of every converted chunk
+//                    into the peer CTA
 //   warp 1         : TMEM allocation; lane 0 issues every MMA
-//   warps 4..19    : four softmax warpgroups, query rows 16g .. 16g+15 each
-//   warps 2..3     : idle (dequantisers, with warp 0, for the FP8 cache)
+//   warps 4..19    : four softmax warpgroups, query rows 16g .. 16g+15 each;
+//                    FP8 cache: before each tile's scores they also convert
+//                    the staged codes to bf16 in place (one 16-code unit per
+//                    thread per chunk)
+//   warps 2..3     : idle
 //
 // Shared memory (1024-byte aligned): 9 KV chunk slots of [128 tok x 64 col]
 // bf16 (16 KB each, 128-byte swizzle), Q as 9 chunks of [64 rows x 64 col]
@@ -282,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup: barriers, TMEM, zeroed padding rows of Q
   const bool multicast = kClusterMulticast && p.n_hblk == 2;
-  // FP8 with two head blocks: each CTA dequantises half of the latent chunks
+  // FP8 with two head blocks: each CTA converts half of the latent chunks
   // (chunk c by head block c mod 2) and copies them into the peer's slots
   const bool share = kMode == KvMode::kPagedFp8 && p.n_hblk == 2;
   if (threadIdx.x == 0) {
