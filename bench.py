@@ -455,7 +455,7 @@ def run_reference(args):
     v = res["flops"] / t / 1e12
     sample = (f"{res['requests']} of 64 requests per step (all 128 heads, 4096 keys), fp64 "
               f"numpy oracle")
-    return {"metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": 0,
+    return {"metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (same seeded workload)", "impl": "reference",
