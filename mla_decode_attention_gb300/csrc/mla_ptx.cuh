@@ -164,18 +164,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
-// The same load delivered to the same shared-memory offset of every CTA in
-// `cta_mask` (cluster multicast); each destination's `bar` receives the bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, int32_t x,
-                                                      int32_t y, uint32_t bar, uint16_t cta_mask,
-                                                      uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-
 // Cluster-wide barrier of all threads of all CTAs in the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -502,26 +490,6 @@ __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
 }
 __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// mbar_wait for threads whose wake-up latency is not critical (TMA issuers,
-// hand-back threads): sleeps `ns` between polls so that waiting does not take
-// issue slots from the compute warps of the same SM sub-partition.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
-                                                uint32_t* err, uint32_t ns, bool cluster_scope = false) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    __nanosleep(ns);
-    if ((it & 15u) == 15u) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        *abort = 1u;
-        if (err) atomicOr(err, MLA_DEVERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
 }
 
 }  // namespace mla

@@ -66,13 +66,6 @@ constexpr int kThreads = 128 * (1 + kSoftmaxGroups);
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kPageBytes = kPage * 576 * 2;   // 73728 contiguous bytes per bf16 page
-constexpr int kPrefetchTiles = 2;
-// With two head blocks per cluster, each CTA loads one 64-token page half of
-// every chunk and multicasts it to both CTAs, so every KV byte leaves L2 once
-// per cluster and each CTA issues half the TMA boxes.
-constexpr bool kClusterMulticast = false;
-constexpr bool kPrefetchKv = false;
 // A later tile moves the softmax reference only when a score exceeds it by
 // more than this (log2 units): probabilities stay <= 2^8, exact in range.
 constexpr float kRescaleLog2 = 8.f;
@@ -230,26 +223,6 @@ __device__ __forceinline__ void load_bcast32(const float* src, float (&dst)[32])
   }
 }
 
-// Iterates the (sequence, tile) pairs of one part in order.
-struct TileWalker {
-  PartCursor cur;
-  int q, t, t1;
-  bool valid;
-  __device__ void init(const int32_t* meta, int num_parts, int part) {
-    cur = part_cursor(meta, part);
-    int t0, split;
-    valid = next_piece(meta, num_parts, &cur, &q, &t0, &t1, &split);
-    t = t0;
-  }
-  __device__ void advance(const int32_t* meta, int num_parts) {
-    if (!valid) return;
-    if (t + 1 < t1) { ++t; return; }
-    int t0, split;
-    valid = next_piece(meta, num_parts, &cur, &q, &t0, &t1, &split);
-    t = t0;
-  }
-};
-
 // Physical page of logical page `pg` of the sequence, or -1 if out of range.
 __device__ __forceinline__ int32_t page_of(const SplitParams& p, int q, int pg) {
   const int32_t keys = meta_seq(p.meta, p.num_parts, q)[kSKeys];
@@ -257,14 +230,6 @@ __device__ __forceinline__ int32_t page_of(const SplitParams& p, int q, int pg) 
   const int32_t* bt_row = p.block_table + static_cast<int64_t>(q / p.s_q) * p.bt_stride;
   const int32_t blk = bt_row[pg < last ? pg : last];
   return (blk < 0 || static_cast<int64_t>(blk) >= p.num_pages) ? -1 : blk;
-}
-
-__device__ __forceinline__ void prefetch_tile(const SplitParams& p, const TileWalker& w) {
-  if (!w.valid) return;
-  for (int h2 = 0; h2 < 2; ++h2) {
-    const int32_t blk = page_of(p, w.q, 2 * w.t + h2);
-    if (blk >= 0) prefetch_l2(p.kv_rows + static_cast<int64_t>(blk) * (kPage * 576), kPageBytes);
-  }
 }
 
 template <KvMode kMode>
@@ -287,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* meta = p.meta;
 
   // ---- setup: barriers, TMEM, zeroed padding rows of Q
-  const bool multicast = kClusterMulticast && p.n_hblk == 2;
   // FP8 with two head blocks: each CTA converts half of the latent chunks
   // (chunk c by head block c mod 2) and copies them into the peer's slots
   const bool share = kMode == KvMode::kPagedFp8 && p.n_hblk == 2;
@@ -300,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (kMode == KvMode::kPagedFp8 && c < kChunks - 1 && !from_peer) ? 4 * kSoftmaxGroups : 1);
       // a slot is free once the MMA threads of every CTA writing into it
       // have released it
-      mbar_init(smem_u32(&sm->empty[c]), (multicast || (share && c < kChunks - 1)) ? 2 : 1);
+      mbar_init(smem_u32(&sm->empty[c]), (share && c < kChunks - 1) ? 2 : 1);
     }
     for (int c = 0; c < kChunks - 1; ++c) mbar_init(smem_u32(&sm->raw_full[c]), 1);
     mbar_init(smem_u32(&sm->q_full), 1);
@@ -339,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (multicast || share) cluster_sync();  // peers' barriers are initialised before any remote arrive
+  if (share) cluster_sync();  // peers' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   volatile uint32_t* abort_flag = &sm->abort;
@@ -506,13 +470,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
-      const bool do_prefetch = kPrefetchKv && hb == 0;
-      TileWalker ahead;
-      ahead.init(meta, p.num_parts, part);
-      for (int k = 0; k <= kPrefetchTiles; ++k) {  // tiles #0..#2 of this part
-        if (do_prefetch && k > 0) prefetch_tile(p, ahead);
-        ahead.advance(meta, p.num_parts);
-      }
       PartCursor cur = part_cursor(meta, part);
       int q, t0, t1, split;
       uint32_t tile_ctr = 0, item_ctr = 0;
@@ -535,8 +492,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.rows * 1152);
         }
         for (int t = t0; t < t1 && ok; ++t) {
-          if (do_prefetch) prefetch_tile(p, ahead);
-          ahead.advance(meta, p.num_parts);
           int32_t y[2];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
@@ -554,13 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bar = smem_u32(&sm->full[c]);
             mbar_arrive_expect_tx(bar, kChunkBytes);
             const uint32_t dst = kv_base + c * kChunkBytes;
-            if (multicast) {
-              tma_load_2d_multicast(dst + hb * (kChunkBytes / 2), &tm_kv, c * 64, y[hb], bar,
-                                    static_cast<uint16_t>(0x3), pol_kv);
-            } else {
-              tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol_kv);
-              tma_load_2d(dst + kChunkBytes / 2, &tm_kv, c * 64, y[1], bar, pol_kv);
-            }
+            tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol_kv);
+            tma_load_2d(dst + kChunkBytes / 2, &tm_kv, c * 64, y[1], bar, pol_kv);
             issued[c] = static_cast<int32_t>(tile_ctr);
           }
           ++tile_ctr;
@@ -625,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t bp = sw128_desc(p_base + 2048 * s, kChunkBytes, 1024);
               mma_bf16_ss(tmem + kTmemO + 64 * m, a, bp, kIdescPV, (t != t0 || s != 0) ? 1u : 0u);
             }
-            if (multicast || share) {  // the slot is written by both CTAs' producers
+            if (share) {  // the slot is written by both CTAs' converters
               mma_commit_multicast(smem_u32(&sm->empty[2 * m]), 0x3);
               mma_commit_multicast(smem_u32(&sm->empty[2 * m + 1]), 0x3);
             } else {
@@ -633,8 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_commit(smem_u32(&sm->empty[2 * m + 1]));
             }
           }
-          if (multicast) mma_commit_multicast(smem_u32(&sm->empty[8]), 0x3);
-          else mma_commit(smem_u32(&sm->empty[8]));
+          mma_commit(smem_u32(&sm->empty[8]));
           if (t == t1 - 1) mma_commit(smem_u32(&sm->o_done));
           ++tile_ctr;
         }
@@ -887,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (multicast || share) cluster_sync();  // no peer still writes into this CTA's smem
+  if (share) cluster_sync();  // no peer still writes into this CTA's smem
   pdl_launch_dependents();
   if (warp == kMmaWarp) {
     tc_fence_after();
