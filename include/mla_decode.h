@@ -85,8 +85,9 @@ const char* mla_last_error(void);
 int mla_num_sm_parts(int device, int h_q, int* num_sm_parts);
 
 /*
- * Size in bytes of the schedule metadata for n_seq = batch * s_q query
- * sequences split over num_sm_parts parts.
+ * Size in bytes of the schedule metadata (both schedules, see
+ * mla_get_metadata) for n_seq = batch * s_q query sequences and
+ * num_sm_parts parts.
  */
 int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes);
 
@@ -100,13 +101,25 @@ int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes);
  *   dense, causal:      max(0, cache_seqlens[b] - s_q + 1 + j)
  *   dense, non-causal:  cache_seqlens[b]
  *   sparse (topk > 0):  topk   (cache_seqlens ignored, may be NULL)
- * Sequences are cut into 128-key tiles and the tiles are dealt out as
- * contiguous ranges of balanced cost (tiles + 2 per sequence piece) to the
- * parts; a sequence cut between parts becomes several splits that the
- * combine step merges.  Layout of `metadata` (int32):
+ * Sequences are cut into 128-key tiles.  The metadata holds two schedules
+ * of W = 16 + 8 * parts + 8 * n_seq words each:
+ *   A (words [0, W)): the tiles dealt out as contiguous ranges of balanced
+ *     cost (tiles + 2 per sequence piece) to the parts; a sequence cut
+ *     between parts becomes several splits that the combine step merges;
+ *   B (words [W, 2W)): present when n_seq <= num_sm_parts (else its magic is
+ *     0 and the rest is not written): part p walks the whole sequence p, no
+ *     sequence is split.
+ * The decode kernels walk B when its largest part cost is at most a
+ * kernel-specific split penalty (4 to 11 tiles) above A's balanced cost:
+ * every extra piece costs a Q load and an epilogue, every split row a
+ * combine read.  Layout of one schedule (int32):
  *   [0,16)                    header: magic 0x4D4C4131, version, n_seq,
  *                             num_sm_parts, tile_tokens (128), s_q, batch,
- *                             causal, topk, total_splits, cost_per_part, 0...
+ *                             causal, topk, total_splits, cost_per_part,
+ *                             largest sequence cost, chosen, 0...
+ *                             (chosen, in A only: 0 or 1 = the schedule the
+ *                             last decode call walked; the decode kernels
+ *                             write it and the combine reads it)
  *   [16, 16 + 8 * parts)      per part: q_begin, t_begin, q_end, t_end,
  *                             split_begin, 0, 0, 0 (half-open range of
  *                             (sequence, tile) pairs in lexicographic order)
@@ -149,7 +162,9 @@ int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts, size_t* by
  *  Cache slots past a request's length inside its last page must hold
  *  finite values (they are masked, but multiply a zero weight).
  *  metadata     from mla_get_metadata(cache_seqlens, batch, s_q, causal, 0,
- *               num_sm_parts, ...) on the same lengths.
+ *               num_sm_parts, ...) on the same lengths.  The kernels record
+ *               in its header word 12 which of its two schedules they walked
+ *               (read by the combine); nothing else in it is written.
  *  workspace    mla_workspace_size() bytes, 16-byte aligned.
  *  out, lse     outputs as described at the top of this file.  A query row
  *               with no visible key gets out = 0, lse = -inf.
@@ -157,7 +172,7 @@ int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts, size_t* by
 int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
                const int32_t* block_table, int64_t block_table_stride,
                const int32_t* cache_seqlens, int batch, int s_q, int h_q, float softmax_scale,
-               int causal, const void* metadata, int num_sm_parts, void* workspace, void* out,
+               int causal, void* metadata, int num_sm_parts, void* workspace, void* out,
                float* lse, uint32_t* err, cudaStream_t stream);
 
 /*
@@ -170,7 +185,7 @@ int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_p
 int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
                        const int32_t* block_table, int64_t block_table_stride,
                        const int32_t* cache_seqlens, int batch, int s_q, int h_q,
-                       float softmax_scale, int causal, const void* metadata, int num_sm_parts,
+                       float softmax_scale, int causal, void* metadata, int num_sm_parts,
                        void* workspace, void* out, float* lse, uint32_t* err,
                        cudaStream_t stream);
 
@@ -189,7 +204,7 @@ int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_format, int64
  */
 int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv, const int32_t* indices,
                       int topk, int batch, int s_q, int h_q, float softmax_scale,
-                      const void* metadata, int num_sm_parts, void* workspace, void* out,
+                      void* metadata, int num_sm_parts, void* workspace, void* out,
                       float* lse, uint32_t* err, cudaStream_t stream);
 
 /*
@@ -200,7 +215,7 @@ int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv, const int32_t
  */
 int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv, const int32_t* indices,
                               int topk, int batch, int s_q, int h_q, float softmax_scale,
-                              const void* metadata, int num_sm_parts, void* workspace, void* out,
+                              void* metadata, int num_sm_parts, void* workspace, void* out,
                               float* lse, uint32_t* err, cudaStream_t stream);
 
 /* Size of the device scratch array that mla_decode_noalloc uses (40 MiB). */

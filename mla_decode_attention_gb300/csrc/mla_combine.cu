@@ -26,12 +26,12 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(
   const int q = blockIdx.x;
   const int head = blockIdx.y * kCombineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  // The schedule was written before the split kernel started; only the
-  // partials need the split kernel to be done.
-  const int32_t* s = meta_seq(meta, num_parts, q);
+  // The split kernel records which of the two schedules it walked.
+  pdl_wait_primary();
+  const int32_t* sched = meta[kHChosen] ? schedule_b(meta) : meta;
+  const int32_t* s = meta_seq(sched, num_parts, q);
   const int n_splits = s[kSNSplits];
   const int off = s[kSSplitOff];
-  pdl_wait_primary();
   if (head >= h || n_splits == 1) return;  // single split: written by the split kernel
   const int b = q / s_q, j = q % s_q;
   __nv_bfloat16* orow = out + (static_cast<int64_t>(q) * h + head) * kDv + 16 * lane;

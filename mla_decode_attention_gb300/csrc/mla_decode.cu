@@ -156,7 +156,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
                                   int64_t num_pages, const int32_t* block_table,
                                   int64_t block_table_stride, const int32_t* cache_seqlens,
                                   int batch, int s_q, int h_q, float softmax_scale, int causal,
-                                  const void* metadata, int num_sm_parts, void* workspace,
+                                  void* metadata, int num_sm_parts, void* workspace,
                                   void* out, float* lse, uint32_t* err, cudaStream_t stream) {
   int rc = check_common(batch, s_q, h_q, num_sm_parts);
   if (rc != MLA_OK) return rc;
@@ -198,7 +198,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   }
 
   SplitParams prm = {};
-  prm.meta = static_cast<const int32_t*>(metadata);
+  prm.meta = static_cast<int32_t*>(metadata);
   prm.block_table = block_table;
   prm.bt_stride = block_table_stride;
   prm.num_pages = num_pages;
@@ -226,7 +226,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
 extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
                           const int32_t* block_table, int64_t block_table_stride,
                           const int32_t* cache_seqlens, int batch, int s_q, int h_q,
-                          float softmax_scale, int causal, const void* metadata, int num_sm_parts,
+                          float softmax_scale, int causal, void* metadata, int num_sm_parts,
                           void* workspace, void* out, float* lse, uint32_t* err,
                           cudaStream_t stream) {
   const int rc = mla_decode_splitkv(q, kv_cache, kv_format, num_pages, block_table,
@@ -239,7 +239,7 @@ extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, in
 
 extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv,
                                          const int32_t* indices, int topk, int batch, int s_q,
-                                         int h_q, float softmax_scale, const void* metadata,
+                                         int h_q, float softmax_scale, void* metadata,
                                          int num_sm_parts, void* workspace, void* out, float* lse,
                                          uint32_t* err, cudaStream_t stream) {
   int rc = check_common(batch, s_q, h_q, num_sm_parts);
@@ -261,7 +261,7 @@ extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t 
     return record_error("cuTensorMapEncodeTiled failed for kv", MLA_ERR_CUDA);
 
   SplitParams prm = {};
-  prm.meta = static_cast<const int32_t*>(metadata);
+  prm.meta = static_cast<int32_t*>(metadata);
   prm.indices = indices;
   prm.topk = topk;
   prm.s_kv = s_kv;
@@ -286,7 +286,7 @@ extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t 
 
 extern "C" int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv,
                                  const int32_t* indices, int topk, int batch, int s_q, int h_q,
-                                 float softmax_scale, const void* metadata, int num_sm_parts,
+                                 float softmax_scale, void* metadata, int num_sm_parts,
                                  void* workspace, void* out, float* lse, uint32_t* err,
                                  cudaStream_t stream) {
   const int rc = mla_sparse_decode_splitkv(q, kv, s_kv, indices, topk, batch, s_q, h_q,

@@ -58,8 +58,13 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   const int q0 = threadIdx.x * chunk;
   const int q1 = min(n_seq, q0 + chunk);
 
+  __shared__ int32_t s_max_cost;
+  if (threadIdx.x == 0) s_max_cost = 0;
+  __syncthreads();
+
   // 1. tiles, keys and cost per sequence; chunk-local cost prefix.
   int64_t local = 0;
+  int32_t local_max = 0, local_nonempty = 0;
   for (int q = q0; q < q1; ++q) {
     const int32_t keys = seq_keys(seqlens, q / s_q, q % s_q, s_q, causal, topk);
     const int32_t nt = tiles_of(keys);
@@ -67,7 +72,10 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
     s[kSTiles] = nt; s[kSKeys] = keys; s[5] = 0; s[6] = 0; s[7] = 0;
     s[kSCostPrefix] = static_cast<int32_t>(local);
     local += cost_of(nt);
+    local_max = max(local_max, cost_of(nt));
+    local_nonempty += nt > 0 ? 1 : 0;
   }
+  atomicMax(&s_max_cost, local_max);
   int64_t base;
   const int64_t total = block_exclusive_scan(local, &base, warp_sums);
   for (int q = q0; q < q1; ++q) {
@@ -109,13 +117,38 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
       fill_part(meta, num_parts, MetaPrefix{meta, num_parts}, n_seq, total, per_part, p);
   }
 
+  // 4. schedule B (one whole sequence per part), when every sequence has a part.
+  const bool has_b = n_seq <= num_parts;
+  int32_t* mb = meta + meta_words(n_seq, num_parts);
+  int64_t b_base = 0;
+  const int64_t b_splits = has_b ? block_exclusive_scan(local_nonempty, &b_base, warp_sums) : 0;
+  if (has_b) {
+    int64_t run_b = b_base;
+    for (int q = q0; q < q1; ++q) {
+      const int32_t* sa = meta_seq(meta, num_parts, q);
+      int32_t* sb = meta_seq(mb, num_parts, q);
+      const int32_t nt = sa[kSTiles];
+      sb[kSTiles] = nt; sb[kSSplitOff] = static_cast<int32_t>(run_b); sb[kSNSplits] = nt > 0 ? 1 : 0;
+      sb[kSKeys] = sa[kSKeys]; sb[kSCostPrefix] = sa[kSCostPrefix]; sb[5] = 0; sb[6] = 0; sb[7] = 0;
+      run_b += nt > 0 ? 1 : 0;
+    }
+    for (int p = threadIdx.x; p < num_parts; p += kMetaThreads) fill_whole_part(mb, num_parts, n_seq, p);
+  }
+
   if (threadIdx.x == 0) {
+    const int32_t max_cost = s_max_cost;
     meta[kHMagic] = kMetaMagic; meta[kHVersion] = kMetaVersion; meta[kHNSeq] = n_seq;
     meta[kHParts] = num_parts; meta[kHTile] = kTileTokens; meta[kHSq] = s_q;
     meta[kHBatch] = batch; meta[kHCausal] = causal; meta[kHTopk] = topk;
     meta[kHTotalSplits] = static_cast<int32_t>(total_splits);
     meta[kHPerPart] = static_cast<int32_t>(per_part);
-    for (int i = kHPerPart + 1; i < kHeaderWords; ++i) meta[i] = 0;
+    meta[kHMaxCost] = max_cost;
+    for (int i = kHMaxCost + 1; i < kHeaderWords; ++i) meta[i] = 0;
+    for (int i = 0; i < kHeaderWords; ++i) mb[i] = has_b ? meta[i] : 0;
+    if (has_b) {
+      mb[kHTotalSplits] = static_cast<int32_t>(b_splits);
+      mb[kHPerPart] = max_cost;
+    }
   }
 }
 
@@ -175,7 +208,7 @@ extern "C" int mla_num_sm_parts(int device, int h_q, int* num_sm_parts) {
 extern "C" int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes) {
   if (!bytes) return MLA_ERR_NULL;
   if (batch <= 0 || s_q <= 0 || s_q > kMaxSq || num_sm_parts <= 0) return MLA_ERR_SHAPE;
-  *bytes = static_cast<size_t>(meta_words(batch * s_q, num_sm_parts)) * sizeof(int32_t);
+  *bytes = static_cast<size_t>(meta_total_words(batch * s_q, num_sm_parts)) * sizeof(int32_t);
   return MLA_OK;
 }
 
@@ -216,6 +249,7 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
   int32_t* meta = static_cast<int32_t*>(metadata_host);
   const int n_seq = batch * s_q;
   int64_t total = 0;
+  int32_t max_cost = 0;
   for (int q = 0; q < n_seq; ++q) {
     const int32_t keys = seq_keys(seqlens, q / s_q, q % s_q, s_q, causal ? 1 : 0, topk);
     const int32_t nt = tiles_of(keys);
@@ -223,6 +257,7 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
     s[kSTiles] = nt; s[kSKeys] = keys; s[5] = 0; s[6] = 0; s[7] = 0;
     s[kSCostPrefix] = static_cast<int32_t>(total);
     total += cost_of(nt);
+    if (cost_of(nt) > max_cost) max_cost = cost_of(nt);
   }
   const int64_t per_part = total > 0 ? (total + num_sm_parts - 1) / num_sm_parts : 1;
   int64_t splits = 0;
@@ -240,6 +275,25 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
   meta[kHBatch] = batch; meta[kHCausal] = causal ? 1 : 0; meta[kHTopk] = topk;
   meta[kHTotalSplits] = static_cast<int32_t>(splits);
   meta[kHPerPart] = static_cast<int32_t>(per_part);
-  for (int i = kHPerPart + 1; i < kHeaderWords; ++i) meta[i] = 0;
+  meta[kHMaxCost] = max_cost;
+  for (int i = kHMaxCost + 1; i < kHeaderWords; ++i) meta[i] = 0;
+  // schedule B (one whole sequence per part), when every sequence has a part
+  const bool has_b = n_seq <= num_sm_parts;
+  int32_t* mb = meta + meta_words(n_seq, num_sm_parts);
+  for (int i = 0; i < kHeaderWords; ++i) mb[i] = has_b ? meta[i] : 0;
+  if (has_b) {
+    int64_t b_splits = 0;
+    for (int q = 0; q < n_seq; ++q) {
+      const int32_t* sa = meta_seq(meta, num_sm_parts, q);
+      int32_t* sb = meta_seq(mb, num_sm_parts, q);
+      const int32_t nt = sa[kSTiles];
+      sb[kSTiles] = nt; sb[kSSplitOff] = static_cast<int32_t>(b_splits); sb[kSNSplits] = nt > 0 ? 1 : 0;
+      sb[kSKeys] = sa[kSKeys]; sb[kSCostPrefix] = sa[kSCostPrefix]; sb[5] = 0; sb[6] = 0; sb[7] = 0;
+      b_splits += nt > 0 ? 1 : 0;
+    }
+    for (int p = 0; p < num_sm_parts; ++p) fill_whole_part(mb, num_sm_parts, n_seq, p);
+    mb[kHTotalSplits] = static_cast<int32_t>(b_splits);
+    mb[kHPerPart] = max_cost;
+  }
   return MLA_OK;
 }

@@ -133,7 +133,6 @@ __global__ void __maxnreg__(224)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const int part = blockIdx.x >> 1;
-  const int32_t* meta = p.meta;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKGroups; ++i) {
@@ -179,6 +178,14 @@ __global__ void __maxnreg__(224)
   // dependent launch); its results (the schedule, the inputs) are read below.
   pdl_wait_primary();
   pdl_launch_dependents();  // the combine may launch now; it waits for this grid to finish
+  // Schedule B (whole sequences) is walked when it is at most kSplitPenalty
+  // tiles longer than A: on b=64, t=4096 (~2.3 us per dense tile) splitting
+  // over 76 parts cost ~26 us in extra pieces and the combine for ~12 us of
+  // better balance; a sparse tile takes about twice as long.
+  constexpr int kSplitPenalty = kSparse ? 5 : 11;
+  const int32_t* meta = schedule_for(p.meta, kSplitPenalty);
+  if (blockIdx.x == 0 && threadIdx.x == 0)  // read by the combine after this grid
+    p.meta[kHChosen] = meta == p.meta ? 0 : 1;
   if (threadIdx.x == 0 && rank == 0) {  // the first piece's query rows start towards L2
     PartCursor c0 = part_cursor(meta, part);
     int q0, a0, b0, s0;

@@ -3,10 +3,16 @@
 //
 // Each (request b, new token j) is a sequence q = b * s_q + j whose keys are
 // cut into 128-key tiles.  A sequence piece costs its tiles plus kFixedCost
-// (the Q load and the epilogue); the global cost line is cut into
-// num_parts equal ranges, so a sequence may be split between parts
-// (FlashMLA deep dive, "Tile Scheduler": balanced assignment of requests and
-// blocks to SMs; DeepGEMM & FlashMLA article, section 7 "split-KV").
+// (the Q load and the epilogue).  The metadata holds two schedules (FlashMLA
+// deep dive, "Tile Scheduler": balanced assignment of requests and blocks to
+// SMs; DeepGEMM & FlashMLA article, section 7 "split-KV"):
+//   A: the global cost line cut into num_parts equal ranges, so a sequence
+//      may be split between parts (its splits are merged by the combine);
+//   B: (only when n_seq <= num_parts) part p walks the whole sequence p, so
+//      nothing is split and the combine has nothing to merge.
+// A decode kernel walks B when B's longest part costs at most its own split
+// penalty more than A's balanced part: every extra piece pays a Q load and
+// an epilogue, and every split row a combine read.
 #pragma once
 
 #include <cstdint>
@@ -24,10 +30,12 @@ constexpr int kFixedCost = 2;  // a piece switch (Q load, epilogue) costs about 
 constexpr int32_t kMetaMagic = 0x4D4C4131;  // "MLA1"
 constexpr int32_t kMetaVersion = 1;
 
-// header words
+// header words (kHMaxCost: the largest single-sequence cost; kHChosen, in
+// schedule A's header only: the schedule the last decode kernel walked,
+// 0 = A, 1 = B, written by that kernel for the combine)
 enum : int {
   kHMagic = 0, kHVersion, kHNSeq, kHParts, kHTile, kHSq, kHBatch, kHCausal, kHTopk,
-  kHTotalSplits, kHPerPart, kHeaderWords = 16
+  kHTotalSplits, kHPerPart, kHMaxCost, kHChosen, kHeaderWords = 16
 };
 constexpr int kPartWords = 8;  // q_begin, t_begin, q_end, t_end, split_begin, 0, 0, 0
 constexpr int kSeqWords = 8;   // n_tiles, split_offset, n_splits, keys, cost_prefix, 0, 0, 0
@@ -37,6 +45,8 @@ MLA_HD int64_t meta_words(int n_seq, int num_parts) {
   return kHeaderWords + static_cast<int64_t>(kPartWords) * num_parts +
          static_cast<int64_t>(kSeqWords) * n_seq;
 }
+// Both schedules: A at word 0, B right after it.
+MLA_HD int64_t meta_total_words(int n_seq, int num_parts) { return 2 * meta_words(n_seq, num_parts); }
 MLA_HD int32_t* meta_part(int32_t* m, int p) { return m + kHeaderWords + kPartWords * p; }
 MLA_HD const int32_t* meta_part(const int32_t* m, int p) {
   return m + kHeaderWords + kPartWords * p;
@@ -123,6 +133,30 @@ MLA_HD void fill_part(int32_t* meta, int num_parts, const Prefix& prefix, int n_
   if (qb < n_seq && tb > 0) split_begin = static_cast<int32_t>(p - floordiv(prefix(qb) + kFixedCost, per_part));
   int32_t* r = meta_part(meta, p);
   r[0] = qb; r[1] = tb; r[2] = qe; r[3] = te; r[4] = split_begin;
+  r[5] = 0; r[6] = 0; r[7] = 0;
+}
+
+// Schedule B of a metadata buffer (its magic is 0 when it does not exist).
+MLA_HD const int32_t* schedule_b(const int32_t* meta) {
+  return meta + meta_words(meta[kHNSeq], meta[kHParts]);
+}
+MLA_HD int32_t* schedule_b(int32_t* meta) { return meta + meta_words(meta[kHNSeq], meta[kHParts]); }
+
+// The schedule a decode kernel with split penalty `penalty` (tile units)
+// walks: B when it exists and costs at most `penalty` more than A.
+MLA_HD bool choose_whole_sequences(const int32_t* meta, int penalty) {
+  return schedule_b(meta)[kHMagic] == kMetaMagic &&
+         static_cast<int64_t>(meta[kHMaxCost]) <= static_cast<int64_t>(meta[kHPerPart]) + penalty;
+}
+MLA_HD const int32_t* schedule_for(const int32_t* meta, int penalty) {
+  return choose_whole_sequences(meta, penalty) ? schedule_b(meta) : meta;
+}
+
+// Schedule B's records: part p walks sequence p (none when p >= n_seq).
+MLA_HD void fill_whole_part(int32_t* meta_b, int num_parts, int n_seq, int p) {
+  int32_t* r = meta_part(meta_b, p);
+  const int q = p < n_seq ? p : n_seq;
+  r[0] = q; r[1] = 0; r[2] = p < n_seq ? p + 1 : n_seq; r[3] = 0; r[4] = 0;
   r[5] = 0; r[6] = 0; r[7] = 0;
 }
 

@@ -93,7 +93,7 @@ static_assert(kRawScaleOff + kRawScaleBytes <= kRawCodeOff && kRawCodeOff + kRaw
               "staging fits in the slot");
 
 struct SplitParams {
-  const int32_t* meta;
+  int32_t* meta;  // the kernels record the schedule they walk (header word kHChosen)
   const int32_t* block_table;
   int64_t bt_stride;
   int64_t num_pages;       // dense: pages in the cache
@@ -249,7 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int part = blockIdx.x / p.n_hblk;
   const int hb = blockIdx.x % p.n_hblk;
-  const int32_t* meta = p.meta;
+  // Schedule B (whole sequences) only when nearly balanced: a tile of this
+  // kernel takes ~3-6 us, so the ~26 us that splitting costs is ~4 tiles.
+  constexpr int kSplitPenalty = 4;
+  const int32_t* meta = schedule_for(p.meta, kSplitPenalty);
+  if (blockIdx.x == 0 && threadIdx.x == 0)  // read by the combine after this grid
+    p.meta[kHChosen] = meta == p.meta ? 0 : 1;
 
   // ---- setup: barriers, TMEM, zeroed padding rows of Q
   // FP8 with two head blocks: each CTA converts half of the latent chunks

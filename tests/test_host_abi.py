@@ -51,7 +51,8 @@ def test_status_strings():
 
 
 def test_sizes():
-    assert binding.mla_metadata_size(64, 1, 76) == 4 * (16 + 8 * 76 + 8 * 64)
+    # two schedules (A: balanced ranges, B: one whole sequence per part)
+    assert binding.mla_metadata_size(64, 1, 76) == 2 * 4 * (16 + 8 * 76 + 8 * 64)
     assert binding.mla_workspace_size(64, 1, 128, 76) == (64 + 76) * 128 * 513 * 4
     with pytest.raises(binding.MlaError):
         binding.mla_workspace_size(64, 1, 100, 76)      # unsupported head count
@@ -158,7 +159,38 @@ def check_schedule(seqlens, s_q, causal, topk, parts):
     assert np.array_equal(seq[:, 1], offs)
     assert hdr[9] == seq[:, 2].sum() <= b * s_q + parts
     assert max(per_part_cost) <= hdr[10] + FIXED_COST
+    costs = [int(nt) + FIXED_COST if nt > 0 else 0 for nt in seq[:, 0]]
+    assert hdr[11] == max(costs) and hdr[12] == 0
+    check_whole_sequence_schedule(m, b * s_q, parts, hdr, seq)
     return m
+
+
+def check_whole_sequence_schedule(m, n_seq, parts, hdr_a, seq_a):
+    """Schedule B: present iff n_seq <= parts; part p walks all of sequence p."""
+    words = 16 + 8 * parts + 8 * n_seq
+    assert len(m) == 2 * words
+    hdr, prt, seq = parse_meta(m[words:], n_seq, parts)
+    if n_seq > parts:
+        assert not hdr.any()
+        return
+    assert np.array_equal(hdr[:9], hdr_a[:9]) and hdr[10] == hdr[11] == hdr_a[11]
+    assert np.array_equal(seq[:, [0, 3, 4]], seq_a[:, [0, 3, 4]])
+    assert np.array_equal(seq[:, 2], (seq[:, 0] > 0).astype(np.int32))
+    assert np.array_equal(seq[:, 1], np.concatenate([[0], np.cumsum(seq[:, 2])[:-1]]))
+    assert hdr[9] == seq[:, 2].sum()
+    for p in range(parts):
+        pieces = walk_part(prt[p], seq)
+        if p < n_seq and seq[p, 0] > 0:
+            assert pieces == [(p, 0, int(seq[p, 0]), 0)]
+        else:
+            assert pieces == []
+
+
+def walks_whole_sequences(m, penalty):
+    """The kernels' choice: B when present and at most `penalty` tiles longer."""
+    hdr = m[:16]
+    words = 16 + 8 * int(hdr[3]) + 8 * int(hdr[2])
+    return m[words] == 0x4D4C4131 and hdr[11] <= hdr[10] + penalty
 
 
 @pytest.mark.parametrize("parts", [1, 2, 7, 76, 152, 400])
@@ -187,3 +219,17 @@ def test_schedule_config_dense_v3_shape():
     hdr, prt, seq = parse_meta(m, 64, 76)
     assert hdr[10] == (64 * (32 + FIXED_COST) + 75) // 76   # balanced cost per part
     assert seq[:, 2].max() <= 3
+    # 34 tiles per part unsplit against 29 split: the two-SM kernels (split
+    # penalties 11 dense, 5 sparse) walk whole sequences, the one-SM kernel (4)
+    # the balanced split
+    assert walks_whole_sequences(m, 11) and walks_whole_sequences(m, 5)
+    assert not walks_whole_sequences(m, 4)
+
+
+def test_schedule_choice_prefers_splitting_long_uneven_batches():
+    # 32 requests of 8192 keys over 76 parts: unsplit 66 tiles against 28
+    m = check_schedule(np.full(32, 8192, np.int32), 1, True, 0, 76)
+    assert not walks_whole_sequences(m, 11)
+    # more sequences than parts: no schedule B at all
+    m = check_schedule(np.full(80, 1000, np.int32), 1, True, 0, 76)
+    assert not walks_whole_sequences(m, 1000)
