@@ -12,10 +12,15 @@ namespace mla {
 
 namespace {
 
-constexpr int kMetaThreads = 1024;
 constexpr int kSmemPrefixes = 8192;  // sequences whose cost prefixes the schedule keeps in smem
+// one CTA of 128 threads up to this many sequences (fewer warps to meet at
+// each barrier), else 1024
+constexpr int kSmallMetaSeqs = 2048;
+// schedule B's count of non-empty sequences rides in the low bits of the cost scan
+constexpr int kCountBits = 25;  // n_seq <= 2^24
 
 // Block-wide exclusive scan of one int64 per thread; returns the total.
+template <int kMetaThreads>
 __device__ int64_t block_exclusive_scan(int64_t v, int64_t* out_excl, int64_t* warp_sums) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int64_t x = v;
@@ -45,6 +50,7 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t* out_excl, int64_t* w
 
 // One CTA builds the whole schedule.  Thread i owns the contiguous sequence
 // chunk [i*chunk, (i+1)*chunk).
+template <int kMetaThreads>
 __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* seqlens, int batch,
                                                                 int s_q, int causal, int topk,
                                                                 int num_parts, int32_t* meta) {
@@ -76,8 +82,12 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
     local_nonempty += nt > 0 ? 1 : 0;
   }
   atomicMax(&s_max_cost, local_max);
-  int64_t base;
-  const int64_t total = block_exclusive_scan(local, &base, warp_sums);
+  int64_t packed_base;
+  const int64_t packed_total = block_exclusive_scan<kMetaThreads>(
+      (local << kCountBits) | local_nonempty, &packed_base, warp_sums);
+  const int64_t base = packed_base >> kCountBits, total = packed_total >> kCountBits;
+  const int64_t b_base = packed_base & ((int64_t{1} << kCountBits) - 1);
+  const int64_t b_splits = packed_total & ((int64_t{1} << kCountBits) - 1);
   for (int q = q0; q < q1; ++q) {
     int32_t* sq = meta_seq(meta, num_parts, q);
     sq[kSCostPrefix] += static_cast<int32_t>(base);
@@ -98,7 +108,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
     nsplit_local += ns;
   }
   int64_t split_base;
-  const int64_t total_splits = block_exclusive_scan(nsplit_local, &split_base, warp_sums);
+  const int64_t total_splits = block_exclusive_scan<kMetaThreads>(nsplit_local, &split_base, warp_sums);
   int64_t run = split_base;
   for (int q = q0; q < q1; ++q) {
     int32_t* s = meta_seq(meta, num_parts, q);
@@ -120,8 +130,6 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   // 4. schedule B (one whole sequence per part), when every sequence has a part.
   const bool has_b = n_seq <= num_parts;
   int32_t* mb = meta + meta_words(n_seq, num_parts);
-  int64_t b_base = 0;
-  const int64_t b_splits = has_b ? block_exclusive_scan(local_nonempty, &b_base, warp_sums) : 0;
   if (has_b) {
     int64_t run_b = b_base;
     for (int q = q0; q < q1; ++q) {
@@ -236,8 +244,12 @@ extern "C" int mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q
                                 int topk, int num_sm_parts, void* metadata, cudaStream_t stream) {
   const int rc = check_meta_args(cache_seqlens, batch, s_q, topk, num_sm_parts, metadata);
   if (rc != MLA_OK) return rc;
-  metadata_kernel<<<1, kMetaThreads, 0, stream>>>(cache_seqlens, batch, s_q, causal ? 1 : 0, topk,
-                                                 num_sm_parts, static_cast<int32_t*>(metadata));
+  if (static_cast<int64_t>(batch) * s_q <= kSmallMetaSeqs)
+    metadata_kernel<128><<<1, 128, 0, stream>>>(cache_seqlens, batch, s_q, causal ? 1 : 0, topk,
+                                                num_sm_parts, static_cast<int32_t*>(metadata));
+  else
+    metadata_kernel<1024><<<1, 1024, 0, stream>>>(cache_seqlens, batch, s_q, causal ? 1 : 0, topk,
+                                                  num_sm_parts, static_cast<int32_t*>(metadata));
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MLA_OK : record_cuda_error("metadata kernel launch", e);
 }

@@ -150,15 +150,16 @@ def test_repeat_calls_are_deterministic():
     assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
 
 
-def test_device_metadata_matches_host_mirror():
+@pytest.mark.parametrize("batch", [70, 2100])  # the 128- and the 1024-thread schedule kernel
+def test_device_metadata_matches_host_mirror(batch):
     rng = np.random.default_rng(5)
-    sl = rng.integers(0, 9000, size=70).astype(np.int32)
-    for s_q, causal, parts in ((1, True, 76), (2, True, 152), (3, False, 5)):
-        n = binding.mla_metadata_size(70, s_q, parts) // 4
+    sl = rng.integers(0, 9000, size=batch).astype(np.int32)
+    for s_q, causal, parts in ((1, True, 76), (2, True, 152), (3, False, 5), (1, True, 4096)):
+        n = binding.mla_metadata_size(batch, s_q, parts) // 4
         meta = torch.zeros(n, dtype=torch.int32, device=DEV)
-        binding.mla_get_metadata(torch.from_numpy(sl).to(DEV), 70, s_q, causal, 0, parts, meta)
+        binding.mla_get_metadata(torch.from_numpy(sl).to(DEV), batch, s_q, causal, 0, parts, meta)
         torch.cuda.synchronize()
-        host = binding.mla_get_metadata_host(sl, 70, s_q, causal, 0, parts)
+        host = binding.mla_get_metadata_host(sl, batch, s_q, causal, 0, parts)
         assert np.array_equal(meta.cpu().numpy(), host)
 
 
