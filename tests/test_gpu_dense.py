@@ -150,6 +150,27 @@ def test_repeat_calls_are_deterministic():
     assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
 
 
+@pytest.mark.parametrize("h,parts,walked", [(128, 76, 1), (128, 3, 0), (64, 76, 0), (64, 4, 1)])
+def test_kernels_record_the_schedule_they_walk(h, parts, walked):
+    """Four requests of 1000 keys (8 tiles, cost 10).  Schedule B (one whole
+    sequence per part) exists when parts >= 4.  With 76 parts A's balanced
+    cost is 1: the two-SM kernel (h = 128, split penalty 11) takes B, the
+    one-SM kernel (penalty 4) keeps A; with 4 parts A costs 10 as well and
+    the one-SM kernel takes B."""
+    w = workloads.Workload("choice", "dense", b=4, s_q=1, h=h, seqlens=(1000,) * 4, seed=21)
+    inp = workloads.make_inputs(w)
+    q, kv = inp["q"].to(DEV), inp["kv_cache"].to(DEV)
+    bt, sl = inp["block_table"].to(DEV), inp["cache_seqlens"].to(DEV)
+    buf = binding.DecodeBuffers(4, 1, h, DEV, parts)
+    binding.mla_get_metadata(sl, 4, 1, True, 0, parts, buf.metadata)
+    binding.mla_decode(q, kv, binding.MLA_KV_BF16, bt, sl, inp["softmax_scale"], True, buf.metadata,
+                       parts, buf.workspace, buf.out, buf.lse, buf.err)
+    torch.cuda.synchronize()
+    assert int(buf.metadata[12].item()) == walked
+    ref_o, ref_l = oracle_dense(inp)
+    assert_parity(buf.out.float().cpu().numpy(), ref_o, buf.lse.cpu().numpy(), ref_l, f"h={h} parts={parts}")
+
+
 @pytest.mark.parametrize("batch", [70, 2100])  # the 128- and the 1024-thread schedule kernel
 def test_device_metadata_matches_host_mirror(batch):
     rng = np.random.default_rng(5)
