@@ -45,6 +45,24 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # --------------------------------------------------------------------- utils
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest per-rank value over all ranks (the slowest rank times the
+    job); `x` itself when there is one rank.  Uses the default process group
+    (NCCL on the GPU machine, gloo in the CPU tests)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Whole-job rate: every rank processes `units_per_rank` per step (weak
+    scaling), the step takes the slowest rank's `ms_per_step`."""
+    return units_per_rank / (ms_per_step * 1e-3) * world
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -271,11 +289,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         barrier()
         t_wall1 = time.time()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     clocks = sampler.summary(t_wall0, t_wall1)
     ms_per_step = ms_total / args.steps
 
@@ -322,11 +336,7 @@ def run_ours(args, rank, world, local_rank):
             e2e_step(k)
     x1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = x0.elapsed_time(x1) / n_e2e
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / n_e2e, world, dev)
 
     # ---- accounting
     flops_nominal = None
@@ -339,8 +349,8 @@ def run_ours(args, rank, world, local_rank):
         seqlens = sets_host[0]["cache_seqlens"].tolist()
         flops, bytes_, kv_bytes = roofline.dense_counts(seqlens, s_q, h, causal=True,
                                                         fp8=(w.kind == "fp8"))
-    tflops = flops / (ms_per_step * 1e-3) / 1e12 * world
-    kv_gbs = kv_bytes / (ms_per_step * 1e-3) / 1e9 * world
+    tflops = job_rate(flops, ms_per_step, world) / 1e12
+    kv_gbs = job_rate(kv_bytes, ms_per_step, world) / 1e9
     ai = flops / bytes_
     roof_tf = min(peaks["bf16_tflops"], peaks["hbm_gbs"] * ai / 1e3)
     split_gbs = bytes_ / (split_ms * 1e-3) / 1e9
@@ -378,7 +388,7 @@ def run_ours(args, rank, world, local_rank):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kernel_name, "kernel_ms": round(split_ms, 5),
                      "peak_source": f"{peaks.get('source')} (MEASURED_PEAKS.json burst copy)"},
-        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 3), "unit": UNIT,
+        "e2e": {"value": round(job_rate(flops, e2e_ms, world) / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
                 "note": "all call inputs (" + ", ".join(in_keys) + ") copied from pinned "
