@@ -218,6 +218,17 @@ int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv, const
                               void* metadata, int num_sm_parts, void* workspace, void* out,
                               float* lse, uint32_t* err, cudaStream_t stream);
 
+/*
+ * Failure-path check (no counterpart on the pages): launches one thread that
+ * waits on a shared-memory barrier nothing ever completes, through the same
+ * bounded wait every kernel of this library uses.  The wait gives up after
+ * its limit (2 s), ORs MLA_DEVERR_TIMEOUT into *err (device memory) and the
+ * kernel exits normally, so the context stays usable; no GPU fault, trap or
+ * hang is involved.  Asynchronous on `stream`; returns MLA_ERR_NULL for a
+ * NULL err, MLA_ERR_CUDA if the launch fails.
+ */
+int mla_check_wait_timeout(uint32_t* err, cudaStream_t stream);
+
 /* Size of the device scratch array that mla_decode_noalloc uses (40 MiB). */
 #define MLA_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
 

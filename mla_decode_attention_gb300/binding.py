@@ -54,6 +54,7 @@ _SIGS = {
     "mla_sparse_decode_splitkv": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _i, _vp, _vp, _vp,
                                _vp, _vp]),
     "mla_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "mla_check_wait_timeout": (_i, [_vp, _vp]),
 }
 
 _lib = None
@@ -263,6 +264,13 @@ def mla_combine(metadata: torch.Tensor, batch: int, s_q: int, h_q: int, num_sm_p
     _check("mla_combine",
            lib().mla_combine(_ptr(metadata), batch, s_q, h_q, num_sm_parts, _ptr(workspace),
                              _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def mla_check_wait_timeout(err: torch.Tensor, stream=None) -> None:
+    """Runs the library's bounded wait on a barrier nothing completes; the
+    kernel ORs MLA_DEVERR_TIMEOUT into err (uint32 device word) after ~2 s."""
+    _dev(err, torch.int32, "err")
+    _check("mla_check_wait_timeout", lib().mla_check_wait_timeout(_ptr(err), _stream(stream)))
 
 
 # ---------------------------------------------------------------- convenience

@@ -160,6 +160,20 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   }
 }
 
+// One thread waits on an mbarrier that nothing arrives on: the decode
+// kernels' bounded wait gives up after its limit, flags MLA_DEVERR_TIMEOUT and
+// returns, and the block exits normally.
+__global__ void wait_timeout_kernel(uint32_t* err) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+    (void)mbar_wait(smem_u32(&bar), 0, &abort_flag, err);
+  }
+}
+
 }  // namespace
 
 namespace {
@@ -202,6 +216,13 @@ extern "C" const char* mla_status_string(int status) {
 }
 
 extern "C" const char* mla_last_error(void) { return g_last_error; }
+
+extern "C" int mla_check_wait_timeout(uint32_t* err, cudaStream_t stream) {
+  if (!err) return MLA_ERR_NULL;
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(err);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MLA_OK : record_cuda_error("wait-timeout check launch", e);
+}
 
 extern "C" int mla_num_sm_parts(int device, int h_q, int* num_sm_parts) {
   if (!num_sm_parts) return MLA_ERR_NULL;

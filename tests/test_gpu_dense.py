@@ -209,3 +209,21 @@ def test_full_size_spec_decode_sampled_rows():
         assert_parity(res["out"][b, j], ref_o[b, j], res["lse"][b, :, j], ref_l[b, :, j],
                       f"spec row {b},{j}")
     assert res["err"] == 0 and np.all(np.isfinite(res["out"]))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait on a barrier nothing completes gives up (MLA_DEVERR_TIMEOUT) and
+    the kernel exits normally; a decode right after it is still correct."""
+    import time
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t0 = time.time()
+    binding.mla_check_wait_timeout(err)
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    assert int(err.item()) == binding.MLA_DEVERR_TIMEOUT
+    assert 1.5 < dt < 30.0
+    inp = workloads.make_inputs(workloads.WORKLOADS["tiny"])
+    res = run_dense(inp)
+    ref_o, ref_l = oracle_dense(inp)
+    assert_parity(res["out"], ref_o, res["lse"], ref_l, "after timeout check")
+    assert res["err"] == 0
