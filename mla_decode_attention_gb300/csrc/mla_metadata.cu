@@ -1,5 +1,6 @@
 // Tile-schedule metadata (device kernel and host mirror) and small host
 // entry points of the C ABI.
+#include <algorithm>
 #include <cstdio>
 #include <vector>
 
@@ -60,18 +61,23 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   // grid to complete before it reads the schedule
   pdl_launch_dependents();
   const int n_seq = batch * s_q;
+  // sequences are walked in group-major order k (schedule_groups)
+  const int groups = schedule_groups(s_q, num_parts);
+  const int n_g = n_seq / groups, parts_g = num_parts / groups;
   const int chunk = (n_seq + kMetaThreads - 1) / kMetaThreads;
-  const int q0 = threadIdx.x * chunk;
-  const int q1 = min(n_seq, q0 + chunk);
+  const int k0 = threadIdx.x * chunk;
+  const int k1 = min(n_seq, k0 + chunk);
 
   __shared__ int32_t s_max_cost;
+  __shared__ int64_t s_group_start[kMaxSq + 1];
   if (threadIdx.x == 0) s_max_cost = 0;
   __syncthreads();
 
   // 1. tiles, keys and cost per sequence; chunk-local cost prefix.
   int64_t local = 0;
   int32_t local_max = 0, local_nonempty = 0;
-  for (int q = q0; q < q1; ++q) {
+  for (int k = k0; k < k1; ++k) {
+    const int q = order_to_q(k, n_g, groups);
     const int32_t keys = seq_keys(seqlens, q / s_q, q % s_q, s_q, causal, topk);
     const int32_t nt = tiles_of(keys);
     int32_t* s = meta_seq(meta, num_parts, q);
@@ -88,20 +94,30 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   const int64_t base = packed_base >> kCountBits, total = packed_total >> kCountBits;
   const int64_t b_base = packed_base & ((int64_t{1} << kCountBits) - 1);
   const int64_t b_splits = packed_total & ((int64_t{1} << kCountBits) - 1);
-  for (int q = q0; q < q1; ++q) {
+  // where each group starts on the group-major cost line
+  for (int k = k0; k < k1; ++k)
+    if (k % n_g == 0)
+      s_group_start[k / n_g] = base + meta_seq(meta, num_parts, order_to_q(k, n_g, groups))[kSCostPrefix];
+  if (threadIdx.x == 0) s_group_start[groups] = total;
+  __syncthreads();
+  // prefixes within each group's own cost line
+  for (int k = k0; k < k1; ++k) {
+    const int q = order_to_q(k, n_g, groups);
     int32_t* sq = meta_seq(meta, num_parts, q);
-    sq[kSCostPrefix] += static_cast<int32_t>(base);
+    sq[kSCostPrefix] = static_cast<int32_t>(base + sq[kSCostPrefix] - s_group_start[k / n_g]);
     if (n_seq <= kSmemPrefixes) s_prefix[q] = sq[kSCostPrefix];
   }
+  int64_t max_group_total = 0;
+  for (int j = 0; j < groups; ++j) max_group_total = max(max_group_total, s_group_start[j + 1] - s_group_start[j]);
   __syncthreads();
   __threadfence_block();
 
-  const int64_t per_part = total > 0 ? (total + num_parts - 1) / num_parts : 1;
+  const int64_t per_part = max_group_total > 0 ? (max_group_total + parts_g - 1) / parts_g : 1;
 
   // 2. split counts per sequence (from the prefixes only).
   int64_t nsplit_local = 0;
-  for (int q = q0; q < q1; ++q) {
-    int32_t* s = meta_seq(meta, num_parts, q);
+  for (int k = k0; k < k1; ++k) {
+    int32_t* s = meta_seq(meta, num_parts, order_to_q(k, n_g, groups));
     const int32_t nt = s[kSTiles];
     const int32_t ns = nt > 0 ? 1 + inner_boundaries(s[kSCostPrefix], nt, per_part) : 0;
     s[kSNSplits] = ns;
@@ -110,21 +126,24 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   int64_t split_base;
   const int64_t total_splits = block_exclusive_scan<kMetaThreads>(nsplit_local, &split_base, warp_sums);
   int64_t run = split_base;
-  for (int q = q0; q < q1; ++q) {
-    int32_t* s = meta_seq(meta, num_parts, q);
+  for (int k = k0; k < k1; ++k) {
+    int32_t* s = meta_seq(meta, num_parts, order_to_q(k, n_g, groups));
     s[kSSplitOff] = static_cast<int32_t>(run);
     run += s[kSNSplits];
   }
   __syncthreads();
 
-  // 3. part ranges.
+  // 3. part ranges: part p is part p % parts_g of group p / parts_g
   // (the binary searches read the prefixes from shared memory when they fit)
-  if (n_seq <= kSmemPrefixes) {
-    for (int p = threadIdx.x; p < num_parts; p += kMetaThreads)
-      fill_part(meta, num_parts, ArrayPrefix{s_prefix}, n_seq, total, per_part, p);
-  } else {
-    for (int p = threadIdx.x; p < num_parts; p += kMetaThreads)
-      fill_part(meta, num_parts, MetaPrefix{meta, num_parts}, n_seq, total, per_part, p);
+  for (int p = threadIdx.x; p < num_parts; p += kMetaThreads) {
+    const int j = p / parts_g;
+    const int64_t total_j = s_group_start[j + 1] - s_group_start[j];
+    if (n_seq <= kSmemPrefixes)
+      fill_part(meta, GroupPrefix<ArrayPrefix>{ArrayPrefix{s_prefix}, j, groups}, n_g, total_j, per_part, p,
+                p % parts_g, j, groups);
+    else
+      fill_part(meta, GroupPrefix<MetaPrefix>{MetaPrefix{meta, num_parts}, j, groups}, n_g, total_j, per_part,
+                p, p % parts_g, j, groups);
   }
 
   // 4. schedule B (one whole sequence per part), when every sequence has a part.
@@ -132,7 +151,8 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   int32_t* mb = meta + meta_words(n_seq, num_parts);
   if (has_b) {
     int64_t run_b = b_base;
-    for (int q = q0; q < q1; ++q) {
+    for (int k = k0; k < k1; ++k) {
+      const int q = order_to_q(k, n_g, groups);
       const int32_t* sa = meta_seq(meta, num_parts, q);
       int32_t* sb = meta_seq(mb, num_parts, q);
       const int32_t nt = sa[kSTiles];
@@ -151,11 +171,14 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
     meta[kHTotalSplits] = static_cast<int32_t>(total_splits);
     meta[kHPerPart] = static_cast<int32_t>(per_part);
     meta[kHMaxCost] = max_cost;
-    for (int i = kHMaxCost + 1; i < kHeaderWords; ++i) meta[i] = 0;
+    meta[kHChosen] = 0;
+    meta[kHGroups] = groups;
+    for (int i = kHGroups + 1; i < kHeaderWords; ++i) meta[i] = 0;
     for (int i = 0; i < kHeaderWords; ++i) mb[i] = has_b ? meta[i] : 0;
     if (has_b) {
       mb[kHTotalSplits] = static_cast<int32_t>(b_splits);
       mb[kHPerPart] = max_cost;
+      mb[kHGroups] = 1;
     }
   }
 }
@@ -281,42 +304,54 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
   if (rc != MLA_OK) return rc;
   int32_t* meta = static_cast<int32_t*>(metadata_host);
   const int n_seq = batch * s_q;
-  int64_t total = 0;
+  const int groups = schedule_groups(s_q, num_sm_parts);
+  const int n_g = n_seq / groups, parts_g = num_sm_parts / groups;
+  // cost prefixes within each group, sequences in group-major order k
+  std::vector<int64_t> group_total(groups, 0);
   int32_t max_cost = 0;
-  for (int q = 0; q < n_seq; ++q) {
+  for (int k = 0; k < n_seq; ++k) {
+    const int q = order_to_q(k, n_g, groups), j = k / n_g;
     const int32_t keys = seq_keys(seqlens, q / s_q, q % s_q, s_q, causal ? 1 : 0, topk);
     const int32_t nt = tiles_of(keys);
     int32_t* s = meta_seq(meta, num_sm_parts, q);
     s[kSTiles] = nt; s[kSKeys] = keys; s[5] = 0; s[6] = 0; s[7] = 0;
-    s[kSCostPrefix] = static_cast<int32_t>(total);
-    total += cost_of(nt);
+    s[kSCostPrefix] = static_cast<int32_t>(group_total[j]);
+    group_total[j] += cost_of(nt);
     if (cost_of(nt) > max_cost) max_cost = cost_of(nt);
   }
-  const int64_t per_part = total > 0 ? (total + num_sm_parts - 1) / num_sm_parts : 1;
+  int64_t max_group_total = 0;
+  for (int j = 0; j < groups; ++j) max_group_total = std::max(max_group_total, group_total[j]);
+  const int64_t per_part = max_group_total > 0 ? (max_group_total + parts_g - 1) / parts_g : 1;
   int64_t splits = 0;
-  for (int q = 0; q < n_seq; ++q) {
-    int32_t* s = meta_seq(meta, num_sm_parts, q);
+  for (int k = 0; k < n_seq; ++k) {
+    int32_t* s = meta_seq(meta, num_sm_parts, order_to_q(k, n_g, groups));
     const int32_t nt = s[kSTiles];
     s[kSNSplits] = nt > 0 ? 1 + inner_boundaries(s[kSCostPrefix], nt, per_part) : 0;
     s[kSSplitOff] = static_cast<int32_t>(splits);
     splits += s[kSNSplits];
   }
-  for (int p = 0; p < num_sm_parts; ++p)
-    fill_part(meta, num_sm_parts, MetaPrefix{meta, num_sm_parts}, n_seq, total, per_part, p);
+  for (int p = 0; p < num_sm_parts; ++p) {
+    const int j = p / parts_g;
+    fill_part(meta, GroupPrefix<MetaPrefix>{MetaPrefix{meta, num_sm_parts}, j, groups}, n_g, group_total[j],
+              per_part, p, p % parts_g, j, groups);
+  }
   meta[kHMagic] = kMetaMagic; meta[kHVersion] = kMetaVersion; meta[kHNSeq] = n_seq;
   meta[kHParts] = num_sm_parts; meta[kHTile] = kTileTokens; meta[kHSq] = s_q;
   meta[kHBatch] = batch; meta[kHCausal] = causal ? 1 : 0; meta[kHTopk] = topk;
   meta[kHTotalSplits] = static_cast<int32_t>(splits);
   meta[kHPerPart] = static_cast<int32_t>(per_part);
   meta[kHMaxCost] = max_cost;
-  for (int i = kHMaxCost + 1; i < kHeaderWords; ++i) meta[i] = 0;
+  meta[kHChosen] = 0;
+  meta[kHGroups] = groups;
+  for (int i = kHGroups + 1; i < kHeaderWords; ++i) meta[i] = 0;
   // schedule B (one whole sequence per part), when every sequence has a part
   const bool has_b = n_seq <= num_sm_parts;
   int32_t* mb = meta + meta_words(n_seq, num_sm_parts);
   for (int i = 0; i < kHeaderWords; ++i) mb[i] = has_b ? meta[i] : 0;
   if (has_b) {
     int64_t b_splits = 0;
-    for (int q = 0; q < n_seq; ++q) {
+    for (int k = 0; k < n_seq; ++k) {
+      const int q = order_to_q(k, n_g, groups);
       const int32_t* sa = meta_seq(meta, num_sm_parts, q);
       int32_t* sb = meta_seq(mb, num_sm_parts, q);
       const int32_t nt = sa[kSTiles];
@@ -327,6 +362,7 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
     for (int p = 0; p < num_sm_parts; ++p) fill_whole_part(mb, num_sm_parts, n_seq, p);
     mb[kHTotalSplits] = static_cast<int32_t>(b_splits);
     mb[kHPerPart] = max_cost;
+    mb[kHGroups] = 1;
   }
   return MLA_OK;
 }

@@ -6,8 +6,12 @@
 // (the Q load and the epilogue).  The metadata holds two schedules (FlashMLA
 // deep dive, "Tile Scheduler": balanced assignment of requests and blocks to
 // SMs; DeepGEMM & FlashMLA article, section 7 "split-KV"):
-//   A: the global cost line cut into num_parts equal ranges, so a sequence
-//      may be split between parts (its splits are merged by the combine);
+//   A: the cost line cut into equal ranges, so a sequence may be split
+//      between parts (its splits are merged by the combine).  With s_q > 1
+//      new tokens per request (and num_parts a multiple of s_q), token j of
+//      every request forms group j with its own cost line and num_parts / s_q
+//      parts: part p of group 0 and part p of group j walk the same requests
+//      in step, so one of them finds the other's cache rows still in L2;
 //   B: (only when n_seq <= num_parts) part p walks the whole sequence p, so
 //      nothing is split and the combine has nothing to merge.
 // A decode kernel walks B when B's longest part costs at most its own split
@@ -28,16 +32,19 @@ namespace mla {
 constexpr int kTileTokens = 128;
 constexpr int kFixedCost = 2;  // a piece switch (Q load, epilogue) costs about two tiles
 constexpr int32_t kMetaMagic = 0x4D4C4131;  // "MLA1"
-constexpr int32_t kMetaVersion = 1;
+constexpr int32_t kMetaVersion = 2;
 
 // header words (kHMaxCost: the largest single-sequence cost; kHChosen, in
 // schedule A's header only: the schedule the last decode kernel walked,
-// 0 = A, 1 = B, written by that kernel for the combine)
+// 0 = A, 1 = B, written by that kernel for the combine; kHGroups: the number
+// of groups of schedule A, 1 or s_q)
 enum : int {
   kHMagic = 0, kHVersion, kHNSeq, kHParts, kHTile, kHSq, kHBatch, kHCausal, kHTopk,
-  kHTotalSplits, kHPerPart, kHMaxCost, kHChosen, kHeaderWords = 16
+  kHTotalSplits, kHPerPart, kHMaxCost, kHChosen, kHGroups, kHeaderWords = 16
 };
-constexpr int kPartWords = 8;  // q_begin, t_begin, q_end, t_end, split_begin, 0, 0, 0
+// q_begin, t_begin, q_end, t_end, split_begin, q_step, 0, 0: the part walks
+// sequences q_begin, q_begin + q_step, ... (q_step = the number of groups)
+constexpr int kPartWords = 8;
 constexpr int kSeqWords = 8;   // n_tiles, split_offset, n_splits, keys, cost_prefix, 0, 0, 0
 enum : int { kSTiles = 0, kSSplitOff, kSNSplits, kSKeys, kSCostPrefix };
 
@@ -119,21 +126,40 @@ MLA_HD int32_t inner_boundaries(int64_t prefix, int32_t n_tiles, int64_t per_par
   return static_cast<int32_t>(floordiv(hi - 1, per_part) - floordiv(lo - 1, per_part));
 }
 
-// Fills part p's record from the per-sequence cost prefixes.
+// Groups of schedule A: s_q (one per new-token index j) when s_q > 1 and the
+// parts divide evenly, else 1.  Group j's members are the sequences
+// q = j + groups * m, m = 0 .. n_seq / groups - 1, in that order; the
+// metadata builders walk all sequences in group-major order k = j * n_g + m.
+MLA_HD int schedule_groups(int s_q, int num_parts) {
+  return (s_q > 1 && num_parts % s_q == 0) ? s_q : 1;
+}
+MLA_HD int order_to_q(int k, int n_g, int groups) { return (k % n_g) * groups + k / n_g; }
+
+// Cost prefix of member m of group j, from a per-sequence prefix functor.
 template <class Prefix>
-MLA_HD void fill_part(int32_t* meta, int num_parts, const Prefix& prefix, int n_seq, int64_t total,
-                      int64_t per_part, int p) {
-  int qb, tb, qe, te;
-  const int64_t xb = static_cast<int64_t>(p) * per_part;
+struct GroupPrefix {
+  Prefix prefix;
+  int j, groups;
+  MLA_HD int32_t operator()(int m) const { return prefix(j + groups * m); }
+};
+
+// Fills the record of part p (the p_local-th part of group j, whose members
+// have cost prefixes `prefix` within the group's cost line of length total).
+template <class Prefix>
+MLA_HD void fill_part(int32_t* meta, const Prefix& prefix, int n_members, int64_t total, int64_t per_part,
+                      int p, int p_local, int j, int groups) {
+  int mb, tb, me, te;
+  const int64_t xb = static_cast<int64_t>(p_local) * per_part;
   int64_t xe = xb + per_part;
   if (xe > total) xe = total;
-  cost_position(prefix, n_seq, total, xb, &qb, &tb);
-  cost_position(prefix, n_seq, total, xe, &qe, &te);
+  cost_position(prefix, n_members, total, xb, &mb, &tb);
+  cost_position(prefix, n_members, total, xe, &me, &te);
   int32_t split_begin = 0;
-  if (qb < n_seq && tb > 0) split_begin = static_cast<int32_t>(p - floordiv(prefix(qb) + kFixedCost, per_part));
+  if (mb < n_members && tb > 0)
+    split_begin = static_cast<int32_t>(p_local - floordiv(prefix(mb) + kFixedCost, per_part));
   int32_t* r = meta_part(meta, p);
-  r[0] = qb; r[1] = tb; r[2] = qe; r[3] = te; r[4] = split_begin;
-  r[5] = 0; r[6] = 0; r[7] = 0;
+  r[0] = j + groups * mb; r[1] = tb; r[2] = j + groups * me; r[3] = te; r[4] = split_begin;
+  r[5] = groups; r[6] = 0; r[7] = 0;
 }
 
 // Schedule B of a metadata buffer (its magic is 0 when it does not exist).
@@ -157,18 +183,18 @@ MLA_HD void fill_whole_part(int32_t* meta_b, int num_parts, int n_seq, int p) {
   int32_t* r = meta_part(meta_b, p);
   const int q = p < n_seq ? p : n_seq;
   r[0] = q; r[1] = 0; r[2] = p < n_seq ? p + 1 : n_seq; r[3] = 0; r[4] = 0;
-  r[5] = 0; r[6] = 0; r[7] = 0;
+  r[5] = 1; r[6] = 0; r[7] = 0;
 }
 
 // The work a part walks: pieces (q, [t0, t1), split index) in order.
 struct PartCursor {
-  int q, t, q_end, t_end, split;
+  int q, t, q_end, t_end, split, step;
 };
 
 MLA_HD PartCursor part_cursor(const int32_t* meta, int p) {
   const int32_t* r = meta_part(meta, p);
   PartCursor c;
-  c.q = r[0]; c.t = r[1]; c.q_end = r[2]; c.t_end = r[3]; c.split = r[4];
+  c.q = r[0]; c.t = r[1]; c.q_end = r[2]; c.t_end = r[3]; c.split = r[4]; c.step = r[5];
   return c;
 }
 
@@ -180,10 +206,10 @@ MLA_HD bool next_piece(const int32_t* meta, int num_parts, PartCursor* c, int* q
     const int stop = (c->q == c->q_end) ? c->t_end : n_tiles;
     if (n_tiles > 0 && c->t < stop) {
       *q = c->q; *t0 = c->t; *t1 = stop; *split = c->split;
-      c->q += 1; c->t = 0; c->split = 0;
+      c->q += c->step; c->t = 0; c->split = 0;
       return true;
     }
-    c->q += 1; c->t = 0; c->split = 0;
+    c->q += c->step; c->t = 0; c->split = 0;
   }
   return false;
 }

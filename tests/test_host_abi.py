@@ -99,15 +99,17 @@ def parse_meta(m, n_seq, parts):
 
 
 def walk_part(prt_row, seq):
-    """Pieces (q, t0, t1, split) a part processes, as the kernels walk them."""
-    q, t, qe, te, split = [int(x) for x in prt_row[:5]]
+    """Pieces (q, t0, t1, split) a part processes, as the kernels walk them
+    (sequences q_begin, q_begin + q_step, ...)."""
+    q, t, qe, te, split, step = [int(x) for x in prt_row[:6]]
+    assert step >= 1
     pieces = []
     while q < qe or (q == qe and t < te):
         nt = int(seq[q, 0])
         stop = te if q == qe else nt
         if nt > 0 and t < stop:
             pieces.append((q, t, stop, split))
-        q, t, split = q + 1, 0, 0
+        q, t, split = q + step, 0, 0
     return pieces
 
 
@@ -155,14 +157,26 @@ def check_schedule(seqlens, s_q, causal, topk, parts):
             assert seq[q, 2] == splits[-1] + 1
         else:
             assert seq[q, 2] == 0
-    offs = np.concatenate([[0], np.cumsum(seq[:, 2])[:-1]])
-    assert np.array_equal(seq[:, 1], offs)
+    order = walk_order(hdr)
+    offs = np.zeros(b * s_q, np.int64)
+    offs[order] = np.concatenate([[0], np.cumsum(seq[order, 2])[:-1]])
+    assert np.array_equal(seq[:, 1], offs)   # split offsets in the builders' walk order
     assert hdr[9] == seq[:, 2].sum() <= b * s_q + parts
+    groups = int(hdr[13])
+    assert groups == (s_q if s_q > 1 and parts % s_q == 0 else 1)
     assert max(per_part_cost) <= hdr[10] + FIXED_COST
     costs = [int(nt) + FIXED_COST if nt > 0 else 0 for nt in seq[:, 0]]
     assert hdr[11] == max(costs) and hdr[12] == 0
     check_whole_sequence_schedule(m, b * s_q, parts, hdr, seq)
     return m
+
+
+def walk_order(hdr):
+    """Sequences in the builders' order: group-major (all first new tokens,
+    then all second ones, ...) when schedule A has one group per token."""
+    n_seq, groups = int(hdr[2]), int(hdr[13])
+    n_g = n_seq // groups
+    return np.array([(k % n_g) * groups + k // n_g for k in range(n_seq)], np.int64)
 
 
 def check_whole_sequence_schedule(m, n_seq, parts, hdr_a, seq_a):
@@ -176,7 +190,10 @@ def check_whole_sequence_schedule(m, n_seq, parts, hdr_a, seq_a):
     assert np.array_equal(hdr[:9], hdr_a[:9]) and hdr[10] == hdr[11] == hdr_a[11]
     assert np.array_equal(seq[:, [0, 3, 4]], seq_a[:, [0, 3, 4]])
     assert np.array_equal(seq[:, 2], (seq[:, 0] > 0).astype(np.int32))
-    assert np.array_equal(seq[:, 1], np.concatenate([[0], np.cumsum(seq[:, 2])[:-1]]))
+    order = walk_order(hdr_a)
+    offs = np.zeros(n_seq, np.int64)
+    offs[order] = np.concatenate([[0], np.cumsum(seq[order, 2])[:-1]])
+    assert np.array_equal(seq[:, 1], offs)
     assert hdr[9] == seq[:, 2].sum()
     for p in range(parts):
         pieces = walk_part(prt[p], seq)
@@ -207,6 +224,22 @@ def test_schedule_spec_invariants(s_q, causal):
     seqlens = rng.integers(0, 20000, size=19).astype(np.int32)
     seqlens[0] = 1   # causal: token 0 of this request sees nothing
     check_schedule(seqlens, s_q, causal, 0, 76)
+
+
+def test_spec_schedule_walks_both_new_tokens_in_step():
+    """s_q = 2 over 76 parts: group j = token j of every request, 38 parts
+    each; part p and part p + 38 walk the same requests and tiles (token 0
+    and token 1), so the second reader of a cache row finds it in L2."""
+    rng = np.random.default_rng(9)
+    seqlens = rng.integers(1024, 16385, size=128).astype(np.int32)
+    m = check_schedule(seqlens, 2, False, 0, 76)   # non-causal: both tokens see L keys
+    hdr, prt, seq = parse_meta(m, 256, 76)
+    assert hdr[13] == 2
+    for p in range(38):
+        a = walk_part(prt[p], seq)
+        b = walk_part(prt[p + 38], seq)
+        assert [(q // 2, t0, t1) for q, t0, t1, _ in a] == [(q // 2, t0, t1) for q, t0, t1, _ in b]
+        assert all(q % 2 == 0 for q, *_ in a) and all(q % 2 == 1 for q, *_ in b)
 
 
 def test_schedule_sparse_invariants():
