@@ -105,7 +105,11 @@ int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes);
  * of W = 16 + 8 * parts + 8 * n_seq words each:
  *   A (words [0, W)): the tiles dealt out as contiguous ranges of balanced
  *     cost (tiles + 2 per sequence piece) to the parts; a sequence cut
- *     between parts becomes several splits that the combine step merges;
+ *     between parts becomes several splits that the combine step merges.
+ *     With s_q > 1 and num_sm_parts a multiple of s_q, new token j of every
+ *     request forms group j with its own cost line and num_sm_parts / s_q
+ *     parts (parts [j * P/s_q, (j+1) * P/s_q)), so that the parts of the
+ *     groups walk the same requests' keys at the same time;
  *   B (words [W, 2W)): present when n_seq <= num_sm_parts (else its magic is
  *     0 and the rest is not written): part p walks the whole sequence p, no
  *     sequence is split.
@@ -113,18 +117,20 @@ int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes);
  * kernel-specific split penalty (4 to 11 tiles) above A's balanced cost:
  * every extra piece costs a Q load and an epilogue, every split row a
  * combine read.  Layout of one schedule (int32):
- *   [0,16)                    header: magic 0x4D4C4131, version, n_seq,
+ *   [0,16)                    header: magic 0x4D4C4131, version (2), n_seq,
  *                             num_sm_parts, tile_tokens (128), s_q, batch,
  *                             causal, topk, total_splits, cost_per_part,
- *                             largest sequence cost, chosen, 0...
+ *                             largest sequence cost, chosen, groups, 0...
  *                             (chosen, in A only: 0 or 1 = the schedule the
  *                             last decode call walked; the decode kernels
  *                             write it and the combine reads it)
  *   [16, 16 + 8 * parts)      per part: q_begin, t_begin, q_end, t_end,
- *                             split_begin, 0, 0, 0 (half-open range of
- *                             (sequence, tile) pairs in lexicographic order)
+ *                             split_begin, q_step, 0, 0 (half-open range of
+ *                             (sequence, tile) pairs, sequences q_begin,
+ *                             q_begin + q_step, ..., q_step = groups)
  *   [.., + 8 * n_seq)         per sequence: n_tiles, split_offset, n_splits,
- *                             key count, cost prefix, 0, 0, 0
+ *                             key count, cost prefix (within its group),
+ *                             0, 0, 0
  * metadata: device buffer of mla_metadata_size() bytes, 16-byte aligned.
  */
 int mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int causal, int topk,
