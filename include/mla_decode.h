@@ -100,7 +100,9 @@ int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes);
  * Each (request b, new token j) is one sequence whose key count is
  *   dense, causal:      max(0, cache_seqlens[b] - s_q + 1 + j)
  *   dense, non-causal:  cache_seqlens[b]
- *   sparse (topk > 0):  topk   (cache_seqlens ignored, may be NULL)
+ *   sparse (topk > 0):  topk, or min(topk, max(0, cache_seqlens[b * s_q + j]))
+ *                       when cache_seqlens is given (it is then topk_length,
+ *                       one int32 per query token; may be NULL)
  * Sequences are cut into 128-key tiles.  The metadata holds two schedules
  * of W = 16 + 8 * parts + 8 * n_seq words each:
  *   A (words [0, W)): the tiles dealt out as contiguous ranges of balanced
@@ -204,14 +206,22 @@ int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_format, int64
  *  indices  [batch, s_q, topk] int32; -1 marks an invalid slot.  Any other
  *           value outside [0, s_kv) is also skipped and sets
  *           MLA_DEVERR_BAD_INDEX (FlashMLA itself does no bound check).
- *  metadata from mla_get_metadata(NULL, batch, s_q, 0, topk, num_sm_parts, ...)
+ *  attn_sink optional [h_q] fp32 device array (NULL = none; FlashMLA sparse
+ *           interface, "attn_sink"): every output row of head h is scaled
+ *           by exp(lse) / (exp(lse) + exp(attn_sink[h])); lse itself is
+ *           returned unchanged.
+ *  metadata from mla_get_metadata(topk_length, batch, s_q, 0, topk,
+ *           num_sm_parts, ...).  topk_length (FlashMLA sparse interface,
+ *           "topk_length") is NULL, or an int32 device array [batch * s_q]:
+ *           query token (b, j) then attends only to its first
+ *           topk_length[b * s_q + j] index slots (clamped to [0, topk]).
  *  Other arguments as for mla_decode.  Invariant to the order of indices up
  *  to floating-point rounding.
  */
 int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv, const int32_t* indices,
                       int topk, int batch, int s_q, int h_q, float softmax_scale,
-                      void* metadata, int num_sm_parts, void* workspace, void* out,
-                      float* lse, uint32_t* err, cudaStream_t stream);
+                      const float* attn_sink, void* metadata, int num_sm_parts, void* workspace,
+                      void* out, float* lse, uint32_t* err, cudaStream_t stream);
 
 /*
  * The split-KV kernel of mla_sparse_decode alone (the sparse counterpart of
@@ -221,8 +231,9 @@ int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv, const int32_t
  */
 int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv, const int32_t* indices,
                               int topk, int batch, int s_q, int h_q, float softmax_scale,
-                              void* metadata, int num_sm_parts, void* workspace, void* out,
-                              float* lse, uint32_t* err, cudaStream_t stream);
+                              const float* attn_sink, void* metadata, int num_sm_parts,
+                              void* workspace, void* out, float* lse, uint32_t* err,
+                              cudaStream_t stream);
 
 /*
  * Failure-path check (no counterpart on the pages): launches one thread that
@@ -278,9 +289,11 @@ int mla_decode_noalloc(const void* q, const void* kv_cache, int kv_format, int64
  * mla_sparse_decode launch it themselves; it is exported for callers that
  * run the split kernels through their own graph.  Writes out/lse for every
  * sequence with two or more splits, and zeros / -inf for empty sequences.
+ * attn_sink: as for mla_sparse_decode (NULL for dense decode).
  */
 int mla_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm_parts,
-                const void* workspace, void* out, float* lse, cudaStream_t stream);
+                const void* workspace, const float* attn_sink, void* out, float* lse,
+                cudaStream_t stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

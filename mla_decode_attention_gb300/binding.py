@@ -49,11 +49,11 @@ _SIGS = {
                                 _vp, _vp, _vp, _vp, _vp]),
     "mla_decode_noalloc": (_i, [_vp, _vp, _i, _i64, _vp, _i64, _vp, _i, _i, _i, _f, _i, _vp, _vp,
                                 _vp, _vp]),
-    "mla_sparse_decode": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _i, _vp, _vp, _vp,
-                               _vp, _vp]),
-    "mla_sparse_decode_splitkv": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _i, _vp, _vp, _vp,
-                               _vp, _vp]),
-    "mla_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "mla_sparse_decode": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _vp, _i, _vp, _vp,
+                               _vp, _vp, _vp]),
+    "mla_sparse_decode_splitkv": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _vp, _i, _vp,
+                                       _vp, _vp, _vp, _vp]),
+    "mla_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "mla_check_wait_timeout": (_i, [_vp, _vp]),
 }
 
@@ -226,8 +226,13 @@ def mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, kv_format: int,
 def _sparse_call(name, q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,
                  softmax_scale: float, metadata: torch.Tensor, num_sm_parts: int,
                  workspace: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
-                 err: Optional[torch.Tensor] = None, stream=None) -> None:
+                 err: Optional[torch.Tensor] = None, stream=None,
+                 attn_sink: Optional[torch.Tensor] = None) -> None:
     _dev(q, torch.bfloat16, "q")
+    if attn_sink is not None:
+        _dev(attn_sink, torch.float32, "attn_sink")
+        if attn_sink.numel() != q.shape[2]:
+            raise ValueError("attn_sink must hold one value per query head")
     _dev(kv, torch.bfloat16, "kv")
     _dev(indices, torch.int32, "indices")
     _dev(metadata, torch.int32, "metadata")
@@ -239,31 +244,35 @@ def _sparse_call(name, q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,
     topk = indices.shape[-1]
     _check(name,
            getattr(lib(), name)(_ptr(q), _ptr(kv), kv.shape[0], _ptr(indices), topk, b, s_q,
-                                h, float(softmax_scale), _ptr(metadata), num_sm_parts,
+                                h, float(softmax_scale), _ptr(attn_sink), _ptr(metadata), num_sm_parts,
                                 _ptr(workspace), _ptr(out), _ptr(lse), _ptr(err),
                                 _stream(stream)))
 
 
 def mla_sparse_decode(q, kv, indices, softmax_scale, metadata, num_sm_parts, workspace, out, lse,
-                      err=None, stream=None) -> None:
-    """q [b, s_q, h, 576] bf16; kv [s_kv, 576] bf16; indices [b, s_q, topk] int32."""
+                      err=None, stream=None, attn_sink=None) -> None:
+    """q [b, s_q, h, 576] bf16; kv [s_kv, 576] bf16; indices [b, s_q, topk] int32;
+    attn_sink optional [h] float32.  A per-token topk_length goes to
+    mla_get_metadata in place of cache_seqlens."""
     _sparse_call("mla_sparse_decode", q, kv, indices, softmax_scale, metadata, num_sm_parts,
-                 workspace, out, lse, err, stream)
+                 workspace, out, lse, err, stream, attn_sink)
 
 
 def mla_sparse_decode_splitkv(q, kv, indices, softmax_scale, metadata, num_sm_parts, workspace,
-                              out, lse, err=None, stream=None) -> None:
+                              out, lse, err=None, stream=None, attn_sink=None) -> None:
     """The split kernel of mla_sparse_decode alone (partials need mla_combine)."""
     _sparse_call("mla_sparse_decode_splitkv", q, kv, indices, softmax_scale, metadata,
-                 num_sm_parts, workspace, out, lse, err, stream)
+                 num_sm_parts, workspace, out, lse, err, stream, attn_sink)
 
 
 def mla_combine(metadata: torch.Tensor, batch: int, s_q: int, h_q: int, num_sm_parts: int,
                 workspace: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
-                stream=None) -> None:
+                stream=None, attn_sink: Optional[torch.Tensor] = None) -> None:
+    if attn_sink is not None:
+        _dev(attn_sink, torch.float32, "attn_sink")
     _check("mla_combine",
            lib().mla_combine(_ptr(metadata), batch, s_q, h_q, num_sm_parts, _ptr(workspace),
-                             _ptr(out), _ptr(lse), _stream(stream)))
+                             _ptr(attn_sink), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def mla_check_wait_timeout(err: torch.Tensor, stream=None) -> None:

@@ -20,9 +20,11 @@ constexpr int kCombineThreads = 32 * kCombineWarps;
 // as 2 KB contiguous per warp, and the bf16 row is written as 1 KB contiguous.
 // At most 64 registers per thread: four CTAs (32 warps) per SM, so that one
 // or two waves cover the rows of a typical batch.
+// attn_sink (optional, [h]): the merged row is scaled by e^lse / (e^lse + e^sink).
 __global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(
     const int32_t* __restrict__ meta, int h, int s_q, int num_parts, const float* __restrict__ ws_o,
-    const float* __restrict__ ws_lse, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+    const float* __restrict__ ws_lse, const float* __restrict__ attn_sink, __nv_bfloat16* __restrict__ out,
+    float* __restrict__ lse) {
   const int q = blockIdx.x;
   const int head = blockIdx.y * kCombineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -65,7 +67,8 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(
 #pragma unroll
   for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
   const float total_lse = sum > 0.f ? ref + __logf(sum) : -INFINITY;
-  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  float inv = sum > 0.f ? 1.f / sum : 0.f;
+  if (attn_sink) inv *= attn_sink_factor(total_lse, attn_sink[head]);
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
@@ -97,7 +100,8 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(
 }  // namespace
 
 int launch_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm_parts,
-                   const void* workspace, void* out, float* lse, cudaStream_t stream, bool pdl) {
+                   const void* workspace, const float* attn_sink, void* out, float* lse,
+                   cudaStream_t stream, bool pdl) {
   const int64_t rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
   const float* ws_o = static_cast<const float*>(workspace);
   const float* ws_lse = ws_o + rows * kDv;
@@ -112,7 +116,7 @@ int launch_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const int32_t*>(metadata),
-                                           h_q, s_q, num_sm_parts, ws_o, ws_lse,
+                                           h_q, s_q, num_sm_parts, ws_o, ws_lse, attn_sink,
                                            static_cast<__nv_bfloat16*>(out), lse);
   return e == cudaSuccess ? MLA_OK : record_cuda_error("combine kernel launch", e);
 }
@@ -120,12 +124,13 @@ int launch_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm
 }  // namespace mla
 
 extern "C" int mla_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm_parts,
-                           const void* workspace, void* out, float* lse, cudaStream_t stream) {
+                           const void* workspace, const float* attn_sink, void* out, float* lse,
+                           cudaStream_t stream) {
   const int rc = mla::check_common(batch, s_q, h_q, num_sm_parts);
   if (rc != MLA_OK) return rc;
   if (!metadata || !workspace || !out || !lse) return MLA_ERR_NULL;
   if (!mla::aligned16(metadata) || !mla::aligned16(workspace) || !mla::aligned16(out))
     return MLA_ERR_ALIGN;
-  return mla::launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, out, lse, stream,
-                             false);
+  return mla::launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, attn_sink, out, lse,
+                             stream, false);
 }

@@ -234,14 +234,15 @@ extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, in
                                     softmax_scale, causal, metadata, num_sm_parts, workspace, out,
                                     lse, err, stream);
   if (rc != MLA_OK) return rc;
-  return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, out, lse, stream, true);
+  return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, nullptr, out, lse, stream,
+                        true);
 }
 
 extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv,
                                          const int32_t* indices, int topk, int batch, int s_q,
-                                         int h_q, float softmax_scale, void* metadata,
-                                         int num_sm_parts, void* workspace, void* out, float* lse,
-                                         uint32_t* err, cudaStream_t stream) {
+                                         int h_q, float softmax_scale, const float* attn_sink,
+                                         void* metadata, int num_sm_parts, void* workspace, void* out,
+                                         float* lse, uint32_t* err, cudaStream_t stream) {
   int rc = check_common(batch, s_q, h_q, num_sm_parts);
   if (rc != MLA_OK) return rc;
   if (!q || !kv || !indices || !metadata || !workspace || !out || !lse) return MLA_ERR_NULL;
@@ -263,6 +264,7 @@ extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t 
   SplitParams prm = {};
   prm.meta = static_cast<int32_t*>(metadata);
   prm.indices = indices;
+  prm.attn_sink = attn_sink;
   prm.topk = topk;
   prm.s_kv = s_kv;
   prm.kv_rows = static_cast<const __nv_bfloat16*>(kv);
@@ -286,12 +288,13 @@ extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t 
 
 extern "C" int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv,
                                  const int32_t* indices, int topk, int batch, int s_q, int h_q,
-                                 float softmax_scale, void* metadata, int num_sm_parts,
-                                 void* workspace, void* out, float* lse, uint32_t* err,
-                                 cudaStream_t stream) {
+                                 float softmax_scale, const float* attn_sink, void* metadata,
+                                 int num_sm_parts, void* workspace, void* out, float* lse,
+                                 uint32_t* err, cudaStream_t stream) {
   const int rc = mla_sparse_decode_splitkv(q, kv, s_kv, indices, topk, batch, s_q, h_q,
-                                           softmax_scale, metadata, num_sm_parts, workspace, out,
-                                           lse, err, stream);
+                                           softmax_scale, attn_sink, metadata, num_sm_parts,
+                                           workspace, out, lse, err, stream);
   if (rc != MLA_OK) return rc;
-  return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, out, lse, stream, true);
+  return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, attn_sink, out, lse, stream,
+                        true);
 }

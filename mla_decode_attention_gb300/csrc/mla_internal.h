@@ -34,7 +34,8 @@ int check_common(int batch, int s_q, int h_q, int num_sm_parts);
 // Launches the split combine on `stream`; `pdl` enables programmatic
 // dependent launch after the split kernel.
 int launch_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm_parts,
-                   const void* workspace, void* out, float* lse, cudaStream_t stream, bool pdl);
+                   const void* workspace, const float* attn_sink, void* out, float* lse,
+                   cudaStream_t stream, bool pdl);
 
 // Workspace partition: partial O then partial LSE.
 inline int64_t workspace_rows(int batch, int s_q, int num_sm_parts) {

@@ -101,13 +101,14 @@ static_assert(kXferBytes <= kPBufStride && kXferBytes % 16 == 0, "P transfer siz
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // Sparse: the index list entries of key slots 128 t + 4 lane .. + 3 of
-// sequence q (-1 past topk); validated by the caller.
-__device__ __forceinline__ void load_idx4(const SplitParams& p, int q, int t, int lane, int32_t (&id)[4]) {
+// sequence q (-1 past its n_slots = topk or topk_length); validated by the caller.
+__device__ __forceinline__ void load_idx4(const SplitParams& p, int q, int t, int lane, int n_slots,
+                                          int32_t (&id)[4]) {
   const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int slot = t * kTileTokens + 4 * lane + i;
-    id[i] = slot < p.topk ? idx_row[slot] : -1;
+    id[i] = slot < n_slots ? idx_row[slot] : -1;
   }
 }
 
@@ -218,7 +219,8 @@ __global__ void __maxnreg__(224)
         bool ok = true;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           int32_t nid[4];  // sparse: the next tile's indices, requested one tile ahead
-          if constexpr (kSparse) load_idx4(p, q, t0, lane, nid);
+          const int n_slots = kSparse ? meta_seq(meta, p.num_parts, q)[kSKeys] : 0;
+          if constexpr (kSparse) load_idx4(p, q, t0, lane, n_slots, nid);
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
             int32_t y[4];
@@ -226,7 +228,7 @@ __global__ void __maxnreg__(224)
               int32_t id[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) id[i] = nid[i];
-              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, nid);
+              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, n_slots, nid);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const bool valid = id[i] >= 0 && static_cast<int64_t>(id[i]) < p.s_kv;
@@ -400,7 +402,7 @@ __global__ void __maxnreg__(224)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int slot = t * kTileTokens + 32 * k + lane;
-              sid[k] = slot < p.topk ? idx_row[slot] : -1;
+              sid[k] = slot < keys ? idx_row[slot] : -1;
             }
           }
           if (ok) ok = mbar_wait(smem_u32(&bars->s_full[sb]), (tc >> 1) & 1, abort_flag, p.err);
@@ -517,7 +519,16 @@ __global__ void __maxnreg__(224)
           lsum += ls + ls2;
           bsum += bs + bs2;
           st_shared_f32(stage + kSideAlpha + 4 * r, alpha);
-          if (t == t1 - 1) st_shared_f32(stage + kSideInvL + 4 * r, bsum > 0.f ? 1.f / bsum : 0.f);
+          if (t == t1 - 1) {
+            float inv_l = bsum > 0.f ? 1.f / bsum : 0.f;
+            // attention sink: applied with 1/l to a final row, by the combine to a split row
+            if (kSparse && p.attn_sink && srec[kSNSplits] == 1) {
+              const float lse_t = (lsum > 0.f && bsum > 0.f) ? (m_use + __log2f(lsum)) * 0.69314718055994531f
+                                                             : -INFINITY;
+              inv_l *= attn_sink_factor(lse_t, p.attn_sink[r]);
+            }
+            st_shared_f32(stage + kSideInvL + 4 * r, inv_l);
+          }
           if (lane == 0) st_shared_u32(stage + kSideFlags + 4 * (warp - 4), any);
           fence_proxy_async_smem();
           if constexpr (!kSparse) named_barrier_arrive(2, kXferNamedThreads);  // staging full: warp 3 copies
@@ -591,7 +602,8 @@ __global__ void __maxnreg__(224)
         bool ok = true;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           int32_t nid[4];  // sparse: the next tile's indices, requested one tile ahead
-          if constexpr (kSparse) load_idx4(p, q, t0, lane, nid);
+          const int n_slots = kSparse ? meta_seq(meta, p.num_parts, q)[kSKeys] : 0;
+          if constexpr (kSparse) load_idx4(p, q, t0, lane, n_slots, nid);
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
             int32_t y[4];
@@ -599,7 +611,7 @@ __global__ void __maxnreg__(224)
               int32_t id[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) id[i] = nid[i];
-              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, nid);
+              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, n_slots, nid);
 #pragma unroll
               for (int i = 0; i < 4; ++i) y[i] = (id[i] >= 0 && static_cast<int64_t>(id[i]) < p.s_kv) ? id[i] : 0;
             } else {

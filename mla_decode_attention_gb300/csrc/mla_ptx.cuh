@@ -350,6 +350,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Attention-sink factor e^lse / (e^lse + e^sink) = 1 / (1 + 2^((sink - lse)
+// log2 e)) (FlashMLA sparse interface, "attn_sink"); 0 for an empty key set.
+__device__ __forceinline__ float attn_sink_factor(float lse, float sink) {
+  if (lse == -INFINITY) return 0.f;
+  return 1.f / (1.f + fast_exp2((sink - lse) * 1.4426950408889634f));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -65,9 +65,15 @@ MLA_HD const int32_t* meta_seq(const int32_t* m, int num_parts, int q) {
   return m + kHeaderWords + kPartWords * num_parts + kSeqWords * q;
 }
 
-// Key count of sequence (b, j).
+// Key count of sequence (b, j).  Sparse (topk > 0): topk, or, when lengths
+// are given, the first topk_length[b * s_q + j] index slots (clamped to
+// [0, topk]; FlashMLA sparse interface, "topk_length").
 MLA_HD int32_t seq_keys(const int32_t* seqlens, int b, int j, int s_q, int causal, int topk) {
-  if (topk > 0) return topk;
+  if (topk > 0) {
+    if (!seqlens) return topk;
+    const int32_t n = seqlens[b * s_q + j];
+    return n < 0 ? 0 : (n > topk ? topk : n);
+  }
   int32_t L = seqlens[b];
   if (L < 0) L = 0;
   if (causal) {

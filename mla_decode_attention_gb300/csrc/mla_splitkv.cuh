@@ -98,6 +98,7 @@ struct SplitParams {
   int64_t bt_stride;
   int64_t num_pages;       // dense: pages in the cache
   const int32_t* indices;  // sparse: [n_seq, topk]
+  const float* attn_sink;  // sparse, optional: [h] sink logits (out scaled by e^lse / (e^lse + e^sink))
   int topk;
   int64_t s_kv;            // sparse: pool rows
   const __nv_bfloat16* kv_rows;  // dense: cache base (L2 prefetch); sparse: pool base
@@ -434,12 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
+      const int32_t n_slots = meta_seq(meta, p.num_parts, q)[kSKeys];  // topk or topk_length
       for (int t = t0; t < t1 && ok; ++t) {
         int32_t rid[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int slot = t * kTileTokens + 4 * lane + i;
-          const int32_t id = slot < p.topk ? idx_row[slot] : -1;
+          const int32_t id = slot < n_slots ? idx_row[slot] : -1;
           const bool valid = id >= 0 && static_cast<int64_t>(id) < p.s_kv;
           if (!valid && id != -1 && p.err) atomicOr(p.err, MLA_DEVERR_BAD_INDEX);
           rid[i] = valid ? id : 0;
@@ -796,8 +798,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const bool has = lsum > 0.f && bsum > 0.f;
-      const float inv_l = has ? 1.f / bsum : 0.f;
+      const bool final_out = srec[kSNSplits] == 1;
+      float inv_l = has ? 1.f / bsum : 0.f;
       const float lse_v = has ? (m_use + __log2f(lsum)) * 0.69314718055994531f : NEG_INF;
+      // attention sink: applied here to a final row, by the combine to a split row
+      if (p.attn_sink && final_out && hb * kRowsPerCta + R * g + row < p.h)
+        inv_l *= attn_sink_factor(lse_v, p.attn_sink[hb * kRowsPerCta + R * g + row]);
       if (lane < R) bc_a[lane] = inv_l;
       __syncwarp();
       float il[R];
@@ -806,7 +812,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4 t4 = *reinterpret_cast<const float4*>(bc_a + i);
         il[i] = t4.x; il[i + 1] = t4.y; il[i + 2] = t4.z; il[i + 3] = t4.w;
       }
-      const bool final_out = srec[kSNSplits] == 1;
       const int row0 = hb * kRowsPerCta + R * g;  // first head of this warpgroup
       const int split_row = srec[kSSplitOff] + split;
       const int b = q / p.s_q, j = q % p.s_q;

@@ -263,17 +263,39 @@ def fp8_dense_decode(q, kv_raw, block_table, cache_seqlens, softmax_scale,
     return dense_decode(q, kv_raw, block_table, cache_seqlens, softmax_scale, causal, rows)
 
 
-def sparse_decode(q, kv_pool, indices, softmax_scale, rows=None):
+def sink_factor(lse: np.ndarray, attn_sink: np.ndarray) -> np.ndarray:
+    """exp(lse) / (exp(lse) + exp(attn_sink)) per head (FlashMLA sparse
+    interface, "attn_sink": the output is additionally scaled by it); 0 when
+    the key set is empty (lse = -inf)."""
+    lse = np.asarray(lse, dtype=np.float64)
+    sink = np.asarray(attn_sink, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        f = 1.0 / (1.0 + np.exp(sink - lse))
+    return np.where(np.isneginf(lse), 0.0, f)
+
+
+def sparse_decode(q, kv_pool, indices, softmax_scale, rows=None, attn_sink=None, topk_length=None):
     """DSA top-k decode: q [b, s_q, h, 576], kv_pool [s_kv, 576],
-    indices [b, s_q, topk] int (-1 = invalid)."""
+    indices [b, s_q, topk] int (-1 = invalid).
+
+    attn_sink [h] (optional): each head's output row is scaled by
+    sink_factor(lse, attn_sink[h]); lse is unchanged.  topk_length [b, s_q]
+    (optional): query token (b, j) uses only its first topk_length[b, j]
+    index slots, clamped to [0, topk] (FlashMLA sparse interface,
+    "attn_sink" and "topk_length")."""
     q = widen(q)
     b, s_q, h, _ = q.shape
+    topk = indices.shape[-1]
     out = np.full((b, s_q, h, D_V), np.nan)
     lse = np.full((b, h, s_q), np.nan)
     todo = rows if rows is not None else [(bi, j) for bi in range(b) for j in range(s_q)]
+    lengths = None if topk_length is None else np.asarray(topk_length).reshape(b, s_q)
     for bi, j in todo:
-        keys = sparse_keys(kv_pool, indices[bi, j])
+        n = topk if lengths is None else min(max(int(lengths[bi, j]), 0), topk)
+        keys = sparse_keys(kv_pool, indices[bi, j][:n])
         o, l = attend(q[bi, j], keys, softmax_scale)
+        if attn_sink is not None:
+            o = o * sink_factor(l, attn_sink)[:, None]
         out[bi, j] = o
         lse[bi, :, j] = l
     return out, lse

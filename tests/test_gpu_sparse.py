@@ -164,3 +164,29 @@ def test_split_entry_then_combine_equals_sparse_decode():
         assert int(buf.err.item()) == ref_e == 0
         assert np.array_equal(buf.out.float().cpu().numpy(), ref_o)
         assert np.array_equal(buf.lse.cpu().numpy(), ref_l)
+
+
+@pytest.mark.parametrize("h,parts", [(128, None), (128, 3), (64, None), (64, 3)])
+def test_sparse_attn_sink_and_topk_length(h, parts):
+    """The sparse extensions: a per-head attention sink and a per-token topk
+    length (through the schedule), on both kernels; with 3 parts the rows are
+    split and the sink is applied by the combine, otherwise by the split
+    kernel's epilogue.  Lengths include 0 (empty row), 1, a ragged tile and topk."""
+    b, s_q, topk = 3, 2, 700
+    inp = small(61 + h, b=b, s_q=s_q, h=h, s_kv=5000, topk=topk, invalid=40)
+    q, kv, idx = inp["q"].to(DEV), inp["kv"].to(DEV), inp["indices"].to(DEV)
+    lengths = torch.tensor([0, 1, 129, 700, 640, 255], dtype=torch.int32)
+    g = torch.Generator().manual_seed(7)
+    sink = (torch.randn(h, generator=g, dtype=torch.float64) * 3 + 6).to(torch.float32)
+    buf = binding.DecodeBuffers(b, s_q, h, DEV, parts)
+    binding.mla_get_metadata(lengths.to(DEV), b, s_q, False, topk, buf.num_sm_parts, buf.metadata)
+    binding.mla_sparse_decode(q, kv, idx, inp["softmax_scale"], buf.metadata, buf.num_sm_parts,
+                              buf.workspace, buf.out, buf.lse, buf.err, attn_sink=sink.to(DEV))
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.sparse_decode(bf16_np(inp["q"]), bf16_np(inp["kv"]), inp["indices"].numpy(),
+                                        inp["softmax_scale"], attn_sink=sink.double().numpy(),
+                                        topk_length=lengths.numpy().reshape(b, s_q))
+    out, lse = buf.out.float().cpu().numpy(), buf.lse.cpu().numpy()
+    assert_parity(out, ref_o, lse, ref_l, f"sink+length h={h} parts={parts}")
+    assert int(buf.err.item()) == 0
+    assert np.all(out[0, 0] == 0) and np.all(np.isneginf(lse[0, :, 0]))   # length 0

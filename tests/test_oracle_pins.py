@@ -405,3 +405,49 @@ def test_parity_checker_accepts_the_bf16_floor_and_rejects_real_errors():
         assert_parity(torch.from_numpy(o2).to(torch.bfloat16).double().numpy(), o, l2, l, "drop")
     with pytest.raises(AssertionError):
         assert_parity(ideal, o, l + 2e-3, l, "lse")
+
+
+# ------------------------------------------- attention sink and topk length
+
+def test_attention_sink_is_a_zero_valued_key_with_the_sink_as_its_score():
+    """exp(lse) / (exp(lse) + exp(sink)) scaling equals attending over the
+    keys plus one extra key whose score is the sink and whose value is 0
+    (brute force through the plain definition, one head at a time)."""
+    r = rng(41)
+    pool = r.standard_normal((50, 576))
+    idx = r.permutation(50)[:12].reshape(1, 1, 12).astype(np.int64)
+    q = r.standard_normal((1, 1, 3, 576))
+    sink = np.array([-1.5, 0.4, 3.0])
+    out, lse = oracle.sparse_decode(q, pool, idx, SCALE, attn_sink=sink)
+    base, base_lse = oracle.sparse_decode(q, pool, idx, SCALE)
+    assert np.array_equal(lse, base_lse)                    # lse is not changed by the sink
+    for h in range(3):
+        k_sink = np.zeros(576)
+        c = 512 + int(np.argmax(np.abs(q[0, 0, h, 512:])))  # a RoPE column with q != 0
+        k_sink[c] = sink[h] / (SCALE * q[0, 0, h, c])       # score = sink, value = 0
+        keys = np.vstack([pool[idx[0, 0]], k_sink])
+        o, _ = oracle.attend(q[0, 0, h:h + 1], keys, SCALE)
+        np.testing.assert_allclose(out[0, 0, h], o[0], rtol=1e-12, atol=1e-14)
+    # special cases: sink = -inf changes nothing, sink = lse halves the output
+    o1, _ = oracle.sparse_decode(q, pool, idx, SCALE, attn_sink=np.full(3, -np.inf))
+    assert np.array_equal(o1, base)
+    o2, _ = oracle.sparse_decode(q, pool, idx, SCALE, attn_sink=base_lse[0, :, 0])
+    np.testing.assert_allclose(o2, 0.5 * base, rtol=1e-12, atol=0)
+
+
+def test_topk_length_equals_masking_the_later_slots():
+    """Using the first n index slots is the same as marking the rest -1;
+    n = 0 gives an empty key set, n > topk is clamped to topk."""
+    r = rng(42)
+    pool = r.standard_normal((80, 576))
+    idx = r.permutation(80)[:40].reshape(2, 2, 10).astype(np.int64)
+    q = r.standard_normal((2, 2, 4, 576))
+    lengths = np.array([[0, 3], [10, 25]])
+    out, lse = oracle.sparse_decode(q, pool, idx, SCALE, topk_length=lengths)
+    masked = idx.copy()
+    for b in range(2):
+        for j in range(2):
+            masked[b, j, min(lengths[b, j], 10):] = -1
+    ref, ref_l = oracle.sparse_decode(q, pool, masked, SCALE)
+    assert np.array_equal(out, ref) and np.array_equal(lse, ref_l)
+    assert np.all(out[0, 0] == 0) and np.all(np.isneginf(lse[0, :, 0]))
