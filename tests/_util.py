@@ -47,7 +47,8 @@ def parity_stats(out, out_ref, lse, lse_ref):
     lse = np.asarray(lse, dtype=np.float64)
     lse_ref = np.asarray(lse_ref, dtype=np.float64)
     both_inf = np.isinf(lse) & np.isinf(lse_ref) & (np.sign(lse) == np.sign(lse_ref))
-    lse_err = np.where(both_inf, 0.0, np.abs(lse - lse_ref))
+    with np.errstate(invalid="ignore"):  # -inf - -inf where both rows are empty
+        lse_err = np.where(both_inf, 0.0, np.abs(lse - lse_ref))
     return dict(rel_l2=rel_l2, max_abs=max_abs, max_abs_beyond_rounding=beyond, rms=rms,
                 max_abs_over_rms=max_abs / rms if rms > 0 else float(max_abs > 0) * np.inf,
                 lse_max_err=float(np.max(lse_err)) if lse_err.size else 0.0)
