@@ -264,9 +264,9 @@ def fp8_dense_decode(q, kv_raw, block_table, cache_seqlens, softmax_scale,
 
 
 def sink_factor(lse: np.ndarray, attn_sink: np.ndarray) -> np.ndarray:
-    """exp(lse) / (exp(lse) + exp(attn_sink)) per head (FlashMLA sparse
-    interface, "attn_sink": the output is additionally scaled by it); 0 when
-    the key set is empty (lse = -inf)."""
+    """exp(lse) / (exp(lse) + exp(attn_sink)) per head, the factor the
+    FlashMLA sparse interface ("attn_sink") multiplies each output row by; 0
+    when the key set is empty (lse = -inf)."""
     lse = np.asarray(lse, dtype=np.float64)
     sink = np.asarray(attn_sink, dtype=np.float64)
     with np.errstate(over="ignore", invalid="ignore"):
