@@ -266,3 +266,21 @@ def test_schedule_choice_prefers_splitting_long_uneven_batches():
     # more sequences than parts: no schedule B at all
     m = check_schedule(np.full(80, 1000, np.int32), 1, True, 0, 76)
     assert not walks_whole_sequences(m, 1000)
+
+
+def test_sparse_schedule_with_topk_length():
+    """Sparse with per-token lengths (topk_length in place of cache_seqlens):
+    each query token's key count is its length clamped to [0, topk], and the
+    schedule covers exactly those tiles."""
+    b, s_q, topk, parts = 5, 2, 700, 7
+    lengths = np.array([0, 1, 127, 128, 129, 700, 701, -3, 640, 255], np.int32)
+    m = binding.mla_get_metadata_host(lengths, b, s_q, False, topk, parts)
+    hdr, prt, seq = parse_meta(m, b * s_q, parts)
+    keys = np.clip(lengths, 0, topk)
+    assert np.array_equal(seq[:, 3], keys) and np.array_equal(seq[:, 0], (keys + 127) // 128)
+    covered = set()
+    for p in range(parts):
+        for (q, t0, t1, _) in walk_part(prt[p], seq):
+            covered.update((q, t) for t in range(t0, t1))
+    assert covered == {(q, t) for q in range(b * s_q) for t in range(int(seq[q, 0]))}
+    assert np.array_equal(seq[:, 2] > 0, seq[:, 0] > 0)     # empty tokens have no split
