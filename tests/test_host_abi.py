@@ -284,3 +284,20 @@ def test_sparse_schedule_with_topk_length():
             covered.update((q, t) for t in range(t0, t1))
     assert covered == {(q, t) for q in range(b * s_q) for t in range(int(seq[q, 0]))}
     assert np.array_equal(seq[:, 2] > 0, seq[:, 0] > 0)     # empty tokens have no split
+
+
+def test_benchmark_workloads_walk_the_documented_schedules():
+    """Dense b=64 t=4096 and DSA walk whole sequences on the two-SM kernels;
+    FP8 t=8192 keeps the balanced split on the one-SM kernel; spec (256 query
+    tokens over 76 parts) has only the balanced split, in two token groups."""
+    from mla_decode_attention_gb300 import workloads
+    dense = binding.mla_get_metadata_host(np.full(64, 4096, np.int32), 64, 1, True, 0, 76)
+    assert walks_whole_sequences(dense, 11)
+    dsa = binding.mla_get_metadata_host(None, 64, 1, False, 2048, 76)
+    assert walks_whole_sequences(dsa, 5)
+    fp8 = binding.mla_get_metadata_host(np.full(64, 8192, np.int32), 64, 1, True, 0, 76)
+    assert not walks_whole_sequences(fp8, 4)
+    w = workloads.WORKLOADS["spec"]
+    sl = np.random.default_rng(3).integers(*w.seqlen_range, size=w.b, endpoint=True).astype(np.int32)
+    spec = binding.mla_get_metadata_host(sl, w.b, w.s_q, True, 0, 76)
+    assert not walks_whole_sequences(spec, 11) and spec[13] == 2
