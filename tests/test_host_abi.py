@@ -301,3 +301,35 @@ def test_benchmark_workloads_walk_the_documented_schedules():
     sl = np.random.default_rng(3).integers(*w.seqlen_range, size=w.b, endpoint=True).astype(np.int32)
     spec = binding.mla_get_metadata_host(sl, w.b, w.s_q, True, 0, 76)
     assert not walks_whole_sequences(spec, 11) and spec[13] == 2
+
+
+def _call_sparse(**over):
+    """mla_sparse_decode with fake (never dereferenced) aligned pointers."""
+    a = dict(q=0x10000, kv=0x20000, s_kv=1000, idx=0x30000, topk=64, batch=2, s_q=1, h=16,
+             scale=0.07, sink=None, meta=0x50000, parts=4, ws=0x60000, out=0x70000, lse=0x80000,
+             err=None, stream=None)
+    a.update(over)
+    return binding.lib().mla_sparse_decode(a["q"], a["kv"], a["s_kv"], a["idx"], a["topk"], a["batch"],
+                                           a["s_q"], a["h"], a["scale"], a["sink"], a["meta"], a["parts"],
+                                           a["ws"], a["out"], a["lse"], a["err"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(idx=None), -1), (dict(meta=None), -1), (dict(topk=0), -2), (dict(s_kv=0), -2),
+    (dict(h=100), -2), (dict(scale=-1.0), -2), (dict(kv=0x20008), -3),
+])
+def test_sparse_decode_rejects_bad_arguments_before_launch(over, code):
+    # the attention sink is optional: a NULL sink never fails validation
+    assert _call_sparse(**over) == code
+
+
+def test_binding_checks_the_attention_sink():
+    import torch
+    cpu = torch.zeros(16, dtype=torch.float32)
+    with pytest.raises(ValueError):   # must live on the GPU
+        binding.mla_combine(torch.zeros(4, dtype=torch.int32), 2, 1, 16, 4, cpu, cpu, cpu,
+                            attn_sink=cpu)
+
+
+def test_wait_timeout_check_rejects_a_null_error_word():
+    assert binding.lib().mla_check_wait_timeout(None, None) == -1   # MLA_ERR_NULL
