@@ -63,6 +63,18 @@ def job_rate(units_per_rank: float, ms_per_step: float, world: int) -> float:
     return units_per_rank / (ms_per_step * 1e-3) * world
 
 
+def check_world(gpus: int, world: int):
+    """None when the launch matches --gpus, else why not.  Every GPU runs one
+    process (one replica of the batch), so N > 1 needs a launcher that starts
+    N ranks (torchrun) and sets WORLD_SIZE = N."""
+    if gpus < 1:
+        return f"--gpus must be >= 1 (got {gpus})"
+    if gpus != world:
+        return (f"--gpus {gpus} but WORLD_SIZE={world}: launch one process per GPU, e.g. "
+                f"python -m torch.distributed.run --nproc-per-node {gpus} bench.py --gpus {gpus}")
+    return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -497,6 +509,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    problem = check_world(args.gpus, world)
+    if problem:
+        print(problem, file=sys.stderr, flush=True)
+        sys.exit(2)
 
     if args.impl == "reference":
         if rank == 0:

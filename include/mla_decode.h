@@ -25,9 +25,16 @@
  *  - Return value: MLA_OK (0) or a negative MLA_ERR_* code.  Errors are
  *    detected on the host before any launch (nothing is launched then).
  *  - `err` (optional, may be NULL): a device uint32 word the kernels OR
- *    MLA_DEVERR_* bits into (bad page id, bad index, bounded-wait timeout).
- *    The caller zeroes it and reads it back when it wants to.  Bad ids never
- *    fault: the row they name is masked out.
+ *    MLA_DEVERR_* bits into (bad page id, bad index, bounded-wait timeout,
+ *    metadata that does not match the call).  The caller zeroes it and reads
+ *    it back when it wants to.  Bad ids never fault: the row they name is
+ *    masked out.
+ *  - Metadata is read-only for every decode entry point.  Each decode kernel
+ *    first compares the metadata header (magic, version, batch, s_q, number
+ *    of parts, topk, causal) with its own arguments; on a mismatch it sets
+ *    MLA_DEVERR_METADATA and returns without reading q, the cache or the
+ *    page table and without writing out or lse (the combine then writes
+ *    nothing either).
  *  - Row layouts (all contiguous, C order):
  *      q      [batch, s_q, h_q, 576] bf16
  *      out    [batch, s_q, h_q, 512] bf16
@@ -58,9 +65,13 @@ extern "C" {
 #define MLA_ERR_UNSUPPORTED (-6) /* device is not sm_103/sm_100 class          */
 
 /* ------------------------------------------------ device error word (err) */
-#define MLA_DEVERR_BAD_PAGE 1u   /* block_table entry outside [0, num_pages)  */
+#define MLA_DEVERR_BAD_PAGE 1u   /* block_table entry outside [0, num_pages), *
+                                  * or a length needing more page slots than *
+                                  * block_table_stride                       */
 #define MLA_DEVERR_BAD_INDEX 2u  /* sparse index < -1 or >= s_kv              */
 #define MLA_DEVERR_TIMEOUT 4u    /* an internal wait ran out (kernel bailed)  */
+#define MLA_DEVERR_METADATA 8u   /* metadata built for another shape (nothing *
+                                  * was computed), or for other lengths      */
 
 /* -------------------------------------------------------- KV cache formats */
 #define MLA_KV_BF16 0    /* [num_pages, 64, 576] bf16, 1152 B per token        */
@@ -119,13 +130,10 @@ int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes);
  * kernel-specific split penalty (4 to 11 tiles) above A's balanced cost:
  * every extra piece costs a Q load and an epilogue, every split row a
  * combine read.  Layout of one schedule (int32):
- *   [0,16)                    header: magic 0x4D4C4131, version (2), n_seq,
+ *   [0,16)                    header: magic 0x4D4C4131, version (3), n_seq,
  *                             num_sm_parts, tile_tokens (128), s_q, batch,
  *                             causal, topk, total_splits, cost_per_part,
- *                             largest sequence cost, chosen, groups, 0...
- *                             (chosen, in A only: 0 or 1 = the schedule the
- *                             last decode call walked; the decode kernels
- *                             write it and the combine reads it)
+ *                             largest sequence cost, 0, groups, 0...
  *   [16, 16 + 8 * parts)      per part: q_begin, t_begin, q_end, t_end,
  *                             split_begin, q_step, 0, 0 (half-open range of
  *                             (sequence, tile) pairs, sequences q_begin,
@@ -147,9 +155,11 @@ int mla_get_metadata_host(const int32_t* cache_seqlens_host, int batch, int s_q,
                           int topk, int num_sm_parts, void* metadata_host);
 
 /*
- * Size in bytes of the fp32 split workspace: partial outputs
- * [batch*s_q + num_sm_parts, h_q, 512] followed by partial LSEs
- * [batch*s_q + num_sm_parts, h_q].
+ * Size in bytes of the split workspace: fp32 partial outputs
+ * [batch*s_q + num_sm_parts, h_q, 512], fp32 partial LSEs
+ * [batch*s_q + num_sm_parts, h_q], then 64 bytes of control words (the
+ * split kernel records there which of the metadata's two schedules it
+ * walked; mla_combine reads it).  One workspace serves one call at a time.
  */
 int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts, size_t* bytes);
 
@@ -163,16 +173,21 @@ int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts, size_t* by
  *               MLA_KV_FP8_656: [num_pages, 64, 656] uint8
  *  block_table  [batch, block_table_stride] int32; entry [b, p] = physical
  *               page of tokens 64p .. 64p+63 of request b.  Only the first
- *               ceil(cache_seqlens[b] / 64) entries of a row are read.
+ *               ceil(cache_seqlens[b] / 64) entries of a row are read, and
+ *               never more than block_table_stride of them: a length that
+ *               needs more page slots than the row has sets
+ *               MLA_DEVERR_BAD_PAGE, and the keys of the missing slots are
+ *               masked out like those of a bad page id.
  *  cache_seqlens [batch] int32, cached tokens per request (new tokens
  *               included).  With causal != 0 and s_q > 1, new token j sees
- *               keys 0 .. cache_seqlens[b] - s_q + j.
+ *               keys 0 .. cache_seqlens[b] - s_q + j.  The key counts come
+ *               from the metadata; the kernel compares them with the ones
+ *               cache_seqlens and causal give and sets MLA_DEVERR_METADATA
+ *               on a difference (metadata computed from other lengths).
  *  Cache slots past a request's length inside its last page must hold
  *  finite values (they are masked, but multiply a zero weight).
  *  metadata     from mla_get_metadata(cache_seqlens, batch, s_q, causal, 0,
- *               num_sm_parts, ...) on the same lengths.  The kernels record
- *               in its header word 12 which of its two schedules they walked
- *               (read by the combine); nothing else in it is written.
+ *               num_sm_parts, ...) on the same lengths; read-only.
  *  workspace    mla_workspace_size() bytes, 16-byte aligned.
  *  out, lse     outputs as described at the top of this file.  A query row
  *               with no visible key gets out = 0, lse = -inf.
@@ -180,7 +195,7 @@ int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts, size_t* by
 int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
                const int32_t* block_table, int64_t block_table_stride,
                const int32_t* cache_seqlens, int batch, int s_q, int h_q, float softmax_scale,
-               int causal, void* metadata, int num_sm_parts, void* workspace, void* out,
+               int causal, const void* metadata, int num_sm_parts, void* workspace, void* out,
                float* lse, uint32_t* err, cudaStream_t stream);
 
 /*
@@ -193,7 +208,7 @@ int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_p
 int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
                        const int32_t* block_table, int64_t block_table_stride,
                        const int32_t* cache_seqlens, int batch, int s_q, int h_q,
-                       float softmax_scale, int causal, void* metadata, int num_sm_parts,
+                       float softmax_scale, int causal, const void* metadata, int num_sm_parts,
                        void* workspace, void* out, float* lse, uint32_t* err,
                        cudaStream_t stream);
 
@@ -206,6 +221,11 @@ int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_format, int64
  *  indices  [batch, s_q, topk] int32; -1 marks an invalid slot.  Any other
  *           value outside [0, s_kv) is also skipped and sets
  *           MLA_DEVERR_BAD_INDEX (FlashMLA itself does no bound check).
+ *           Only rows a query token names are ever read for it: an invalid
+ *           slot is loaded from a row the token does name (its weight is
+ *           0), so the contents of unnamed pool rows (NaN included) never
+ *           reach the output.  A token that names no row gets out = 0 and
+ *           lse = -inf.
  *  attn_sink optional [h_q] fp32 device array (NULL = none; FlashMLA sparse
  *           interface, "attn_sink"): every output row of head h is scaled
  *           by exp(lse) / (exp(lse) + exp(attn_sink[h])); lse itself is
@@ -220,7 +240,7 @@ int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_format, int64
  */
 int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv, const int32_t* indices,
                       int topk, int batch, int s_q, int h_q, float softmax_scale,
-                      const float* attn_sink, void* metadata, int num_sm_parts, void* workspace,
+                      const float* attn_sink, const void* metadata, int num_sm_parts, void* workspace,
                       void* out, float* lse, uint32_t* err, cudaStream_t stream);
 
 /*
@@ -231,7 +251,7 @@ int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv, const int32_t
  */
 int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv, const int32_t* indices,
                               int topk, int batch, int s_q, int h_q, float softmax_scale,
-                              const float* attn_sink, void* metadata, int num_sm_parts,
+                              const float* attn_sink, const void* metadata, int num_sm_parts,
                               void* workspace, void* out, float* lse, uint32_t* err,
                               cudaStream_t stream);
 
@@ -269,12 +289,15 @@ int mla_check_wait_timeout(uint32_t* err, cudaStream_t stream);
  *    b=64, s_q=1, h_q=128 decode fits; use mla_decode for larger batches.
  *  - The array exists once per device that loads this library and stays
  *    reserved until the process exits.
- *  - The first call on a device looks up the array's address on that device
- *    (with the device current) and caches it; make that first call before
- *    any stream capture.
+ *  - The first call in a CUDA context looks up the array's address in that
+ *    context (the array is per context: a context created after
+ *    cudaDeviceReset, or another context the caller made current, has its
+ *    own copy) and caches it per context; make that first call before any
+ *    stream capture.
  *  - Every call shares the array: calls that overlap on the GPU (other
  *    streams, other host threads on the same device) race and corrupt each
- *    other's results.  Nothing in it needs clearing between calls.
+ *    other's results.  Nothing in it needs clearing between calls: every
+ *    call rewrites the schedule and the control word before reading them.
  */
 int mla_decode_noalloc(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
                        const int32_t* block_table, int64_t block_table_stride,

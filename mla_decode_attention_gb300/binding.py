@@ -23,6 +23,7 @@ MLA_KV_FP8_656 = 1
 MLA_DEVERR_BAD_PAGE = 1
 MLA_DEVERR_BAD_INDEX = 2
 MLA_DEVERR_TIMEOUT = 4
+MLA_DEVERR_METADATA = 8
 
 META_HEADER_WORDS = 16
 META_PART_WORDS = 8

@@ -1,13 +1,17 @@
 """Builds the in-tree C-ABI library ``libmla_decode.so`` for sm_103a.
 
 Each ``csrc/*.cu`` translation unit is compiled in parallel with nvcc, then
-linked into one shared library next to this file.  ``python -m
+linked into one shared library next to this file.  The build fails when any
+kernel spills registers (the ptxas report of every kernel is checked, as the
+FlashMLA build does after compiling; ``MLA_SKIP_REG_SPILL_CHECK=1`` skips
+the check).  ``python -m
 mla_decode_attention_gb300.build`` runs it.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -44,13 +48,26 @@ def _compile(src: str) -> tuple[str, str]:
     return obj, r.stderr
 
 
+_ENTRY = re.compile(r"Compiling entry function '([^']+)'")
+_SPILL = re.compile(r"(\d+) bytes spill stores, (\d+) bytes spill loads")
+
+
 def spill_report(ptxas_log: str) -> list[str]:
-    """Lines of the ptxas log that report register spills (build hygiene)."""
+    """Kernels that spill registers, one line each, from a ``-Xptxas -v`` log.
+
+    Each ``Compiling entry function`` line names a kernel; the next
+    ``bytes spill stores, ... bytes spill loads`` line gives its spills.
+    """
     out = []
+    entry = None
     for line in ptxas_log.splitlines():
-        if "spill" in line and not line.strip().startswith("0 bytes spill stores, 0 bytes spill loads"):
-            if " 0 bytes spill stores, 0 bytes spill loads" not in line:
-                out.append(line.strip())
+        m = _ENTRY.search(line)
+        if m:
+            entry = m.group(1)
+            continue
+        m = _SPILL.search(line)
+        if m and (int(m.group(1)) or int(m.group(2))):
+            out.append(f"{entry}: {line.strip()}")
     return out
 
 
@@ -64,6 +81,10 @@ def build(verbose: bool = False) -> str:
         f.write(log)
     if verbose:
         print(log)
+    spills = spill_report(log)
+    if spills and os.environ.get("MLA_SKIP_REG_SPILL_CHECK") != "1":
+        raise RuntimeError("register spilling detected, build failed (set "
+                           "MLA_SKIP_REG_SPILL_CHECK=1 to skip this check):\n" + "\n".join(spills))
     lib = os.path.join(HERE, LIB_NAME)
     tmp = lib + ".tmp"
     cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]

@@ -18,19 +18,28 @@ constexpr int kCombineThreads = 32 * kCombineWarps;
 
 // Lane l of a warp owns output columns [16 l, 16 l + 16): each split row is read
 // as 2 KB contiguous per warp, and the bf16 row is written as 1 KB contiguous.
-// At most 64 registers per thread: four CTAs (32 warps) per SM, so that one
-// or two waves cover the rows of a typical batch.
+// At most 80 registers per thread (three CTAs, 24 warps per SM): no spills.
 // attn_sink (optional, [h]): the merged row is scaled by e^lse / (e^lse + e^sink).
-__global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(
-    const int32_t* __restrict__ meta, int h, int s_q, int num_parts, const float* __restrict__ ws_o,
-    const float* __restrict__ ws_lse, const float* __restrict__ attn_sink, __nv_bfloat16* __restrict__ out,
-    float* __restrict__ lse) {
+__global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(
+    const int32_t* __restrict__ meta, int batch, int h, int s_q, int num_parts, const float* __restrict__ ws_o,
+    const float* __restrict__ ws_lse, const int32_t* __restrict__ ws_ctrl, const float* __restrict__ attn_sink,
+    __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   const int q = blockIdx.x;
   const int head = blockIdx.y * kCombineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  // The split kernel records which of the two schedules it walked.
   pdl_wait_primary();
-  const int32_t* sched = meta[kHChosen] ? schedule_b(meta) : meta;
+  // Metadata for another shape: the split kernel computed nothing (and set
+  // MLA_DEVERR_METADATA); write nothing either.  The topk and causal words
+  // do not change the layout, so any matching batch / s_q / parts passes.
+  if (meta[kHMagic] != kMetaMagic || meta[kHVersion] != kMetaVersion || meta[kHNSeq] != batch * s_q ||
+      meta[kHParts] != num_parts || meta[kHSq] != s_q || meta[kHBatch] != batch)
+    return;
+  // The split kernel recorded in the workspace which schedule it walked, or
+  // -1 when it rejected the metadata (then there is nothing to merge).
+  const int32_t walked = ws_ctrl[0];
+  if (walked != 0 && walked != 1) return;
+  const bool use_b = walked == 1 && schedule_b(meta)[kHMagic] == kMetaMagic;
+  const int32_t* sched = use_b ? schedule_b(meta) : meta;
   const int32_t* s = meta_seq(sched, num_parts, q);
   const int n_splits = s[kSNSplits];
   const int off = s[kSSplitOff];
@@ -105,6 +114,7 @@ int launch_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm
   const int64_t rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
   const float* ws_o = static_cast<const float*>(workspace);
   const float* ws_lse = ws_o + rows * kDv;
+  const int32_t* ws_ctrl = workspace_ctrl(workspace, rows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(batch * s_q, (h_q + kCombineWarps - 1) / kCombineWarps, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
@@ -116,7 +126,7 @@ int launch_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const int32_t*>(metadata),
-                                           h_q, s_q, num_sm_parts, ws_o, ws_lse, attn_sink,
+                                           batch, h_q, s_q, num_sm_parts, ws_o, ws_lse, ws_ctrl, attn_sink,
                                            static_cast<__nv_bfloat16*>(out), lse);
   return e == cudaSuccess ? MLA_OK : record_cuda_error("combine kernel launch", e);
 }

@@ -156,7 +156,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
                                   int64_t num_pages, const int32_t* block_table,
                                   int64_t block_table_stride, const int32_t* cache_seqlens,
                                   int batch, int s_q, int h_q, float softmax_scale, int causal,
-                                  void* metadata, int num_sm_parts, void* workspace,
+                                  const void* metadata, int num_sm_parts, void* workspace,
                                   void* out, float* lse, uint32_t* err, cudaStream_t stream) {
   int rc = check_common(batch, s_q, h_q, num_sm_parts);
   if (rc != MLA_OK) return rc;
@@ -169,7 +169,6 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(metadata) || !aligned16(workspace) ||
       !aligned16(out))
     return MLA_ERR_ALIGN;
-  (void)causal;  // causality is baked into the metadata's key counts
 
   const int n_seq = batch * s_q;
   const int n_hblk = head_blocks(h_q);
@@ -198,16 +197,21 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   }
 
   SplitParams prm = {};
-  prm.meta = static_cast<int32_t*>(metadata);
+  prm.meta = static_cast<const int32_t*>(metadata);
   prm.block_table = block_table;
   prm.bt_stride = block_table_stride;
   prm.num_pages = num_pages;
+  prm.cache_seqlens = cache_seqlens;
+  prm.causal = causal ? 1 : 0;
+  prm.batch = batch;
+  prm.topk = 0;
   prm.kv_rows = static_cast<const __nv_bfloat16*>(kv_cache);
   prm.kv_fp8 = static_cast<const uint8_t*>(kv_cache);
   prm.q = static_cast<const __nv_bfloat16*>(q);
   const int64_t ws_rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
   prm.ws_o = static_cast<float*>(workspace);
   prm.ws_lse = prm.ws_o + ws_rows * kDv;
+  prm.ws_ctrl = workspace_ctrl(workspace, ws_rows);
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
   prm.err = err;
@@ -226,7 +230,7 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
 extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, int64_t num_pages,
                           const int32_t* block_table, int64_t block_table_stride,
                           const int32_t* cache_seqlens, int batch, int s_q, int h_q,
-                          float softmax_scale, int causal, void* metadata, int num_sm_parts,
+                          float softmax_scale, int causal, const void* metadata, int num_sm_parts,
                           void* workspace, void* out, float* lse, uint32_t* err,
                           cudaStream_t stream) {
   const int rc = mla_decode_splitkv(q, kv_cache, kv_format, num_pages, block_table,
@@ -241,7 +245,7 @@ extern "C" int mla_decode(const void* q, const void* kv_cache, int kv_format, in
 extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv,
                                          const int32_t* indices, int topk, int batch, int s_q,
                                          int h_q, float softmax_scale, const float* attn_sink,
-                                         void* metadata, int num_sm_parts, void* workspace, void* out,
+                                         const void* metadata, int num_sm_parts, void* workspace, void* out,
                                          float* lse, uint32_t* err, cudaStream_t stream) {
   int rc = check_common(batch, s_q, h_q, num_sm_parts);
   if (rc != MLA_OK) return rc;
@@ -262,7 +266,9 @@ extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t 
     return record_error("cuTensorMapEncodeTiled failed for kv", MLA_ERR_CUDA);
 
   SplitParams prm = {};
-  prm.meta = static_cast<int32_t*>(metadata);
+  prm.meta = static_cast<const int32_t*>(metadata);
+  prm.batch = batch;
+  prm.causal = 0;
   prm.indices = indices;
   prm.attn_sink = attn_sink;
   prm.topk = topk;
@@ -272,6 +278,7 @@ extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t 
   const int64_t ws_rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
   prm.ws_o = static_cast<float*>(workspace);
   prm.ws_lse = prm.ws_o + ws_rows * kDv;
+  prm.ws_ctrl = workspace_ctrl(workspace, ws_rows);
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
   prm.err = err;
@@ -288,7 +295,7 @@ extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t 
 
 extern "C" int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv,
                                  const int32_t* indices, int topk, int batch, int s_q, int h_q,
-                                 float softmax_scale, const float* attn_sink, void* metadata,
+                                 float softmax_scale, const float* attn_sink, const void* metadata,
                                  int num_sm_parts, void* workspace, void* out, float* lse,
                                  uint32_t* err, cudaStream_t stream) {
   const int rc = mla_sparse_decode_splitkv(q, kv, s_kv, indices, topk, batch, s_q, h_q,

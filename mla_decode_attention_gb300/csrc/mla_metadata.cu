@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
     meta[kHTotalSplits] = static_cast<int32_t>(total_splits);
     meta[kHPerPart] = static_cast<int32_t>(per_part);
     meta[kHMaxCost] = max_cost;
-    meta[kHChosen] = 0;
+    meta[kHReserved] = 0;
     meta[kHGroups] = groups;
     for (int i = kHGroups + 1; i < kHeaderWords; ++i) meta[i] = 0;
     for (int i = 0; i < kHeaderWords; ++i) mb[i] = has_b ? meta[i] : 0;
@@ -269,7 +269,7 @@ extern "C" int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts,
   const int rc = check_common(batch, s_q, h_q, num_sm_parts);
   if (rc != MLA_OK) return rc;
   const int64_t rows = workspace_rows(batch, s_q, num_sm_parts) * h_q;
-  *bytes = static_cast<size_t>(rows) * (kDv + 1) * sizeof(float);
+  *bytes = static_cast<size_t>(rows) * (kDv + 1) * sizeof(float) + kWorkspaceCtrlBytes;
   return MLA_OK;
 }
 
@@ -341,7 +341,7 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
   meta[kHTotalSplits] = static_cast<int32_t>(splits);
   meta[kHPerPart] = static_cast<int32_t>(per_part);
   meta[kHMaxCost] = max_cost;
-  meta[kHChosen] = 0;
+  meta[kHReserved] = 0;
   meta[kHGroups] = groups;
   for (int i = kHGroups + 1; i < kHeaderWords; ++i) meta[i] = 0;
   // schedule B (one whole sequence per part), when every sequence has a part

@@ -14,6 +14,8 @@
 // different host threads on the same device) race and corrupt each other's
 // results; serialise them.  Nothing in it needs to start at zero: every call
 // rewrites the metadata and every partial it later reads.
+#include <cuda.h>
+
 #include <cstdint>
 #include <mutex>
 
@@ -24,23 +26,68 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+// The array's device address depends on where the library's device code is
+// loaded: once per CUDA context.  A context created after cudaDeviceReset,
+// or a non-primary context made current by the caller, has its own copy at
+// its own address, so the cache is keyed by the context current at the call.
+constexpr int kMaxContexts = 64;
+struct ScratchEntry {
+  CUcontext ctx;
+  void* ptr;
+};
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+ScratchEntry g_scratch[kMaxContexts] = {};
+int g_scratch_n = 0;
 
-// Device address of the scratch array on the current device.  The first call
-// per device looks it up (this can load the library's device code onto that
-// device); later calls reuse the cached address.
-int scratch_address(int device, void** out) {
-  if (device < 0 || device >= kMaxDevices) return mla::record_error("device index out of range", MLA_ERR_UNSUPPORTED);
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[device] == nullptr) {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of the scratch array in the current context.  The first
+// call in a context looks it up with that context current (this can load the
+// library's device code into it); later calls in that context reuse it.
+int scratch_address(void** out) {
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return mla::record_error("cuCtxGetCurrent is not available", MLA_ERR_CUDA);
+  CUcontext ctx = nullptr;
+  void* p = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+    // no context yet: the symbol lookup makes the runtime set up the
+    // device's primary context, which is then current
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return mla::record_cuda_error("cudaGetSymbolAddress(noalloc scratch)", e);
-    g_scratch_ptr[device] = p;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+      return mla::record_error("no current CUDA context", MLA_ERR_CUDA);
   }
-  *out = g_scratch_ptr[device];
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  for (int i = 0; i < g_scratch_n; ++i)
+    if (g_scratch[i].ctx == ctx) {
+      *out = g_scratch[i].ptr;
+      return MLA_OK;
+    }
+  if (p == nullptr) {
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return mla::record_cuda_error("cudaGetSymbolAddress(noalloc scratch)", e);
+  }
+  if (g_scratch_n < kMaxContexts) {
+    g_scratch[g_scratch_n++] = ScratchEntry{ctx, p};
+  } else {  // a full cache keeps working: the oldest entry makes room
+    for (int i = 1; i < kMaxContexts; ++i) g_scratch[i - 1] = g_scratch[i];
+    g_scratch[kMaxContexts - 1] = ScratchEntry{ctx, p};
+  }
+  *out = p;
   return MLA_OK;
 }
 
@@ -70,7 +117,7 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv_cache, int kv_fo
         "MLA_NOALLOC_SCRATCH_BYTES scratch; use mla_decode with caller-provided buffers",
         MLA_ERR_SHAPE);
   void* base = nullptr;
-  rc = scratch_address(device, &base);
+  rc = scratch_address(&base);
   if (rc != MLA_OK) return rc;
   unsigned char* scratch = static_cast<unsigned char*>(base);
   rc = mla_get_metadata(cache_seqlens, batch, s_q, causal, 0, parts, scratch, stream);

@@ -184,10 +184,16 @@ __global__ void __maxnreg__(224)
   // over 76 parts cost ~26 us in extra pieces and the combine for ~12 us of
   // better balance; a sparse tile takes about twice as long.
   constexpr int kSplitPenalty = kSparse ? 5 : 11;
-  const int32_t* meta = schedule_for(p.meta, kSplitPenalty);
-  if (blockIdx.x == 0 && threadIdx.x == 0)  // read by the combine after this grid
-    p.meta[kHChosen] = meta == p.meta ? 0 : 1;
-  if (threadIdx.x == 0 && rank == 0) {  // the first piece's query rows start towards L2
+  // The metadata must describe this call; otherwise nothing is read or written.
+  const bool meta_ok = meta_header_matches(p.meta, p.batch, p.s_q, p.num_parts, p.topk, p.causal);
+  const int32_t* meta = meta_ok ? schedule_for(p.meta, kSplitPenalty) : p.meta;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // read by the combine after this grid: the schedule walked, or -1 when
+    // the metadata was rejected (the combine then writes nothing)
+    p.ws_ctrl[0] = meta_ok ? (meta == p.meta ? 0 : 1) : -1;
+    if (!meta_ok && p.err) atomicOr(p.err, MLA_DEVERR_METADATA);
+  }
+  if (meta_ok && threadIdx.x == 0 && rank == 0) {  // the first piece's query rows start towards L2
     PartCursor c0 = part_cursor(meta, part);
     int q0, a0, b0, s0;
     if (next_piece(meta, p.num_parts, &c0, &q0, &a0, &b0, &s0))
@@ -196,7 +202,9 @@ __global__ void __maxnreg__(224)
   const uint32_t tmem = bars->tmem_base;
   volatile uint32_t* abort_flag = &bars->abort;
 
-  if (rank == 0) {
+  if (!meta_ok) {
+    // nothing to do: every role is skipped, the teardown below still runs
+  } else if (rank == 0) {
     // ================================================================ score CTA
     if (warp == 0 || warp == 2 || (kSparse && warp == 3)) {
       // ---------------------------------------------------- K tile producers
@@ -219,8 +227,12 @@ __global__ void __maxnreg__(224)
         bool ok = true;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           int32_t nid[4];  // sparse: the next tile's indices, requested one tile ahead
-          const int n_slots = kSparse ? meta_seq(meta, p.num_parts, q)[kSKeys] : 0;
-          if constexpr (kSparse) load_idx4(p, q, t0, lane, n_slots, nid);
+          const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
+          const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
+          const int32_t* bt_row = kSparse ? nullptr : bt_row_of(p, q);
+          int32_t fallback = -2;  // sparse: first row the query names, found when a tile names none
+          if constexpr (kSparse) load_idx4(p, q, t0, lane, keys, nid);
+          else if (pw == 0) check_seq_keys(p, q, keys);
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
             int32_t y[4];
@@ -228,17 +240,12 @@ __global__ void __maxnreg__(224)
               int32_t id[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) id[i] = nid[i];
-              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, n_slots, nid);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const bool valid = id[i] >= 0 && static_cast<int64_t>(id[i]) < p.s_kv;
-                if (!valid && id[i] != -1 && p.err && pw == 0) atomicOr(p.err, MLA_DEVERR_BAD_INDEX);
-                y[i] = valid ? id[i] : 0;
-              }
+              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, keys, nid);
+              sparse_rows4(p, id, lane, idx_row, keys, pw == 0, &fallback, y);
             } else {
 #pragma unroll
               for (int h2 = 0; h2 < 2; ++h2) {
-                int32_t blk = page_of(p, q, 2 * t + h2);
+                int32_t blk = page_of(p, bt_row, keys, 2 * t + h2);
                 if (blk < 0) {
                   if (p.err && pw == 0) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
                   blk = static_cast<int32_t>(p.num_pages);  // out of range: TMA fills zeros
@@ -602,8 +609,11 @@ __global__ void __maxnreg__(224)
         bool ok = true;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           int32_t nid[4];  // sparse: the next tile's indices, requested one tile ahead
-          const int n_slots = kSparse ? meta_seq(meta, p.num_parts, q)[kSKeys] : 0;
-          if constexpr (kSparse) load_idx4(p, q, t0, lane, n_slots, nid);
+          const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
+          const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
+          const int32_t* bt_row = kSparse ? nullptr : bt_row_of(p, q);
+          int32_t fallback = -2;
+          if constexpr (kSparse) load_idx4(p, q, t0, lane, keys, nid);
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
             int32_t y[4];
@@ -611,13 +621,12 @@ __global__ void __maxnreg__(224)
               int32_t id[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) id[i] = nid[i];
-              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, n_slots, nid);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) y[i] = (id[i] >= 0 && static_cast<int64_t>(id[i]) < p.s_kv) ? id[i] : 0;
+              if (t + 1 < t1) load_idx4(p, q, t + 1, lane, keys, nid);
+              sparse_rows4(p, id, lane, idx_row, keys, false, &fallback, y);
             } else {
 #pragma unroll
               for (int h2 = 0; h2 < 2; ++h2) {
-                int32_t blk = page_of(p, q, 2 * t + h2);
+                int32_t blk = page_of(p, bt_row, keys, 2 * t + h2);
                 if (blk < 0) blk = static_cast<int32_t>(p.num_pages);
                 y[h2] = blk * kPage;
               }
@@ -783,8 +792,11 @@ __global__ void __maxnreg__(224)
                 float v[32];
                 tmem_ld32(t_o + 64 * blk + 32 * h2, v);
                 tmem_wait_ld();
+                // a row without keys (inv_l = 0) is written as exact zeros: its O
+                // may hold products of zero weights with rows nobody named
 #pragma unroll
-                for (int i = 0; i < 16; ++i) pk[16 * h2 + i] = pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
+                for (int i = 0; i < 16; ++i)
+                  pk[16 * h2 + i] = inv_l != 0.f ? pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l) : 0u;
               }
 #pragma unroll
               for (int u = 0; u < 8; ++u)
@@ -805,6 +817,10 @@ __global__ void __maxnreg__(224)
               float v[32];
               tmem_ld32(t_o + 32 * blk, v);
               tmem_wait_ld();
+              if (inv_l == 0.f) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+              }
 #pragma unroll
               for (int u = 0; u < 8; ++u)
                 st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) << 4), __float_as_uint(v[4 * u] * inv_l),

@@ -16,7 +16,9 @@
 //      nothing is split and the combine has nothing to merge.
 // A decode kernel walks B when B's longest part costs at most its own split
 // penalty more than A's balanced part: every extra piece pays a Q load and
-// an epilogue, and every split row a combine read.
+// an epilogue, and every split row a combine read.  The metadata is read-only
+// for the decode kernels; the schedule a call walked is recorded in that
+// call's workspace (workspace_ctrl) for the combine.
 #pragma once
 
 #include <cstdint>
@@ -32,15 +34,13 @@ namespace mla {
 constexpr int kTileTokens = 128;
 constexpr int kFixedCost = 2;  // a piece switch (Q load, epilogue) costs about two tiles
 constexpr int32_t kMetaMagic = 0x4D4C4131;  // "MLA1"
-constexpr int32_t kMetaVersion = 2;
+constexpr int32_t kMetaVersion = 3;
 
-// header words (kHMaxCost: the largest single-sequence cost; kHChosen, in
-// schedule A's header only: the schedule the last decode kernel walked,
-// 0 = A, 1 = B, written by that kernel for the combine; kHGroups: the number
-// of groups of schedule A, 1 or s_q)
+// header words (kHMaxCost: the largest single-sequence cost; kHReserved: 0;
+// kHGroups: the number of groups of schedule A, 1 or s_q)
 enum : int {
   kHMagic = 0, kHVersion, kHNSeq, kHParts, kHTile, kHSq, kHBatch, kHCausal, kHTopk,
-  kHTotalSplits, kHPerPart, kHMaxCost, kHChosen, kHGroups, kHeaderWords = 16
+  kHTotalSplits, kHPerPart, kHMaxCost, kHReserved, kHGroups, kHeaderWords = 16
 };
 // q_begin, t_begin, q_end, t_end, split_begin, q_step, 0, 0: the part walks
 // sequences q_begin, q_begin + q_step, ... (q_step = the number of groups)
@@ -218,6 +218,21 @@ MLA_HD bool next_piece(const int32_t* meta, int num_parts, PartCursor* c, int* q
     c->q += c->step; c->t = 0; c->split = 0;
   }
   return false;
+}
+
+// True when the header of `meta` describes the call: the same magic and
+// version, sequence count, part count, tile size, tokens per request and
+// batch; for sparse calls (topk > 0) the same topk, for dense calls topk 0
+// and the same causal flag.  A decode kernel that gets metadata built for
+// another shape would index q, out and the page table with that shape's
+// sequence numbers, so the kernels check this before touching any input.
+MLA_HD bool meta_header_matches(const int32_t* meta, int batch, int s_q, int num_parts, int topk,
+                                int causal) {
+  if (meta[kHMagic] != kMetaMagic || meta[kHVersion] != kMetaVersion) return false;
+  if (meta[kHNSeq] != batch * s_q || meta[kHParts] != num_parts || meta[kHTile] != kTileTokens)
+    return false;
+  if (meta[kHSq] != s_q || meta[kHBatch] != batch || meta[kHTopk] != topk) return false;
+  return topk > 0 || meta[kHCausal] == (causal ? 1 : 0);
 }
 
 }  // namespace mla

@@ -17,19 +17,19 @@
 // (the seesaw in the FlashMLA deep dive exists because WGMMA keeps O in
 // registers).
 //
-// Roles (640 threads):
-//   warp 0 lane 0  : producer: TMA loads of Q (once per piece) and of each
-//                    tile's 9 column chunks (two 64-token pages per chunk);
-//                    FP8 cache: the raw codes and scales of the latent chunks
-//                    (staged inside their slots) and the bf16 RoPE chunk, and
-//                    with two head blocks the copy of every converted chunk
-//                    into the peer CTA
-//   warp 1         : TMEM allocation; lane 0 issues every MMA
-//   warps 4..19    : four softmax warpgroups, query rows 16g .. 16g+15 each;
+// Roles (576 threads; 96 registers per thread: five warps share each of two
+// SM sub-partitions):
+//   warps 0..15    : four softmax warpgroups, query rows 16g .. 16g+15 each;
 //                    FP8 cache: before each tile's scores they also convert
 //                    the staged codes to bf16 in place (one 16-code unit per
 //                    thread per chunk)
-//   warps 2..3     : idle
+//   warp 16        : producer (lane 0; sparse: all lanes gather): TMA loads of
+//                    Q (once per piece) and of each tile's 9 column chunks
+//                    (two 64-token pages per chunk); FP8 cache: the raw codes
+//                    and scales of the latent chunks (staged inside their
+//                    slots) and the bf16 RoPE chunk, and with two head blocks
+//                    the copy of every converted chunk into the peer CTA
+//   warp 17        : TMEM allocation; lane 0 issues every MMA
 //
 // Shared memory (1024-byte aligned): 9 KV chunk slots of [128 tok x 64 col]
 // bf16 (16 KB each, 128-byte swizzle), Q as 9 chunks of [64 rows x 64 col]
@@ -62,10 +62,10 @@ constexpr int kSmemBytes = kSmallBytes + kSmemSmall + 1024;   // + alignment sla
 static_assert(kSmemBytes <= 232448, "dynamic shared memory per CTA");
 constexpr int kSoftmaxGroups = 4;                  // warpgroups on the softmax
 constexpr int kRowsPerGroup = kRowsPerCta / kSoftmaxGroups;  // 16 query rows each
-constexpr int kThreads = 128 * (1 + kSoftmaxGroups);
-constexpr int kProducerWarp = 0;
-constexpr int kMmaWarp = 1;
-constexpr int kSoftmaxWarp0 = 4;
+constexpr int kSoftmaxWarp0 = 0;
+constexpr int kProducerWarp = 4 * kSoftmaxGroups;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 // A later tile moves the softmax reference only when a score exceeds it by
 // more than this (log2 units): probabilities stay <= 2^8, exact in range.
 constexpr float kRescaleLog2 = 8.f;
@@ -93,10 +93,12 @@ static_assert(kRawScaleOff + kRawScaleBytes <= kRawCodeOff && kRawCodeOff + kRaw
               "staging fits in the slot");
 
 struct SplitParams {
-  int32_t* meta;  // the kernels record the schedule they walk (header word kHChosen)
+  const int32_t* meta;     // schedule metadata (read-only)
+  int32_t* ws_ctrl;        // workspace control words: [0] = the schedule walked (for the combine)
   const int32_t* block_table;
-  int64_t bt_stride;
+  int64_t bt_stride;       // dense: int32 entries per block-table row (page slots of a request)
   int64_t num_pages;       // dense: pages in the cache
+  const int32_t* cache_seqlens;  // dense: [batch] lengths, checked against the metadata's key counts
   const int32_t* indices;  // sparse: [n_seq, topk]
   const float* attn_sink;  // sparse, optional: [h] sink logits (out scaled by e^lse / (e^lse + e^sink))
   int topk;
@@ -111,6 +113,8 @@ struct SplitParams {
   uint32_t* err;
   int h;
   int s_q;
+  int batch;
+  int causal;              // dense: causal flag of the call (checked against the metadata)
   int num_parts;
   int n_hblk;
   int rows;                // query rows loaded per CTA (min(h, 64))
@@ -224,13 +228,97 @@ __device__ __forceinline__ void load_bcast32(const float* src, float (&dst)[32])
   }
 }
 
-// Physical page of logical page `pg` of the sequence, or -1 if out of range.
-__device__ __forceinline__ int32_t page_of(const SplitParams& p, int q, int pg) {
-  const int32_t keys = meta_seq(p.meta, p.num_parts, q)[kSKeys];
+// Physical page of logical page `pg` of a sequence with `keys` keys whose
+// block-table row is `bt_row`, or -1 when there is none: the entry is outside
+// [0, num_pages), or the page slot lies past the row's bt_stride entries
+// (more keys than the row can address).  Pages past the last one of the
+// sequence (the second page of a tile's last 64-key half) map to the last.
+__device__ __forceinline__ int32_t page_of(const SplitParams& p, const int32_t* bt_row, int32_t keys,
+                                           int pg) {
   const int last = (keys - 1) / kPage;
-  const int32_t* bt_row = p.block_table + static_cast<int64_t>(q / p.s_q) * p.bt_stride;
-  const int32_t blk = bt_row[pg < last ? pg : last];
+  const int slot = pg < last ? pg : last;
+  if (static_cast<int64_t>(slot) >= p.bt_stride) return -1;
+  const int32_t blk = bt_row[slot];
   return (blk < 0 || static_cast<int64_t>(blk) >= p.num_pages) ? -1 : blk;
+}
+
+// Block-table row of sequence q (request q / s_q).
+__device__ __forceinline__ const int32_t* bt_row_of(const SplitParams& p, int q) {
+  return p.block_table + static_cast<int64_t>(q / p.s_q) * p.bt_stride;
+}
+
+// Dense: flags MLA_DEVERR_METADATA when the metadata's key count for sequence
+// q differs from the one cache_seqlens and the causal flag give (metadata
+// computed from other lengths).  The kernels keep walking the metadata's
+// tiles; page_of keeps every block-table read inside its row.
+__device__ __forceinline__ void check_seq_keys(const SplitParams& p, int q, int32_t keys) {
+  if (!p.cache_seqlens) return;
+  const int32_t want = seq_keys(p.cache_seqlens, q / p.s_q, q % p.s_q, p.s_q, p.causal, 0);
+  if (want != keys && p.err) atomicOr(p.err, MLA_DEVERR_METADATA);
+}
+
+// Sparse: the first index among a query's n_slots index slots that names a
+// pool row (warp-wide; every lane gets it), or 0 when there is none.
+// Invalid slots are loaded from a row the query does name, so a masked slot
+// (weight 0) never multiplies a row the caller did not ask for: 0 * NaN is
+// NaN, and rows the query does not name may hold anything.
+__device__ __forceinline__ int32_t first_valid_index(const int32_t* idx_row, int n_slots, int64_t s_kv,
+                                                     int lane) {
+  for (int base = 0; base < n_slots; base += 32) {
+    const int slot = base + lane;
+    const int32_t id = slot < n_slots ? idx_row[slot] : -1;
+    const uint32_t m = __ballot_sync(0xffffffffu, id >= 0 && static_cast<int64_t>(id) < s_kv);
+    if (m) return __shfl_sync(0xffffffffu, id, __ffs(m) - 1);
+  }
+  return 0;
+}
+
+// Sparse: the pool rows a warp loads for one 128-slot tile, lane L owning
+// slots 4L .. 4L + 3 (id: the index list entries, -1 past the key count).
+// Slots that name no row (-1, out of range) take the first row named in the
+// tile, or, in a tile with none, the first row the query names (found by a
+// scan of its list, `fallback`, computed once and cached in *fallback_cache,
+// -2 = not yet known).  Out-of-range entries other than -1 set
+// MLA_DEVERR_BAD_INDEX (when `flag`).
+__device__ __forceinline__ void sparse_rows4(const SplitParams& p, const int32_t (&id)[4], int lane,
+                                             const int32_t* idx_row, int n_slots, bool flag,
+                                             int32_t* fallback_cache, int32_t (&y)[4]) {
+  bool valid[4];
+  int32_t first = -1;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    valid[i] = id[i] >= 0 && static_cast<int64_t>(id[i]) < p.s_kv;
+    if (!valid[i] && id[i] != -1 && flag && p.err) atomicOr(p.err, MLA_DEVERR_BAD_INDEX);
+    if (valid[i] && first < 0) first = id[i];
+  }
+  const uint32_t any = __ballot_sync(0xffffffffu, first >= 0);
+  int32_t sub;
+  if (any) {
+    sub = __shfl_sync(0xffffffffu, first, __ffs(any) - 1);
+  } else {
+    if (*fallback_cache == -2) *fallback_cache = first_valid_index(idx_row, n_slots, p.s_kv, lane);
+    sub = *fallback_cache;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) y[i] = valid[i] ? id[i] : sub;
+}
+
+// FP8 cache: 16 e4m3 codes of token dq_r (unit dq_u of a 64-code chunk) times
+// their fp32 scale, rounded to bf16, into the chunk's 128-byte-swizzled row
+// `row` (shared memory).  Kept out of line: inlined into the softmax loop it
+// pushed that loop past the 96 registers a thread of this kernel may hold.
+__device__ __noinline__ void convert_unit(uint32_t row, int dq_r, int dq_u, uint4 codes, float sc) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t w0 = half ? codes.z : codes.x, w1 = half ? codes.w : codes.y;
+    const float2 a0 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xFFFFu)));
+    const float2 a1 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)));
+    const float2 a2 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xFFFFu)));
+    const float2 a3 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16)));
+    st_shared_v4(row + ((2 * dq_u + half) ^ (dq_r & 7)) * 16, pack_bf16x2(a0.x * sc, a0.y * sc),
+                 pack_bf16x2(a1.x * sc, a1.y * sc), pack_bf16x2(a2.x * sc, a2.y * sc),
+                 pack_bf16x2(a3.x * sc, a3.y * sc));
+  }
 }
 
 template <KvMode kMode>
@@ -250,12 +338,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int part = blockIdx.x / p.n_hblk;
   const int hb = blockIdx.x % p.n_hblk;
+  // The metadata must describe this call; otherwise nothing is read or written.
+  const bool meta_ok = meta_header_matches(p.meta, p.batch, p.s_q, p.num_parts, p.topk, p.causal);
   // Schedule B (whole sequences) only when nearly balanced: a tile of this
   // kernel takes ~3-6 us, so the ~26 us that splitting costs is ~4 tiles.
   constexpr int kSplitPenalty = 4;
-  const int32_t* meta = schedule_for(p.meta, kSplitPenalty);
-  if (blockIdx.x == 0 && threadIdx.x == 0)  // read by the combine after this grid
-    p.meta[kHChosen] = meta == p.meta ? 0 : 1;
+  const int32_t* meta = meta_ok ? schedule_for(p.meta, kSplitPenalty) : p.meta;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // read by the combine after this grid: the schedule walked, or -1 when
+    // the metadata was rejected (the combine then writes nothing)
+    p.ws_ctrl[0] = meta_ok ? (meta == p.meta ? 0 : 1) : -1;
+    if (!meta_ok && p.err) atomicOr(p.err, MLA_DEVERR_METADATA);
+  }
 
   // ---- setup: barriers, TMEM, zeroed padding rows of Q
   // FP8 with two head blocks: each CTA converts half of the latent chunks
@@ -314,7 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm->tmem_base;
   volatile uint32_t* abort_flag = &sm->abort;
 
-  if (kMode == KvMode::kPagedFp8 && warp == kProducerWarp) {
+  if (!meta_ok) {
+    // nothing to do: every role is skipped, the teardown below still runs
+  } else if (kMode == KvMode::kPagedFp8 && warp == kProducerWarp) {
     // ===================================================== producer (FP8)
     // Lane 0 loads Q, the bf16 RoPE columns (chunk 8) and, for every latent
     // chunk this CTA converts, the raw e4m3 codes and token scales by TMA into
@@ -338,11 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kChunks; ++c)
           tma_load_2d(q_base + c * kQChunkBytes, &tm_q, c * 64, q_row, smem_u32(&sm->q_full),
                       l2_policy_evict_last());
+        const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
+        const int32_t* bt_row = bt_row_of(p, q);
+        check_seq_keys(p, q, keys);
         for (int t = t0; t < t1 && ok; ++t) {
           const uint32_t par = (tile_ctr & 1) ^ 1;
           int32_t blk[2];
           for (int h2 = 0; h2 < 2; ++h2) {
-            blk[h2] = page_of(p, q, 2 * t + h2);
+            blk[h2] = page_of(p, bt_row, keys, 2 * t + h2);
             if (blk[h2] < 0) {
               if (p.err) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
               blk[h2] = 0;  // read a valid page; the bad page's keys are wrong but finite
@@ -436,16 +535,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
       const int32_t n_slots = meta_seq(meta, p.num_parts, q)[kSKeys];  // topk or topk_length
+      int32_t fallback = -2;  // first row the query names, found when a tile names none
       for (int t = t0; t < t1 && ok; ++t) {
-        int32_t rid[4];
+        int32_t id[4], rid[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int slot = t * kTileTokens + 4 * lane + i;
-          const int32_t id = slot < n_slots ? idx_row[slot] : -1;
-          const bool valid = id >= 0 && static_cast<int64_t>(id) < p.s_kv;
-          if (!valid && id != -1 && p.err) atomicOr(p.err, MLA_DEVERR_BAD_INDEX);
-          rid[i] = valid ? id : 0;
+          id[i] = slot < n_slots ? idx_row[slot] : -1;
         }
+        sparse_rows4(p, id, lane, idx_row, n_slots, true, &fallback, rid);
         const uint32_t par = (tile_ctr & 1) ^ 1;
         for (int c = 0; c < kChunks; ++c) {
           if (lane == 0) {
@@ -498,11 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_l2(p.q + (static_cast<int64_t>(nq) * p.h + hb * kRowsPerCta) * 576,
                         p.rows * 1152);
         }
+        const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
+        const int32_t* bt_row = bt_row_of(p, q);
+        check_seq_keys(p, q, keys);
         for (int t = t0; t < t1 && ok; ++t) {
           int32_t y[2];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            int32_t blk = page_of(p, q, 2 * t + h2);
+            int32_t blk = page_of(p, bt_row, keys, 2 * t + h2);
             if (blk < 0) {
               if (p.err) atomicOr(p.err, MLA_DEVERR_BAD_PAGE);
               blk = static_cast<int32_t>(p.num_pages);  // out of range: TMA fills zeros
@@ -610,7 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // weights the PV MMA multiplies (to normalise O), so a stale reference
     // leaves no coherent gain error on the output (flash-attention sparse-MLA
     // article: summing the bf16-rounded p brings the row gain to the noise
-    // floor).  Sums stay per lane until the piece ends.
+    // floor).  Each tile's 16 x 32 per-lane values are reduce-scattered over
+    // the warp, so lane l keeps only the running sums of row l & 15 over the
+    // warp's tokens; the four warps' sums meet in shared memory at the end.
     constexpr int R = kRowsPerGroup;
     const int g = (warp - kSoftmaxWarp0) >> 2;  // rows R*g .. R*g + R-1
     const int wq = warp & 3;                    // TMEM lane quarter
@@ -638,10 +741,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_true = NEG_INF;  // running max of row R*g + (lane & 15) (-inf: no key yet)
       float m_use = 0.f;       // reference the probabilities are taken against
       float m_low = NEG_INF;   // smallest m_true over the warpgroup's rows
-      float lp[R];             // this lane's share of sum p (fp32)
-      float lb[R];             // this lane's share of sum bf16(p)
-#pragma unroll
-      for (int i = 0; i < R; ++i) { lp[i] = 0.f; lb[i] = 0.f; }
+      float lsum = 0.f;        // sum p of row R*g + (lane & 15) over this warp's tokens
+      float bsum = 0.f;        // sum bf16(p) of the same row
       for (int t = t0; t < t1; ++t) {
         if constexpr (kMode == KvMode::kPagedFp8) {
           // ---- FP8: convert this tile's owned latent chunks in place.  Thread
@@ -649,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the named barrier before any bf16 write lands on it.  Every exit
           // is decided at a barrier, so all 16 warps leave together.
           const int own0 = share ? hb : 0, own_step = share ? 2 : 1;
+#pragma unroll 1
           for (int c = own0; c < kChunks - 1; c += own_step) {
             if (lane == 0 && ok) ok = mbar_wait(smem_u32(&sm->raw_full[c]), tile_ctr & 1, abort_flag, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -657,18 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float sc = ld_shared_f32(slot + kRawScaleOff + dq_r * 16 + (c >> 1) * 4);
             ok = !named_barrier_or(kDequantBarrier, 128 * kSoftmaxGroups, !ok);
             if (!ok) break;
-            const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-            uint32_t packed[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu)));
-              const float2 b2 = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16)));
-              packed[2 * i] = pack_bf16x2(a.x * sc, a.y * sc);
-              packed[2 * i + 1] = pack_bf16x2(b2.x * sc, b2.y * sc);
-            }
-            const uint32_t row = slot + dq_r * 128;
-            st_shared_v4(row + ((2 * dq_u) ^ (dq_r & 7)) * 16, packed[0], packed[1], packed[2], packed[3]);
-            st_shared_v4(row + ((2 * dq_u + 1) ^ (dq_r & 7)) * 16, packed[4], packed[5], packed[6], packed[7]);
+            convert_unit(slot + dq_r * 128, dq_r, dq_u, codes, sc);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm->full[c]));
@@ -689,10 +780,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t id = idx_row[tok];
           valid = id >= 0 && static_cast<int64_t>(id) < p.s_kv;
         }
-        const float mul = valid ? p.scale_log2 : 0.f;
-        const float add = valid ? 0.f : NEG_INF;
+        // masked keys: -inf by selection, so a non-finite score of a masked
+        // row cannot leak into the max or the sums
 #pragma unroll
-        for (int i = 0; i < R; ++i) x[i] = fmaf(x[i], mul, add);
+        for (int i = 0; i < R; ++i) x[i] = valid ? x[i] * p.scale_log2 : NEG_INF;
         bool full = true;
         if (t != t0) {
           float u = x[0];
@@ -725,12 +816,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           if (t != t0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-            for (int i = 0; i < R; i += 4) {
-              const float4 a4 = *reinterpret_cast<const float4*>(bc_a + i);
-              lp[i] *= a4.x; lp[i + 1] *= a4.y; lp[i + 2] *= a4.z; lp[i + 3] *= a4.w;
-              lb[i] *= a4.x; lb[i + 1] *= a4.y; lb[i + 2] *= a4.z; lb[i + 3] *= a4.w;
-            }
+            lsum *= alpha;  // this lane's row is row = lane & 15, whose factor is alpha
+            bsum *= alpha;
             // PV of the previous tile completed before s_full of this tile
             // fired (one thread's tcgen05 operations complete in order)
 #pragma unroll 1
@@ -751,6 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // probabilities against the reference; P^T row r, rows R*g .. R*g+R-1
         // -> 16-byte units 2g, 2g+1 (swizzled)
         const uint32_t prow = p_slot + r * 128;
+        float tp[R], tb[R];  // this tile's p and bf16(p) of the lane's token, per row
 #pragma unroll
         for (int cu = 0; cu < 2; ++cu) {
           const float4 m0 = *reinterpret_cast<const float4*>(bc_m + 8 * cu);
@@ -764,10 +852,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             pk[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
-            lp[8 * cu + 2 * k] += e[2 * k];
-            lp[8 * cu + 2 * k + 1] += e[2 * k + 1];
-            lb[8 * cu + 2 * k] += __uint_as_float(pk[k] << 16);
-            lb[8 * cu + 2 * k + 1] += __uint_as_float(pk[k] & 0xFFFF0000u);
+            tp[8 * cu + 2 * k] = e[2 * k];
+            tp[8 * cu + 2 * k + 1] = e[2 * k + 1];
+            tb[8 * cu + 2 * k] = __uint_as_float(pk[k] << 16);
+            tb[8 * cu + 2 * k + 1] = __uint_as_float(pk[k] & 0xFFFF0000u);
           }
           const uint32_t unit = static_cast<uint32_t>((2 * g + cu) ^ (r & 7));
           st_shared_v4(prow + unit * 16, pk[0], pk[1], pk[2], pk[3]);
@@ -776,13 +864,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
+        lsum += warp_sum_scatter16(tp, lane);  // row lane & 15, this warp's 32 tokens
+        bsum += warp_sum_scatter16(tb, lane);
         ++tile_ctr;
       }
       if (!ok) break;
       // ---- epilogue: O^T / sum bf16(p) -> out (one split) or fp32 partial
       const int row = lane & (R - 1);
-      float lsum = warp_sum_scatter16(lp, lane);  // this warp's tokens, row R*g + row
-      float bsum = warp_sum_scatter16(lb, lane);
       if (lane < R) {
         sm->red_sum[g][wq][lane] = lsum;
         sm->red_bsum[g][wq][lane] = bsum;
@@ -806,31 +894,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         inv_l *= attn_sink_factor(lse_v, p.attn_sink[hb * kRowsPerCta + R * g + row]);
       if (lane < R) bc_a[lane] = inv_l;
       __syncwarp();
-      float il[R];
-#pragma unroll
-      for (int i = 0; i < R; i += 4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(bc_a + i);
-        il[i] = t4.x; il[i + 1] = t4.y; il[i + 2] = t4.z; il[i + 3] = t4.w;
-      }
+      const volatile float* il = bc_a;  // 1 / sum of row i, read per store (broadcast)
       const int row0 = hb * kRowsPerCta + R * g;  // first head of this warpgroup
       const int split_row = srec[kSSplitOff] + split;
       const int b = q / p.s_q, j = q % p.s_q;
+      // h is a multiple of 16, so a warpgroup's 16 rows are all heads or all padding
+      if (row0 < p.h) {
 #pragma unroll 1
-      for (int m = 0; m < 4; ++m) {
-        float o[32];
-        tmem_ld32(t_o + 64 * m, o);
-        tmem_wait_ld();
-        const int d = 128 * m + 32 * wq + lane;
-        if (final_out) {
-          __nv_bfloat16* dst = p.out + (static_cast<int64_t>(q) * p.h + row0) * kDv + d;
+        for (int m = 0; m < 4; ++m) {
+          float o[R];  // O^T rows d of block m, columns = this warpgroup's 16 query rows
+          tmem_ld16(t_o + 64 * m, o);
+          tmem_wait_ld();
+          const int d = 128 * m + 32 * wq + lane;
+          // a row without keys (il = 0) is written as exact zeros: its O may
+          // hold products of zero weights with rows nobody named
+          if (final_out) {
+            __nv_bfloat16* dst = p.out + (static_cast<int64_t>(q) * p.h + row0) * kDv + d;
 #pragma unroll
-          for (int i = 0; i < R; ++i)
-            if (row0 + i < p.h) dst[static_cast<int64_t>(i) * kDv] = __float2bfloat16_rn(o[i] * il[i]);
-        } else {
-          float* dst = p.ws_o + (static_cast<int64_t>(split_row) * p.h + row0) * kDv + d;
+            for (int i = 0; i < R; ++i) {
+              const float f = il[i];
+              dst[i * kDv] = __float2bfloat16_rn(f != 0.f ? o[i] * f : 0.f);
+            }
+          } else {
+            float* dst = p.ws_o + (static_cast<int64_t>(split_row) * p.h + row0) * kDv + d;
 #pragma unroll
-          for (int i = 0; i < R; ++i)
-            if (row0 + i < p.h) dst[static_cast<int64_t>(i) * kDv] = o[i] * il[i];
+            for (int i = 0; i < R; ++i) {
+              const float f = il[i];
+              dst[i * kDv] = f != 0.f ? o[i] * f : 0.f;
+            }
+          }
         }
       }
       if (wq == 0 && lane < R && row0 + lane < p.h) {

@@ -1,7 +1,12 @@
 """GPU parity of the dense paged decode against the fp64 oracle (through the C ABI).
 
 Tolerances: bf16 out rel-L2 <= 3e-3 and max-abs <= 2e-2 * RMS(out_ref),
-LSE abs error <= 1e-3; gathers (single-key rows) bit-exact.
+LSE abs error <= 1e-3.  The block-table gather is checked bit-exactly: in the
+probe tests each query row is built so that one cached token outweighs every
+other by more than 2^-150 (all other weights are exactly 0 in fp32), so the
+output row must be that token's V row, bit for bit; every token position of
+every request (every block-table entry, every slot of a page, the partial
+last page) is addressed by some row.
 """
 import numpy as np
 import pytest
@@ -132,14 +137,20 @@ def test_empty_sequences():
     assert_parity(res["out"][2], ref_o[2], res["lse"][2], ref_l[2], "empty/nonempty")
 
 
-def test_bad_page_ids_are_flagged_not_faulted():
-    w = workloads.Workload("badpage", "dense", b=2, s_q=1, h=16, seqlens=(100, 200), seed=17)
+@pytest.mark.parametrize("h", [16, 128])
+def test_bad_page_ids_are_flagged_not_faulted(h):
+    """Bad page ids in two requests are flagged and read as nothing outside the
+    cache; the third request, whose pages are all valid, is unaffected."""
+    w = workloads.Workload("badpage", "dense", b=3, s_q=1, h=h, seqlens=(100, 200, 300), seed=17)
     inp = workloads.make_inputs(w)
+    good = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in inp.items()}
     inp["block_table"][1, 1] = 10 ** 6      # past the cache
     inp["block_table"][0, 0] = -5
     res = run_dense(inp)
     assert res["err"] & binding.MLA_DEVERR_BAD_PAGE
     assert np.all(np.isfinite(res["out"]))
+    ref_o, ref_l = oracle_dense(good, rows=[(2, 0)])
+    assert_parity(res["out"][2], ref_o[2], res["lse"][2], ref_l[2], "request with valid pages")
 
 
 def test_repeat_calls_are_deterministic():
@@ -166,7 +177,7 @@ def test_kernels_record_the_schedule_they_walk(h, parts, walked):
     binding.mla_decode(q, kv, binding.MLA_KV_BF16, bt, sl, inp["softmax_scale"], True, buf.metadata,
                        parts, buf.workspace, buf.out, buf.lse, buf.err)
     torch.cuda.synchronize()
-    assert int(buf.metadata[12].item()) == walked
+    assert int(workspace_ctrl(buf)[0]) == walked
     ref_o, ref_l = oracle_dense(inp)
     assert_parity(buf.out.float().cpu().numpy(), ref_o, buf.lse.cpu().numpy(), ref_l, f"h={h} parts={parts}")
 
@@ -184,31 +195,32 @@ def test_device_metadata_matches_host_mirror(batch):
         assert np.array_equal(meta.cpu().numpy(), host)
 
 
-def test_full_size_dense_v3_sampled_rows():
-    """b=64, h=128, t=4096 in the bench's launch configuration; 6 requests checked."""
+def test_full_size_dense_v3_all_rows():
+    """b=64, h=128, t=4096 in the bench's launch configuration; every request
+    and head compared with the oracle, and each request on its own."""
     w = workloads.WORKLOADS["dense_v3"]
     inp = workloads.make_inputs(w)
     res = run_dense(inp)
-    rows = [(0, 0), (1, 0), (17, 0), (31, 0), (50, 0), (63, 0)]
-    ref_o, ref_l = oracle_dense(inp, rows=rows)
-    for b, j in rows:
-        assert_parity(res["out"][b, j], ref_o[b, j], res["lse"][b, :, j], ref_l[b, :, j],
-                      f"dense_v3 row {b}")
+    ref_o, ref_l = oracle_dense(inp)
+    assert_parity(res["out"], ref_o, res["lse"], ref_l, "dense_v3 (all rows)")
+    for b in range(w.b):
+        assert_parity(res["out"][b], ref_o[b], res["lse"][b], ref_l[b], f"dense_v3 request {b}")
     assert res["err"] == 0
-    assert np.all(np.isfinite(res["out"]))
 
 
-def test_full_size_spec_decode_sampled_rows():
-    """b=128, s_q=2 causal, lengths U[1024, 16384]: sampled query tokens of both positions."""
+def test_full_size_spec_decode_all_rows():
+    """b=128, s_q=2 causal, lengths U[1024, 16384]: every query token of both
+    positions and every head compared with the oracle."""
     w = workloads.WORKLOADS["spec"]
     inp = workloads.make_inputs(w)
     res = run_dense(inp, causal=True)
-    rows = [(0, 0), (0, 1), (47, 1), (90, 0), (127, 1)]
-    ref_o, ref_l = oracle_dense(inp, causal=True, rows=rows)
-    for b, j in rows:
-        assert_parity(res["out"][b, j], ref_o[b, j], res["lse"][b, :, j], ref_l[b, :, j],
-                      f"spec row {b},{j}")
-    assert res["err"] == 0 and np.all(np.isfinite(res["out"]))
+    ref_o, ref_l = oracle_dense(inp, causal=True)
+    assert_parity(res["out"], ref_o, res["lse"], ref_l, "spec (all rows)")
+    for b in range(w.b):
+        for j in range(w.s_q):
+            assert_parity(res["out"][b, j], ref_o[b, j], res["lse"][b, :, j], ref_l[b, :, j],
+                          f"spec token {b},{j}")
+    assert res["err"] == 0
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
@@ -227,3 +239,182 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     ref_o, ref_l = oracle_dense(inp)
     assert_parity(res["out"], ref_o, res["lse"], ref_l, "after timeout check")
     assert res["err"] == 0
+
+
+def workspace_ctrl(buf):
+    """The workspace's control words (int32), after the partial O and LSE rows."""
+    rows = (buf.batch * buf.s_q + buf.num_sm_parts) * buf.h_q
+    return buf.workspace[rows * 513:].view(torch.int32).cpu().numpy()
+
+
+# ---------------------------------------------------------------- gather probes
+
+ROPE_GAIN = 256.0  # q's RoPE part = ROPE_GAIN * the target key's RoPE signs (exact in bf16)
+
+
+def probe_cache(seqlens, extra_pages, seed):
+    """A paged cache whose RoPE columns are random +-1 signs (latent columns
+    N(0,1) bf16), with a shuffled block table.  Returns (kv [pages, 64, 576]
+    bf16, block_table [b, max_pages] int32)."""
+    g = torch.Generator().manual_seed(seed)
+    n_pages = [(L + 63) // 64 for L in seqlens]
+    total = sum(n_pages) + extra_pages
+    perm = torch.randperm(total, generator=g).to(torch.int32)
+    bt = torch.full((len(seqlens), max(n_pages)), -1, dtype=torch.int32)
+    pos = 0
+    for i, n in enumerate(n_pages):
+        bt[i, :n] = perm[pos:pos + n]
+        pos += n
+    kv = torch.randn((total, 64, 576), generator=g).to(torch.bfloat16)
+    signs = torch.randint(0, 2, (total, 64, 64), generator=g).to(torch.float32) * 2 - 1
+    kv[:, :, 512:] = signs.to(torch.bfloat16)
+    return kv, bt
+
+
+def probe_queries(kv, bt, seqlens, h, rnd):
+    """Query rows for round `rnd`: head hh of request b targets token
+    t = rnd * h + hh (when t < seqlens[b], else a zero row).  Returns q
+    [b, 1, h, 576] bf16 and the targets [b, h] (-1 = none)."""
+    b = len(seqlens)
+    q = torch.zeros((b, 1, h, 576), dtype=torch.bfloat16)
+    tgt = torch.full((b, h), -1, dtype=torch.int64)
+    for bi, L in enumerate(seqlens):
+        t = torch.arange(rnd * h, min(L, (rnd + 1) * h))
+        if len(t) == 0:
+            continue
+        rows = kv[bt[bi, t // 64].long(), t % 64]                 # [n, 576]
+        q[bi, 0, :len(t), 512:] = (rows[:, 512:].float() * ROPE_GAIN).to(torch.bfloat16)
+        tgt[bi, :len(t)] = t
+    return q, tgt
+
+
+def assert_probe_preconditions(kv, bt, seqlens):
+    """Every other visible token's RoPE signs differ from the target's in at
+    least 3 of 64 places: its score is lower by >= 6 * 256 / sqrt(192) > 110,
+    i.e. a weight below 2^-150, exactly 0 in fp32."""
+    for bi, L in enumerate(seqlens):
+        t = torch.arange(L)
+        s = kv[bt[bi, t // 64].long(), t % 64][:, 512:].float()
+        gram = s @ s.T
+        gram.fill_diagonal_(-64)
+        assert float(gram.max()) <= 64 - 6
+
+
+def check_probe(out, lse, kv, bt, tgt, what):
+    scale = workloads.SOFTMAX_SCALE
+    for bi in range(tgt.shape[0]):
+        for hh in range(tgt.shape[1]):
+            t = int(tgt[bi, hh])
+            if t < 0:
+                continue
+            v = kv[int(bt[bi, t // 64]), t % 64, :512]
+            assert torch.equal(out[bi, 0, hh], v), f"{what}: request {bi} token {t} (head {hh})"
+            assert abs(float(lse[bi, hh, 0]) - scale * ROPE_GAIN * 64) < 1e-3, (what, bi, t)
+
+
+def run_probe(kv, bt, seqlens, h, parts=None):
+    dev_kv, dev_bt = kv.to(DEV), bt.to(DEV)
+    sl = torch.tensor(seqlens, dtype=torch.int32)
+    b = len(seqlens)
+    buf = binding.DecodeBuffers(b, 1, h, DEV, parts)
+    binding.mla_get_metadata(sl.to(DEV), b, 1, True, 0, buf.num_sm_parts, buf.metadata)
+    for rnd in range((max(seqlens) + h - 1) // h):
+        q, tgt = probe_queries(kv, bt, seqlens, h, rnd)
+        buf.out.fill_(float("nan"))
+        binding.mla_decode(q.to(DEV), dev_kv, binding.MLA_KV_BF16, dev_bt, sl.to(DEV),
+                           workloads.SOFTMAX_SCALE, True, buf.metadata, buf.num_sm_parts,
+                           buf.workspace, buf.out, buf.lse, buf.err)
+        torch.cuda.synchronize()
+        check_probe(buf.out.cpu(), buf.lse.cpu(), kv, bt, tgt, f"h={h} round {rnd}")
+    assert int(buf.err.item()) == 0
+
+
+@pytest.mark.parametrize("h,parts", [(16, None), (64, None), (128, None), (128, 5), (16, 3)])
+def test_gather_bit_exact_every_token_small_cache(h, parts):
+    """The small cache's shape (two requests of 200 and 333 tokens, 10 of 16
+    pages used, shuffled): every token position of both requests is the
+    target of one query row; its output must be the token's V row exactly."""
+    seqlens = (200, 333)
+    kv, bt = probe_cache(seqlens, 6, seed=71)
+    assert_probe_preconditions(kv, bt, seqlens)
+    run_probe(kv, bt, seqlens, h, parts)
+
+
+def test_gather_bit_exact_every_token_full_size():
+    """b=64, h=128, every request 4096 tokens, 4096 shuffled pages, in the
+    bench's launch configuration: 32 calls, call k addressing tokens
+    128k .. 128k+127 of every request (every block-table entry and slot)."""
+    seqlens = (4096,) * 64
+    kv, bt = probe_cache(seqlens, 0, seed=72)
+    assert_probe_preconditions(kv, bt, seqlens[:4])
+    run_probe(kv, bt, seqlens, 128)
+
+
+# ---------------------------------------------------------------- metadata checks
+
+@pytest.mark.parametrize("h", [64, 128])
+def test_metadata_for_another_shape_is_rejected_on_the_device(h):
+    """Metadata built for b=4 passed to a b=2 call (and metadata built for a
+    sparse call, and for the other causal flag): the kernel sets
+    MLA_DEVERR_METADATA and writes nothing."""
+    w = workloads.Workload("meta", "dense", b=2, s_q=2, h=h, seqlens=(300, 500), seed=24)
+    inp = workloads.make_inputs(w)
+    q, kv = inp["q"].to(DEV), inp["kv_cache"].to(DEV)
+    bt, sl = inp["block_table"].to(DEV), inp["cache_seqlens"].to(DEV)
+    sl4 = torch.tensor([300, 500, 700, 900], dtype=torch.int32, device=DEV)
+    big = binding.DecodeBuffers(4, 2, h, DEV)
+    cases = [("batch", lambda m: binding.mla_get_metadata(sl4, 4, 2, True, 0, big.num_sm_parts, m)),
+             ("topk", lambda m: binding.mla_get_metadata(None, 2, 2, False, 64, big.num_sm_parts, m)),
+             ("causal", lambda m: binding.mla_get_metadata(sl, 2, 2, False, 0, big.num_sm_parts, m))]
+    for name, build_meta in cases:
+        build_meta(big.metadata)
+        buf = binding.DecodeBuffers(2, 2, h, DEV, big.num_sm_parts)
+        buf.out.fill_(7.0)
+        buf.lse.fill_(7.0)
+        binding.mla_decode(q, kv, binding.MLA_KV_BF16, bt, sl, inp["softmax_scale"], True,
+                           big.metadata, big.num_sm_parts, buf.workspace, buf.out, buf.lse, buf.err)
+        torch.cuda.synchronize()
+        assert int(buf.err.item()) & binding.MLA_DEVERR_METADATA, name
+        assert torch.all(buf.out == 7.0) and torch.all(buf.lse == 7.0), name
+
+
+@pytest.mark.parametrize("h", [64, 128])
+def test_metadata_from_other_lengths_is_flagged(h):
+    """The right shape but lengths that differ from cache_seqlens: flagged,
+    no fault, and the result follows the metadata's key counts."""
+    w = workloads.Workload("meta_len", "dense", b=2, s_q=1, h=h, seqlens=(300, 500), seed=25)
+    inp = workloads.make_inputs(w)
+    q, kv = inp["q"].to(DEV), inp["kv_cache"].to(DEV)
+    bt, sl = inp["block_table"].to(DEV), inp["cache_seqlens"].to(DEV)
+    buf = binding.DecodeBuffers(2, 1, h, DEV)
+    binding.mla_get_metadata(torch.tensor([300, 260], dtype=torch.int32, device=DEV), 2, 1, True, 0,
+                             buf.num_sm_parts, buf.metadata)
+    binding.mla_decode(q, kv, binding.MLA_KV_BF16, bt, sl, inp["softmax_scale"], True, buf.metadata,
+                       buf.num_sm_parts, buf.workspace, buf.out, buf.lse, buf.err)
+    torch.cuda.synchronize()
+    assert int(buf.err.item()) == binding.MLA_DEVERR_METADATA
+    short = dict(inp)
+    short["cache_seqlens"] = torch.tensor([300, 260], dtype=torch.int32)
+    ref_o, ref_l = oracle_dense(short)
+    assert_parity(buf.out.float().cpu().numpy(), ref_o, buf.lse.cpu().numpy(), ref_l, "metadata lengths")
+
+
+@pytest.mark.parametrize("h", [64, 128])
+def test_length_beyond_the_block_table_row_is_flagged(h):
+    """A request whose length needs more page slots than block_table_stride:
+    MLA_DEVERR_BAD_PAGE, nothing read past the row, the other request exact."""
+    w = workloads.Workload("stride", "dense", b=2, s_q=1, h=h, seqlens=(300, 200), extra_pages=4, seed=26)
+    inp = workloads.make_inputs(w)
+    bt = inp["block_table"][:, :4].contiguous()          # room for 256 tokens per request
+    lens = torch.tensor([300, 200], dtype=torch.int32)   # request 0 needs 5 slots
+    q, kv = inp["q"].to(DEV), inp["kv_cache"].to(DEV)
+    buf = binding.DecodeBuffers(2, 1, h, DEV)
+    binding.mla_get_metadata(lens.to(DEV), 2, 1, True, 0, buf.num_sm_parts, buf.metadata)
+    binding.mla_decode(q, kv, binding.MLA_KV_BF16, bt.to(DEV), lens.to(DEV), inp["softmax_scale"], True,
+                       buf.metadata, buf.num_sm_parts, buf.workspace, buf.out, buf.lse, buf.err)
+    torch.cuda.synchronize()
+    assert int(buf.err.item()) & binding.MLA_DEVERR_BAD_PAGE
+    out, lse = buf.out.float().cpu().numpy(), buf.lse.cpu().numpy()
+    assert np.all(np.isfinite(out))
+    ref_o, ref_l = oracle_dense(inp, rows=[(1, 0)])
+    assert_parity(out[1], ref_o[1], lse[1], ref_l[1], "request within its row")

@@ -53,7 +53,8 @@ def test_status_strings():
 def test_sizes():
     # two schedules (A: balanced ranges, B: one whole sequence per part)
     assert binding.mla_metadata_size(64, 1, 76) == 2 * 4 * (16 + 8 * 76 + 8 * 64)
-    assert binding.mla_workspace_size(64, 1, 128, 76) == (64 + 76) * 128 * 513 * 4
+    # fp32 partial O and LSE rows, then 64 bytes of control words
+    assert binding.mla_workspace_size(64, 1, 128, 76) == (64 + 76) * 128 * 513 * 4 + 64
     with pytest.raises(binding.MlaError):
         binding.mla_workspace_size(64, 1, 100, 76)      # unsupported head count
     with pytest.raises(binding.MlaError):
@@ -333,3 +334,17 @@ def test_binding_checks_the_attention_sink():
 
 def test_wait_timeout_check_rejects_a_null_error_word():
     assert binding.lib().mla_check_wait_timeout(None, None) == -1   # MLA_ERR_NULL
+
+
+def test_binding_constants_match_the_header():
+    """The binding's status, device-error and format constants are the
+    header's #defines (a value the kernels OR into the error word must mean
+    the same thing on both sides)."""
+    import re
+    text = open(os.path.join(ROOT, "include", "mla_decode.h")).read()
+    defines = {m.group(1): int(m.group(2)) for m in
+               re.finditer(r"#define (MLA_(?:DEVERR|KV)_\w+)\s+\(?(-?\d+)u?\)?", text)}
+    assert {"MLA_DEVERR_BAD_PAGE", "MLA_DEVERR_BAD_INDEX", "MLA_DEVERR_TIMEOUT",
+            "MLA_DEVERR_METADATA", "MLA_KV_BF16", "MLA_KV_FP8_656"} <= set(defines)
+    for name, value in defines.items():
+        assert getattr(binding, name) == value, name

@@ -43,3 +43,23 @@ def test_two_ranks_take_the_slowest_time_and_add_their_units():
 def test_one_rank_is_the_identity():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.job_rate(2e9, 4.0, 1) == pytest.approx(5e11)
+
+
+def test_gpus_flag_must_match_the_launch():
+    """--gpus N is honoured only as the world size of the launch: N ranks
+    started by torchrun.  A mismatch is refused (non-zero exit), never run
+    as a different number of replicas."""
+    assert bench.check_world(1, 1) is None
+    assert bench.check_world(8, 8) is None
+    assert "WORLD_SIZE=1" in bench.check_world(8, 1)
+    assert bench.check_world(2, 4) is not None
+    assert bench.check_world(0, 1) is not None
+
+
+def test_bench_exits_non_zero_when_gpus_exceeds_the_world():
+    import subprocess
+    import sys
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, bench.__file__, "--gpus", "2", "--steps", "1"],
+                       capture_output=True, text=True, env=env, timeout=120)
+    assert r.returncode == 2 and "WORLD_SIZE=1" in r.stderr
