@@ -279,9 +279,9 @@ def probe_queries(kv, bt, seqlens, h, rnd):
     q = torch.zeros((b, 1, h, 576), dtype=torch.bfloat16)
     tgt = torch.full((b, h), -1, dtype=torch.int64)
     for bi, L in enumerate(seqlens):
-        t = torch.arange(rnd * h, min(L, (rnd + 1) * h))
-        if len(t) == 0:
+        if rnd * h >= L:
             continue
+        t = torch.arange(rnd * h, min(L, (rnd + 1) * h))
         rows = kv[bt[bi, t // 64].long(), t % 64]                 # [n, 576]
         q[bi, 0, :len(t), 512:] = (rows[:, 512:].float() * ROPE_GAIN).to(torch.bfloat16)
         tgt[bi, :len(t)] = t
@@ -301,15 +301,20 @@ def assert_probe_preconditions(kv, bt, seqlens):
 
 
 def check_probe(out, lse, kv, bt, tgt, what):
+    """Rows with a target equal that token's V row bit for bit; their lse is
+    the target's score (every other weight is exactly 0)."""
     scale = workloads.SOFTMAX_SCALE
-    for bi in range(tgt.shape[0]):
-        for hh in range(tgt.shape[1]):
-            t = int(tgt[bi, hh])
-            if t < 0:
-                continue
-            v = kv[int(bt[bi, t // 64]), t % 64, :512]
-            assert torch.equal(out[bi, 0, hh], v), f"{what}: request {bi} token {t} (head {hh})"
-            assert abs(float(lse[bi, hh, 0]) - scale * ROPE_GAIN * 64) < 1e-3, (what, bi, t)
+    bi, hh = torch.nonzero(tgt >= 0, as_tuple=True)
+    t = tgt[bi, hh]
+    want = kv[bt[bi, t // 64].long(), t % 64, :512]
+    got = out[bi, 0, hh]
+    same = torch.all(got.view(torch.int16) == want.view(torch.int16), dim=-1)
+    if not bool(torch.all(same)):
+        k = int(torch.nonzero(~same)[0])
+        raise AssertionError(f"{what}: request {int(bi[k])} token {int(t[k])} (head {int(hh[k])}) "
+                             f"is not an exact copy of its V row")
+    err = torch.abs(lse[bi, hh, 0].double() - scale * ROPE_GAIN * 64)
+    assert float(err.max()) < 1e-3, (what, float(err.max()))
 
 
 def run_probe(kv, bt, seqlens, h, parts=None):
