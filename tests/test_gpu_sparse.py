@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from mla_decode_attention_gb300 import binding, workloads
-from tests._util import assert_parity, bf16_np
+from tests._util import assert_parity, assert_parity_per_token, bf16_np
 
 pytestmark = pytest.mark.gpu
 
@@ -144,9 +144,8 @@ def test_full_size_dsa_all_rows():
     inp = workloads.make_inputs(w)
     out, lse, err = run_sparse(inp)
     ref_o, ref_l = oracle_sparse(inp)
-    assert_parity(out, ref_o, lse, ref_l, "dsa (all rows)")
-    for b in range(w.b):
-        assert_parity(out[b], ref_o[b], lse[b], ref_l[b], f"dsa token {b}")
+    st = assert_parity_per_token(out, ref_o, lse, ref_l, "dsa")
+    print("dsa parity:", st)
     assert err == 0
 
 

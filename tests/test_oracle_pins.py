@@ -407,6 +407,38 @@ def test_parity_checker_accepts_the_bf16_floor_and_rejects_real_errors():
         assert_parity(ideal, o, l + 2e-3, l, "lse")
 
 
+def test_per_token_parity_checker_scales_with_each_token():
+    """Two tokens of very different output size (4 keys vs 4000 keys): the
+    ideal bf16 output passes per token; a 1% gain on the small-valued token
+    alone, or a dropped key of the short token, fails."""
+    from tests._util import assert_parity_per_token
+    r = rng(31)
+    outs, lses = [], []
+    for n in (4, 4000):
+        q = r.standard_normal((8, 576))
+        keys = r.standard_normal((n, 576))
+        o, l = oracle.attend(q, keys, SCALE)
+        outs.append(o)
+        lses.append(l)
+    o = np.stack(outs)[:, None]                 # [2, 1, 8, 512]
+    l = np.stack(lses)[:, :, None]              # [2, 8, 1]
+    ideal = torch.from_numpy(o).to(torch.bfloat16).double().numpy()
+    assert_parity_per_token(ideal, o, l, l, "ideal bf16")
+    bad = ideal.copy()
+    bad[1] *= 1.01
+    with pytest.raises(AssertionError):
+        assert_parity_per_token(bad, o, l, l, "gain on the long token")
+    q = r.standard_normal((8, 576))
+    keys = r.standard_normal((4, 576))
+    o0, l0 = oracle.attend(q, keys, SCALE)
+    o1, l1 = oracle.attend(q, keys[1:], SCALE)
+    o[0, 0], l[0, :, 0] = o0, l0
+    drop = o.copy()
+    drop[0, 0] = o1
+    with pytest.raises(AssertionError):
+        assert_parity_per_token(torch.from_numpy(drop).to(torch.bfloat16).double().numpy(), o, l, l, "drop")
+
+
 # ------------------------------------------- attention sink and topk length
 
 def test_attention_sink_is_a_zero_valued_key_with_the_sink_as_its_score():
