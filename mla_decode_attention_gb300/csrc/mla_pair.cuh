@@ -293,8 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = pw; c < kChunks && ok; c += kIssuers) {
               const int g = c / 3;
               if (lane == 0) {
-                ok = c == 7 ? mbar_wait(smem_u32(&bars->c7empty[tc & 1]), ((tc >> 1) & 1) ^ 1, abort_flag, p.err)
-                            : mbar_wait(smem_u32(&bars->kempty[g]), (tc & 1) ^ 1, abort_flag, p.err);
+                // every chunk waits for its group's previous round to be consumed,
+                // so no arrival can land in a phase of kfull[g] before the
+                // previous phase has completed (chunk 7's own buffers are fresh
+                // for the first two tiles and would not hold it back); chunk 7
+                // also waits for its buffer's last P.V tail
+                ok = mbar_wait(smem_u32(&bars->kempty[g]), (tc & 1) ^ 1, abort_flag, p.err);
+                if (ok && c == 7)
+                  ok = mbar_wait(smem_u32(&bars->c7empty[tc & 1]), ((tc >> 1) & 1) ^ 1, abort_flag, p.err);
                 if (ok) mbar_arrive_expect_tx(smem_u32(&bars->kfull[g]), kChunk);
               }
               if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
