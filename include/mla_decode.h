@@ -40,8 +40,9 @@
  *      out    [batch, s_q, h_q, 512] bf16
  *      lse    [batch, h_q, s_q]      fp32   (transposed w.r.t. out, as in the
  *                                            FlashMLA README "Return Values")
- *  - Supported shapes: d_qk = 576, d_v = 512, page block 64 tokens,
- *    h_q in {16, 32, 48, 64, 128}, 1 <= s_q <= 16.
+ *  - Supported shapes: d_qk = 576 (512 with the V4.1 cache, MLA_KV_FP8_528),
+ *    d_v = 512, page block 64 tokens, h_q in {16, 32, 48, 64, 128},
+ *    1 <= s_q <= 16.
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
@@ -79,6 +80,13 @@ extern "C" {
                           * codes, 4 fp32 scales (one per 128 latent channels),  *
                           * 64 bf16 RoPE values (FlashMLA "Hopper FP8 sparse     *
                           * decode" note, "The FP8 KVCache Format")              */
+#define MLA_KV_FP8_528 2 /* [num_pages, 64, 528] bytes per token, DeepSeek V4.1  *
+                          * (head_dim 512): 512 e4m3 codes covering all 512      *
+                          * dimensions (RoPE ones included), then 16 e8m0        *
+                          * scales, one per 32 consecutive codes (FlashMLA       *
+                          * README, "FP8 / FP4 KV Cache Format").  Keys are 512  *
+                          * wide and the value is the whole key: q is            *
+                          * [batch, s_q, h_q, 512] and out keeps 512 columns.    */
 
 /* Human-readable name of a status code. Never NULL. */
 const char* mla_status_string(int status);
@@ -168,9 +176,11 @@ int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts, size_t* by
  * q, kvcache, block_table, cache_seqlens).  Runs the split-KV kernel and then
  * the combine kernel (programmatic dependent launch) on `stream`.
  *
- *  q            [batch, s_q, h_q, 576] bf16
+ *  q            [batch, s_q, h_q, 576] bf16 ([.., 512] with MLA_KV_FP8_528)
  *  kv_cache     MLA_KV_BF16: [num_pages, 64, 576] bf16;
- *               MLA_KV_FP8_656: [num_pages, 64, 656] uint8
+ *               MLA_KV_FP8_656: [num_pages, 64, 656] uint8;
+ *               MLA_KV_FP8_528: [num_pages, 64, 528] uint8 (the value of a
+ *               token is its whole 512-wide key)
  *  block_table  [batch, block_table_stride] int32; entry [b, p] = physical
  *               page of tokens 64p .. 64p+63 of request b.  Only the first
  *               ceil(cache_seqlens[b] / 64) entries of a row are read, and

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(HERE, "libmla_decode.so")
 
 MLA_KV_BF16 = 0
 MLA_KV_FP8_656 = 1
+MLA_KV_FP8_528 = 2
 MLA_DEVERR_BAD_PAGE = 1
 MLA_DEVERR_BAD_INDEX = 2
 MLA_DEVERR_TIMEOUT = 4
@@ -161,10 +162,24 @@ def mla_get_metadata_host(cache_seqlens, batch: int, s_q: int, causal: bool, top
 
 # ---------------------------------------------------------------- decode
 
+# query width and bytes per cached token of each cache format
+_FORMATS = {MLA_KV_BF16: (576, None), MLA_KV_FP8_656: (576, 656), MLA_KV_FP8_528: (512, 528)}
+
+
+def _check_format(q, kv_cache, kv_format):
+    if kv_format not in _FORMATS:
+        raise ValueError(f"unknown kv_format {kv_format}")
+    d_qk, token_bytes = _FORMATS[kv_format]
+    _dev(kv_cache, torch.bfloat16 if kv_format == MLA_KV_BF16 else torch.uint8, "kv_cache")
+    if q.shape[-1] != d_qk or (token_bytes is not None and kv_cache.shape[-1] != token_bytes):
+        raise ValueError(f"kv_format {kv_format} needs q [..., {d_qk}] and "
+                         f"kv_cache [..., {token_bytes or 576}]")
+
+
 def _decode_call(name, q, kv_cache, kv_format, block_table, cache_seqlens, softmax_scale,
                  causal, metadata, num_sm_parts, workspace, out, lse, err, stream):
     _dev(q, torch.bfloat16, "q")
-    _dev(kv_cache, torch.bfloat16 if kv_format == MLA_KV_BF16 else torch.uint8, "kv_cache")
+    _check_format(q, kv_cache, kv_format)
     _dev(cache_seqlens, torch.int32, "cache_seqlens")
     _dev(metadata, torch.int32, "metadata")
     _dev(out, torch.bfloat16, "out")
@@ -186,9 +201,11 @@ def mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, kv_format: int,
                causal: bool, metadata: torch.Tensor, num_sm_parts: int,
                workspace: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
                err: Optional[torch.Tensor] = None, stream=None) -> None:
-    """q [b, s_q, h, 576] bf16; kv_cache [pages, 64, 576] bf16 (MLA_KV_BF16) or
-    [pages, 64, 656] uint8 (MLA_KV_FP8_656); block_table [b, max_pages] int32;
-    cache_seqlens [b] int32; out [b, s_q, h, 512] bf16; lse [b, h, s_q] fp32."""
+    """q [b, s_q, h, 576] bf16; kv_cache [pages, 64, 576] bf16 (MLA_KV_BF16),
+    [pages, 64, 656] uint8 (MLA_KV_FP8_656) or, with q [b, s_q, h, 512],
+    [pages, 64, 528] uint8 (MLA_KV_FP8_528, V4.1); block_table [b, max_pages]
+    int32; cache_seqlens [b] int32; out [b, s_q, h, 512] bf16; lse [b, h, s_q]
+    fp32."""
     _decode_call("mla_decode", q, kv_cache, kv_format, block_table, cache_seqlens,
                  softmax_scale, causal, metadata, num_sm_parts, workspace, out, lse, err, stream)
 
@@ -209,7 +226,7 @@ def mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, kv_format: int,
     device scratch array: the caller passes only inputs and outputs.  Calls
     sharing that array must not overlap on the GPU."""
     _dev(q, torch.bfloat16, "q")
-    _dev(kv_cache, torch.bfloat16 if kv_format == MLA_KV_BF16 else torch.uint8, "kv_cache")
+    _check_format(q, kv_cache, kv_format)
     _dev(cache_seqlens, torch.int32, "cache_seqlens")
     _dev(out, torch.bfloat16, "out")
     _dev(lse, torch.float32, "lse")

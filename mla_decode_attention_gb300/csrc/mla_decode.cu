@@ -28,13 +28,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 row-major tensor [rows, 576] with row stride `stride_bytes`; boxes
-// of [box_rows x 64 columns] with 128-byte swizzle.
+// 2-D bf16 row-major tensor [rows, cols] (cols = 576, or 512 for V4.1
+// queries) with row stride `stride_bytes`; boxes of [box_rows x 64 columns]
+// with 128-byte swizzle.
 bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t stride_bytes,
-                   uint32_t box_rows) {
+                   uint32_t box_rows, uint64_t cols = kDqk) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), rows};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), rows};
   const cuuint64_t strides[1] = {stride_bytes};
   const cuuint32_t box[2] = {64u, box_rows};
   const cuuint32_t estr[2] = {1u, 1u};
@@ -162,7 +163,8 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   if (rc != MLA_OK) return rc;
   if (!q || !kv_cache || !block_table || !cache_seqlens || !metadata || !workspace || !out || !lse)
     return MLA_ERR_NULL;
-  if (kv_format != MLA_KV_BF16 && kv_format != MLA_KV_FP8_656) return MLA_ERR_UNSUPPORTED;
+  if (kv_format != MLA_KV_BF16 && kv_format != MLA_KV_FP8_656 && kv_format != MLA_KV_FP8_528)
+    return MLA_ERR_UNSUPPORTED;
   if (num_pages <= 0 || num_pages > (int64_t{1} << 25) || block_table_stride <= 0)
     return MLA_ERR_SHAPE;
   if (!(softmax_scale > 0.f) || !(softmax_scale < 1e30f)) return MLA_ERR_SHAPE;
@@ -173,11 +175,24 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   const int n_seq = batch * s_q;
   const int n_hblk = head_blocks(h_q);
   const int rows = h_q < kRowsPerCta ? h_q : kRowsPerCta;
+  // the V4.1 cache holds 512-wide keys (values are the whole key), others 576
+  const bool v41 = kv_format == MLA_KV_FP8_528;
+  const int d_qk = v41 ? kV41HeadDim : kDqk;
   CUtensorMap tm_q, tm_kv, tm_codes, tm_scales;
-  if (!make_rows_map(&tm_q, q, static_cast<uint64_t>(n_seq) * h_q, kDqk * 2, rows))
+  if (!make_rows_map(&tm_q, q, static_cast<uint64_t>(n_seq) * h_q, d_qk * 2, rows, d_qk))
     return record_error("cuTensorMapEncodeTiled failed for q", MLA_ERR_CUDA);
   const bool fp8 = kv_format == MLA_KV_FP8_656;
-  if (!fp8) {
+  if (v41) {
+    // the 512 e4m3 codes (boxes of 64 tokens x 64 codes) and the 16 e8m0
+    // scales at byte 512 (boxes of 64 tokens x 16 bytes) of every 528-byte
+    // token; no bf16 part (tm_kv is not read)
+    const uint64_t tokens = static_cast<uint64_t>(num_pages) * kPage;
+    if (!make_byte_map(&tm_codes, kv_cache, tokens, kV41HeadDim, kFp8V41TokenBytes, 64, kPage) ||
+        !make_byte_map(&tm_scales, static_cast<const uint8_t*>(kv_cache) + kV41HeadDim, tokens, 16,
+                       kFp8V41TokenBytes, 16, kPage))
+      return record_error("cuTensorMapEncodeTiled failed for the V4.1 FP8 codes or scales", MLA_ERR_CUDA);
+    tm_kv = tm_codes;
+  } else if (!fp8) {
     if (!make_rows_map(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kDqk * 2, kPage))
       return record_error("cuTensorMapEncodeTiled failed for kv_cache", MLA_ERR_CUDA);
   } else {
@@ -216,11 +231,13 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   prm.lse = lse;
   prm.err = err;
   prm.h = h_q;
+  prm.d_qk = d_qk;
   prm.s_q = s_q;
   prm.num_parts = num_sm_parts;
   prm.n_hblk = n_hblk;
   prm.rows = rows;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
+  if (v41) return launch_split<KvMode::kPagedFp8V41>(tm_q, tm_kv, prm, stream, &tm_codes, &tm_scales);
   if (fp8) return launch_split<KvMode::kPagedFp8>(tm_q, tm_kv, prm, stream, &tm_codes, &tm_scales);
   // 128 query rows: the two-SM kernel (scores and softmax on one SM, P.V on the other)
   if (h_q == pair::kRows) return launch_pair<false>(tm_kv, prm, stream);
@@ -283,6 +300,7 @@ extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t 
   prm.lse = lse;
   prm.err = err;
   prm.h = h_q;
+  prm.d_qk = kDqk;
   prm.s_q = s_q;
   prm.num_parts = num_sm_parts;
   prm.n_hblk = head_blocks(h_q);

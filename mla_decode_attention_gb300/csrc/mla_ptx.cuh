@@ -498,6 +498,20 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t ld_shared_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// float8 e8m0 scale code -> fp32: 2^(code - 127) (an 8-bit exponent, no sign
+// or mantissa); code 0 is 2^-127 (an fp32 subnormal), code 255 is NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t code) {
+  if (code == 0u) return __uint_as_float(0x00400000u);
+  if (code == 255u) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float(code << 23);
+}
+
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");

@@ -75,7 +75,18 @@ constexpr uint32_t kTmemS = 256;   // S^T: 64 columns
 constexpr uint32_t kIdescQK = idesc_bf16(128, kRowsPerCta, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, kRowsPerCta, true, true);
 
-enum class KvMode : int { kPagedBf16 = 0, kSparseBf16 = 1, kPagedFp8 = 2 };
+enum class KvMode : int { kPagedBf16 = 0, kSparseBf16 = 1, kPagedFp8 = 2, kPagedFp8V41 = 3 };
+
+// kPagedFp8: the 656-byte cache (fp32 scale per 128 latent codes, bf16 RoPE
+// chunk); kPagedFp8V41: the 528-byte cache (FlashMLA README, "FP8 / FP4 KV
+// Cache Format", V4.1): 512 e4m3 codes covering all 512 dimensions and 16
+// e8m0 scales (one per 32 codes) at byte 512 of the token.  Keys and values
+// are then 512 wide: QK^T runs over 8 chunks (no RoPE chunk) and P.V over
+// the same 8 chunks.
+__host__ __device__ constexpr bool is_fp8(KvMode m) {
+  return m == KvMode::kPagedFp8 || m == KvMode::kPagedFp8V41;
+}
+__host__ __device__ constexpr int qk_chunks(KvMode m) { return m == KvMode::kPagedFp8V41 ? 8 : 9; }
 
 // FP8 cache token: 512 e4m3 codes, 4 fp32 scales (one per 128 latent
 // channels), 64 bf16 RoPE values (FlashMLA "Hopper FP8 sparse decode" note,
@@ -83,6 +94,10 @@ enum class KvMode : int { kPagedBf16 = 0, kSparseBf16 = 1, kPagedFp8 = 2 };
 constexpr int kFp8TokenBytes = 656;
 constexpr int kFp8ScaleOffset = 512;
 constexpr int kFp8RopeOffset = 528;
+// V4.1 cache token (FlashMLA README, "FP8 / FP4 KV Cache Format"): 512 e4m3
+// codes, then 16 e8m0 scales (one per 32 codes) at byte 512.
+constexpr int kFp8V41TokenBytes = 528;
+constexpr int kV41HeadDim = 512;
 constexpr uint32_t kDequantBarrier = 5;  // FP8: all softmax warps (1..4: one softmax group each)
 // staging of a latent chunk's raw FP8 data inside its own 16 KB bf16 slot
 constexpr int kRawScaleOff = 4096;                  // [128 tokens][4 fp32 scales]
@@ -112,6 +127,7 @@ struct SplitParams {
   float* lse;
   uint32_t* err;
   int h;
+  int d_qk;                // query / key width: 576, or 512 for the V4.1 cache
   int s_q;
   int batch;
   int causal;              // dense: causal flag of the call (checked against the metadata)
@@ -354,14 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- setup: barriers, TMEM, zeroed padding rows of Q
   // FP8 with two head blocks: each CTA converts half of the latent chunks
   // (chunk c by head block c mod 2) and copies them into the peer's slots
-  const bool share = kMode == KvMode::kPagedFp8 && p.n_hblk == 2;
+  const bool share = is_fp8(kMode) && p.n_hblk == 2;
+  constexpr int kQk = qk_chunks(kMode);  // key chunks of QK^T
   if (threadIdx.x == 0) {
     for (int c = 0; c < kChunks; ++c) {
       // FP8: a latent chunk is filled by this CTA's softmax warps (one
       // arrive each), or by one bulk copy from the peer (one local arm + bytes)
       const bool from_peer = share && c < kChunks - 1 && (c & 1) != hb;
       mbar_init(smem_u32(&sm->full[c]),
-                (kMode == KvMode::kPagedFp8 && c < kChunks - 1 && !from_peer) ? 4 * kSoftmaxGroups : 1);
+                (is_fp8(kMode) && c < kChunks - 1 && !from_peer) ? 4 * kSoftmaxGroups : 1);
       // a slot is free once the MMA threads of every CTA writing into it
       // have released it
       mbar_init(smem_u32(&sm->empty[c]), (share && c < kChunks - 1) ? 2 : 1);
@@ -396,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
-    if (kMode == KvMode::kPagedFp8) {
+    if (is_fp8(kMode)) {
       tma_prefetch_desc(&tm_codes);
       tma_prefetch_desc(&tm_scales);
     }
@@ -410,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (!meta_ok) {
     // nothing to do: every role is skipped, the teardown below still runs
-  } else if (kMode == KvMode::kPagedFp8 && warp == kProducerWarp) {
+  } else if (is_fp8(kMode) && warp == kProducerWarp) {
     // ===================================================== producer (FP8)
-    // Lane 0 loads Q, the bf16 RoPE columns (chunk 8) and, for every latent
+    // Lane 0 loads Q, the bf16 RoPE columns (chunk 8; 656-byte cache only) and, for every latent
     // chunk this CTA converts, the raw e4m3 codes and token scales by TMA into
     // that chunk's own slot (codes at +8 KB, scales at +4 KB), each as soon as
     // the slot is released; the softmax warps convert the slot in place.
@@ -421,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int own0 = share ? hb : 0, own_step = share ? 2 : 1;
       const int n_own = (kChunks - 1) / own_step;
+      const int n_req = kMode == KvMode::kPagedFp8V41 ? n_own : n_own + 1;  // + the RoPE chunk
       PartCursor cur = part_cursor(meta, part);
       int q, t0, t1, split;
       uint32_t tile_ctr = 0, item_ctr = 0;
@@ -429,9 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
         ok = mbar_wait(smem_u32(&sm->q_empty), (item_ctr & 1) ^ 1, abort_flag, p.err);
         if (!ok) break;
-        mbar_arrive_expect_tx(smem_u32(&sm->q_full), kChunks * p.rows * 128);
+        mbar_arrive_expect_tx(smem_u32(&sm->q_full), kQk * p.rows * 128);
         const int q_row = q * p.h + hb * kRowsPerCta;
-        for (int c = 0; c < kChunks; ++c)
+        for (int c = 0; c < kQk; ++c)
           tma_load_2d(q_base + c * kQChunkBytes, &tm_q, c * 64, q_row, smem_u32(&sm->q_full),
                       l2_policy_evict_last());
         const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
@@ -484,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fbar = smem_u32(&sm->full[c]);
             const uint64_t t_start = globaltimer_ns();
             while (ok && !mbar_try_wait_hint(fbar, tile_ctr & 1, 200)) {
-              while (issued <= n_own && mbar_test_wait(smem_u32(&sm->empty[slot_of(issued)]), par))
+              while (issued < n_req && mbar_test_wait(smem_u32(&sm->empty[slot_of(issued)]), par))
                 issue(issued++);
               if (*abort_flag) {
                 ok = false;
@@ -500,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 mapa_shared(fbar, hb ^ 1));
             }
           }
-          while (ok && issued <= n_own) {  // the RoPE chunk, if still due
+          while (ok && issued < n_req) {  // the RoPE chunk, if still due
             ok = mbar_wait(smem_u32(&sm->empty[slot_of(issued)]), par, abort_flag, p.err);
             if (ok) issue(issued++);
           }
@@ -593,8 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           PartCursor nc = cur;
           int nq, nt0, nt1, ns;
           if (next_piece(meta, p.num_parts, &nc, &nq, &nt0, &nt1, &ns))
-            prefetch_l2(p.q + (static_cast<int64_t>(nq) * p.h + hb * kRowsPerCta) * 576,
-                        p.rows * 1152);
+            prefetch_l2(p.q + (static_cast<int64_t>(nq) * p.h + hb * kRowsPerCta) * p.d_qk,
+                        p.rows * p.d_qk * 2);
         }
         const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
         const int32_t* bt_row = bt_row_of(p, q);
@@ -650,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = t0; t < t1 && ok; ++t) {
           const uint32_t par = tile_ctr & 1;
           // S^T = K_tile . Q^T: A = tile chunk (K-major), B = Q chunk (K-major)
-          for (int c = 0; c < kChunks; ++c) {
+          for (int c = 0; c < kQk; ++c) {
             // FP8 chunks converted by the peer complete on its bulk copy
             const bool from_peer = share && c < kChunks - 1 && (c & 1) != hb;
             ok = from_peer ? mbar_wait_cluster(smem_u32(&sm->full[c]), par, abort_flag, p.err)
@@ -744,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lsum = 0.f;        // sum p of row R*g + (lane & 15) over this warp's tokens
       float bsum = 0.f;        // sum bf16(p) of the same row
       for (int t = t0; t < t1; ++t) {
-        if constexpr (kMode == KvMode::kPagedFp8) {
+        if constexpr (is_fp8(kMode)) {
           // ---- FP8: convert this tile's owned latent chunks in place.  Thread
           // = (token dq_r, 16-code unit dq_u); reads of the staging finish at
           // the named barrier before any bf16 write lands on it.  Every exit
@@ -756,7 +774,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             const uint32_t slot = kv_base + c * kChunkBytes;
             const uint4 codes = ld_shared_v4(slot + kRawCodeOff + dq_r * 64 + dq_u * 16);
-            const float sc = ld_shared_f32(slot + kRawScaleOff + dq_r * 16 + (c >> 1) * 4);
+            // the unit's scale: fp32 per 128 codes (656-byte cache), or e8m0
+            // per 32 codes, 2^(byte - 127) (528-byte cache)
+            const float sc = kMode == KvMode::kPagedFp8V41
+                                 ? e8m0_to_f32(ld_shared_u8(slot + kRawScaleOff + dq_r * 16 + 2 * c + (dq_u >> 1)))
+                                 : ld_shared_f32(slot + kRawScaleOff + dq_r * 16 + (c >> 1) * 4);
             ok = !named_barrier_or(kDequantBarrier, 128 * kSoftmaxGroups, !ok);
             if (!ok) break;
             convert_unit(slot + dq_r * 128, dq_r, dq_u, codes, sc);
@@ -767,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         ok = mbar_wait(smem_u32(&sm->s_full), tile_ctr & 1, abort_flag, p.err);
-        if constexpr (kMode == KvMode::kPagedFp8)  // leave together (the barrier above)
+        if constexpr (is_fp8(kMode))  // leave together (the barrier above)
           ok = !named_barrier_or(kDequantBarrier, 128 * kSoftmaxGroups, !ok);
         if (!ok) break;
         tc_fence_after();
@@ -881,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bsum = (sm->red_bsum[g][0][row] + sm->red_bsum[g][1][row]) +
              (sm->red_bsum[g][2][row] + sm->red_bsum[g][3][row]);
       ok = mbar_wait(smem_u32(&sm->o_done), item_ctr & 1, abort_flag, p.err);
-      if constexpr (kMode == KvMode::kPagedFp8)  // the next piece starts at a shared barrier
+      if constexpr (is_fp8(kMode))  // the next piece starts at a shared barrier
         ok = !named_barrier_or(kDequantBarrier, 128 * kSoftmaxGroups, !ok);
       if (!ok) break;
       tc_fence_after();

@@ -2,12 +2,17 @@
 
 This module is shared by the tests, ``bench.py`` and the oracle-side checks.  It
 holds the workload shapes and the random draws only: no attention arithmetic.
-The one encoding step here is the FP8 cache format of the inputs (FlashMLA
-"Hopper FP8 sparse decode" note, section "The FP8 KVCache Format": per token
-512 float8_e4m3 latent values quantised in 1x128 tiles, 4 float32 scales, then
-64 bfloat16 RoPE values, 656 bytes).  The e4m3 rounding itself is
-``torch.float8_e4m3fn``'s cast (round to nearest even); scales are
-``absmax / 448`` in fp32.
+The encoding steps here are the FP8 cache formats of the inputs:
+* 656 bytes (FlashMLA "Hopper FP8 sparse decode" note, section "The FP8
+  KVCache Format"): per token 512 float8_e4m3 latent values quantised in
+  1x128 tiles, 4 float32 scales, then 64 bfloat16 RoPE values; scales are
+  ``absmax / 448`` in fp32;
+* 528 bytes (FlashMLA README, "FP8 / FP4 KV Cache Format", DeepSeek V4.1,
+  head_dim 512): 512 float8_e4m3 values covering all dimensions, then 16
+  float8_e8m0 scales, one per 32 values; an e8m0 scale is a power of two, here
+  the smallest one at or above ``absmax / 448`` (so no code saturates).
+The e4m3 rounding itself is ``torch.float8_e4m3fn``'s cast (round to nearest
+even).
 
 Shapes follow the DeepSeek-V3 MLA decode setting described on the pages
 (128 query heads, one shared 576-wide latent+RoPE key row, V = the first 512
@@ -27,6 +32,9 @@ D_ROPE = 64
 PAGE = 64           # page block size (tokens)
 FP8_TOKEN_BYTES = 656   # 512 e4m3 + 4 x fp32 scale + 64 x bf16
 FP8_TILE = 128      # channels per fp32 scale
+FP8_V41_TOKEN_BYTES = 528   # 512 e4m3 + 16 e8m0 scales
+V41_HEAD_DIM = 512  # V4.1: key = value = 512 dims (RoPE dims included)
+V41_TILE = 32       # values per e8m0 scale
 E4M3_MAX = 448.0
 SOFTMAX_SCALE = 1.0 / math.sqrt(192.0)
 TAIL_MAGNITUDE = 1.0e4  # finite junk placed in page slots past the sequence end
@@ -36,7 +44,7 @@ TAIL_MAGNITUDE = 1.0e4  # finite junk placed in page slots past the sequence end
 class Workload:
     """One synthetic decode workload."""
     name: str
-    kind: str                 # "dense" | "sparse" | "fp8"
+    kind: str                 # "dense" | "sparse" | "fp8" (656 B) | "fp8_v41" (528 B)
     b: int
     s_q: int
     h: int
@@ -163,6 +171,40 @@ def fp8_inputs(w: Workload, seed: Optional[int] = None) -> dict:
                 causal=w.causal)
 
 
+def quantize_fp8_v41_tokens(x: torch.Tensor) -> torch.Tensor:
+    """Encode float32 token rows [..., 512] into the 528-byte V4.1 layout.
+
+    Bytes [0, 512): e4m3 codes of x / scale[c // 32]; bytes [512, 528): the 16
+    e8m0 scale codes (biased exponents: scale = 2^(code - 127)), each the
+    smallest power of two at or above absmax / 448 of its 32 values (code 127,
+    scale 1, for an all-zero block).
+    """
+    lead = x.shape[:-1]
+    blocks = x.reshape(*lead, V41_HEAD_DIM // V41_TILE, V41_TILE)
+    ratio = blocks.abs().amax(dim=-1) / E4M3_MAX
+    mant, expo = torch.frexp(ratio)              # ratio = mant * 2^expo, 0.5 <= mant < 1
+    up = torch.where(mant == 0.5, expo - 1, expo)  # ceil(log2(ratio))
+    up = torch.where(ratio > 0, up, torch.zeros_like(up)).clamp(-127, 127)
+    scale = torch.pow(2.0, up.to(torch.float32))
+    codes = (blocks / scale.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
+    codes = codes.reshape(*lead, V41_HEAD_DIM)
+    sc = (up + 127).to(torch.uint8)
+    return torch.cat([codes, sc], dim=-1).contiguous()
+
+
+def fp8_v41_inputs(w: Workload, seed: Optional[int] = None) -> dict:
+    """V4.1 FP8 (528 B/token) paged-cache inputs with bf16 queries of 512."""
+    g = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    seqlens = _draw_seqlens(w, g)
+    bt, n_pool = _page_layout(seqlens, w.extra_pages, g)
+    kv = torch.randn((n_pool, PAGE, V41_HEAD_DIM), generator=g, dtype=torch.float32)
+    _fill_tails(kv, seqlens, bt, g)
+    q = _bf16_normal((w.b, w.s_q, w.h, V41_HEAD_DIM), g)
+    return dict(q=q, kv_cache=quantize_fp8_v41_tokens(kv), block_table=bt,
+                cache_seqlens=seqlens, softmax_scale=SOFTMAX_SCALE,
+                causal=w.causal)
+
+
 def sparse_inputs(w: Workload, seed: Optional[int] = None) -> dict:
     """DSA top-k inputs: a flat pool of latent rows and per-query indices.
 
@@ -194,6 +236,8 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
         return dense_inputs(w, seed)
     if w.kind == "fp8":
         return fp8_inputs(w, seed)
+    if w.kind == "fp8_v41":
+        return fp8_v41_inputs(w, seed)
     if w.kind == "sparse":
         return sparse_inputs(w, seed)
     raise ValueError(w.kind)

@@ -26,7 +26,14 @@ What it computes (one "row" = one query token of one head):
   "indices Tensor").
 * FP8 cache: 656 bytes per token = 512 e4m3 codes, 4 fp32 scales (one per 128
   channels), 64 bf16 RoPE values (FlashMLA "Hopper FP8 sparse decode" note,
-  "The FP8 KVCache Format").  The kernel dequantises the codes into bf16
+  "The FP8 KVCache Format").
+* V4.1 FP8 cache (FlashMLA README, "FP8 / FP4 KV Cache Format"): head_dim 512,
+  528 bytes per token = 512 e4m3 codes covering all 512 dimensions (the RoPE
+  dimensions are quantised too) followed by 16 e8m0 scales, one per 32
+  consecutive codes.  A key is 512 wide and, with no separate latent part,
+  the value is the whole key row (d_qk = d_v = 512).  e8m0 holds a power of
+  two only, so e4m3 * scale has at most 4 significant bits: it is exactly a
+  bf16 value, and the dequantised key is that exact product.  The kernel dequantises the codes into bf16
   before its bf16 MMAs (same note: convert e4m3 to bf16, multiply by the fp32
   scale; "we first dequantize ... into 512 bfloat16s"), so a key's latent value
   is bf16(e4m3(code) * scale): the exact product rounded once to bf16.
@@ -51,6 +58,8 @@ PAGE = 64
 D_QK = 576
 D_V = 512
 FP8_TOKEN_BYTES = 656
+FP8_V41_TOKEN_BYTES = 528
+V41_HEAD_DIM = 512
 
 
 # ---------------------------------------------------------------------------
@@ -103,6 +112,24 @@ def fp8_tokens_to_f64(raw: np.ndarray) -> np.ndarray:
     return np.concatenate([lat.reshape(*lead, 512), bf16_bits_to_f64(rope_bits)], axis=-1)
 
 
+def e8m0_to_f64(codes: np.ndarray) -> np.ndarray:
+    """float8 e8m0 scale codes -> float64: an 8-bit biased exponent and no
+    sign or mantissa, value 2^(code - 127); code 255 is NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.float64)
+    return np.where(c == 255, np.nan, np.exp2(c - 127.0))
+
+
+def fp8_v41_tokens_to_f64(raw: np.ndarray) -> np.ndarray:
+    """528-byte V4.1 cache tokens [..., 528] uint8 -> [..., 512] float64:
+    value[c] = e4m3(raw[c]) * e8m0(raw[512 + c // 32]) for c < 512."""
+    raw = np.ascontiguousarray(raw, dtype=np.uint8)
+    assert raw.shape[-1] == FP8_V41_TOKEN_BYTES
+    lead = raw.shape[:-1]
+    codes = e4m3_to_f64(raw[..., :512]).reshape(*lead, 16, 32)
+    scales = e8m0_to_f64(raw[..., 512:528])
+    return (codes * scales[..., :, None]).reshape(*lead, 512)
+
+
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """Nearest bfloat16 value (8 significant bits, ties to even), as float64.
 
@@ -129,7 +156,8 @@ def fp8_tokens_to_keys(raw: np.ndarray) -> np.ndarray:
 def attend(q_rows: np.ndarray, keys: np.ndarray, softmax_scale: float):
     """softmax(scale * q K^T) V for query rows sharing one key set.
 
-    q_rows [R, 576], keys [T, 576] (V = keys[:, :512]).
+    q_rows [R, d], keys [T, d] with V = keys[:, :512] (d = 576: 512 latent +
+    64 RoPE; d = 512: the V4.1 head, where V is the whole key).
     Returns out [R, 512], lse [R] (natural log of sum exp of scaled scores).
     """
     q_rows = np.asarray(q_rows, dtype=np.float64)
@@ -201,12 +229,15 @@ def visible_length(seqlen: int, s_q: int, j: int, causal: bool) -> int:
 def widen(x: np.ndarray) -> np.ndarray:
     """float64 view of an input array: uint16 arrays are bf16 bit patterns,
     uint8 arrays with a last dimension of 656 are FP8 cache tokens (decoded
-    to their bf16 keys), anything else is converted with ``astype``."""
+    to their bf16 keys), of 528 V4.1 FP8 tokens (decoded exactly), anything
+    else is converted with ``astype``."""
     x = np.asarray(x)
     if x.dtype == np.uint16:
         return bf16_bits_to_f64(x)
     if x.dtype == np.uint8 and x.shape[-1] == FP8_TOKEN_BYTES:
         return fp8_tokens_to_keys(x)
+    if x.dtype == np.uint8 and x.shape[-1] == FP8_V41_TOKEN_BYTES:
+        return fp8_v41_tokens_to_f64(x)
     return x.astype(np.float64)
 
 
@@ -252,6 +283,16 @@ def dense_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
         out[bi, j] = o
         lse[bi, :, j] = l
     return out, lse
+
+
+def fp8_v41_dense_decode(q, kv_raw, block_table, cache_seqlens, softmax_scale,
+                         causal=True, rows=None):
+    """Paged decode over the 528-byte V4.1 FP8 cache: q [b, s_q, h, 512],
+    kv_raw [n_pages, 64, 528] uint8; each gathered token decodes exactly to
+    its 512-wide key, which is also its value row."""
+    kv_raw = np.asarray(kv_raw, dtype=np.uint8)
+    assert kv_raw.shape[-1] == FP8_V41_TOKEN_BYTES
+    return dense_decode(q, kv_raw, block_table, cache_seqlens, softmax_scale, causal, rows)
 
 
 def fp8_dense_decode(q, kv_raw, block_table, cache_seqlens, softmax_scale,

@@ -132,3 +132,75 @@ def test_combine_after_decodes_of_two_kernels_on_one_metadata():
     for bf, (ro, rl), name in zip(bufs, ref, ("bf16", "fp8")):
         assert int(bf.err.item()) == 0
         assert_parity(bf.out.float().cpu().numpy(), ro, bf.lse.cpu().numpy(), rl, name)
+
+
+# ------------------------------------------------ V4.1 cache (528 bytes per token)
+
+def v41_case(seed, b, s_q, h, seqlens, extra_pages=0):
+    w = workloads.Workload("v41", "fp8_v41", b=b, s_q=s_q, h=h, seqlens=tuple(seqlens),
+                           extra_pages=extra_pages, seed=seed)
+    return workloads.make_inputs(w)
+
+
+def run_v41(inp, num_sm_parts=None, causal=True):
+    q = inp["q"].to(DEV)
+    kv = inp["kv_cache"].to(DEV)
+    bt = inp["block_table"].to(DEV)
+    sl = inp["cache_seqlens"].to(DEV)
+    b, s_q, h, _ = q.shape
+    buf = binding.DecodeBuffers(b, s_q, h, DEV, num_sm_parts)
+    binding.mla_get_metadata(sl, b, s_q, causal, 0, buf.num_sm_parts, buf.metadata)
+    binding.mla_decode(q, kv, binding.MLA_KV_FP8_528, bt, sl, inp["softmax_scale"], causal,
+                       buf.metadata, buf.num_sm_parts, buf.workspace, buf.out, buf.lse, buf.err)
+    torch.cuda.synchronize()
+    return buf.out.float().cpu().numpy(), buf.lse.cpu().numpy(), int(buf.err.item())
+
+
+def oracle_v41(inp, causal=True, rows=None):
+    return oracle.fp8_v41_dense_decode(bf16_np(inp["q"]), inp["kv_cache"].numpy(),
+                                       inp["block_table"].numpy(), inp["cache_seqlens"].numpy(),
+                                       inp["softmax_scale"], causal, rows)
+
+
+def test_v41_small_parity():
+    inp = v41_case(61, 2, 1, 16, (200, 333), extra_pages=6)
+    out, lse, err = run_v41(inp)
+    ref_o, ref_l = oracle_v41(inp)
+    assert_parity(out, ref_o, lse, ref_l, "v41 small")
+    assert err == 0
+
+
+@pytest.mark.parametrize("h,parts", [(64, None), (128, None), (128, 5), (32, 3)])
+def test_v41_spec_ragged(h, parts):
+    inp = v41_case(62 + h, 4, 2, h, (2, 129, 1000, 2500))
+    out, lse, err = run_v41(inp, parts)
+    ref_o, ref_l = oracle_v41(inp)
+    assert_parity(out, ref_o, lse, ref_l, f"v41 h={h} parts={parts}")
+    assert err == 0
+
+
+@pytest.mark.parametrize("h", [64, 128])
+def test_v41_single_key_rows_are_the_exact_key_row(h):
+    """One visible key: the output row is that key's whole 512-wide dequantised
+    row (RoPE dimensions included), bit for bit: e4m3 times a power of two is
+    a bf16 value, so nothing rounds."""
+    inp = v41_case(63, 4, 1, h, (1, 1, 1, 1), extra_pages=8)
+    out, lse, err = run_v41(inp)
+    dec = oracle.fp8_v41_tokens_to_f64(inp["kv_cache"].numpy())
+    bt = inp["block_table"].numpy()
+    for b in range(4):
+        row = dec[bt[b, 0], 0]
+        assert np.array_equal(out[b, 0], np.repeat(row[None], h, axis=0))
+    assert err == 0
+
+
+def test_v41_full_size_all_rows():
+    """b=64, h=128, every request 8192 tokens of the 528-byte cache: every
+    request and head compared with the oracle."""
+    w = workloads.Workload("v41_full", "fp8_v41", b=64, s_q=1, h=128, seqlens=(8192,) * 64, seed=64)
+    inp = workloads.make_inputs(w)
+    out, lse, err = run_v41(inp)
+    ref_o, ref_l = oracle_v41(inp)
+    st = assert_parity_per_token(out, ref_o, lse, ref_l, "v41")
+    print("v41 parity:", st)
+    assert err == 0

@@ -99,6 +99,79 @@ def test_fp8_quantise_decode_error_bound():
     assert np.array_equal(dec[:, 512:], rope_ref)
 
 
+def test_e8m0_all_codes_match_torch():
+    """All 256 e8m0 scale codes decode like torch's float8_e8m0fnu (2^(c-127),
+    255 = NaN)."""
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("this torch has no float8_e8m0fnu")
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e8m0_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).float().double().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert ours[127] == 1.0 and ours[0] == 2.0 ** -127 and ours[254] == 2.0 ** 127
+
+
+def test_fp8_v41_token_layout_offsets():
+    """A 528-byte token built by hand: codes at bytes 0..511, one e8m0 scale
+    per 32 codes at bytes 512..527 (the page's 512 + 16 = 528)."""
+    g = GOLDEN["fp8_v41_token_bytes"]
+    assert g["value"] == sum(g["parts"]) == oracle.FP8_V41_TOKEN_BYTES
+    assert g["parts"][0] // g["values_per_scale"] == g["parts"][1]
+    raw = np.zeros((1, 528), dtype=np.uint8)
+    raw[0, 0] = 0x38        # e4m3 1.0
+    raw[0, 31] = 0x40       # 2.0, same 32-block as byte 0
+    raw[0, 32] = 0x38       # 1.0, the next block
+    raw[0, 480] = 0x3C      # 1.5, block 15
+    raw[0, 511] = 0xB8      # -1.0, block 15
+    raw[0, 512] = 127 + 3   # block 0 scale 8
+    raw[0, 513] = 127 - 2   # block 1 scale 0.25
+    raw[0, 527] = 127       # block 15 scale 1
+    dec = oracle.fp8_v41_tokens_to_f64(raw)[0]
+    want = np.zeros(512)
+    want[0], want[31], want[32], want[480], want[511] = 8.0, 16.0, 0.25, 1.5, -1.0
+    assert np.array_equal(dec, want)
+
+
+def test_fp8_v41_quantise_decode_error_bound():
+    """Each 32-value block's scale is the power of two at or above
+    absmax / 448 and below twice that; each value is within half an e4m3 step
+    (2^-4 relative, or 2^-10 * scale below the e4m3 normal range)."""
+    from mla_decode_attention_gb300 import workloads
+    x = torch.randn((7, 512), generator=torch.Generator().manual_seed(5)) * 3
+    x[2, :32] = 0.0                                       # an all-zero block
+    raw = workloads.quantize_fp8_v41_tokens(x).numpy()
+    dec = oracle.fp8_v41_tokens_to_f64(raw)
+    scale = oracle.e8m0_to_f64(raw[:, 512:]).repeat(32, axis=1)
+    amax = np.abs(x.double().numpy()).reshape(7, 16, 32).max(axis=2).repeat(32, axis=1)
+    nz = amax > 0
+    assert np.all(scale[nz] >= amax[nz] / 448) and np.all(scale[nz] < 2 * amax[nz] / 448)
+    assert np.all(scale[~nz] == 1.0) and np.all(dec[2, :32] == 0.0)
+    err = np.abs(dec - x.double().numpy())
+    assert np.all(err <= np.maximum(2.0 ** -4 * np.abs(x.double().numpy()), 2.0 ** -10 * scale))
+
+
+def test_fp8_v41_keys_are_exact_bf16_values():
+    """e4m3 * 2^k has at most 4 significant bits, so the dequantised key is a
+    bf16 value exactly: no rounding between the format and the bf16 MMA."""
+    from mla_decode_attention_gb300 import workloads
+    x = torch.randn((64, 512), generator=torch.Generator().manual_seed(6))
+    dec = oracle.fp8_v41_tokens_to_f64(workloads.quantize_fp8_v41_tokens(x).numpy())
+    assert np.array_equal(oracle.round_to_bf16(dec), dec)
+
+
+def test_fp8_v41_single_key_returns_the_whole_key_row():
+    """V4.1 keys are 512 wide and the value is the whole key (RoPE dims
+    included): one key gives out = that key row."""
+    r = rng(33)
+    keys = oracle.fp8_v41_tokens_to_f64(
+        __import__("mla_decode_attention_gb300.workloads", fromlist=["x"]).quantize_fp8_v41_tokens(
+            torch.from_numpy(r.standard_normal((1, 512))).float()).numpy())
+    out, lse = oracle.attend(r.standard_normal((4, 512)), keys, SCALE)
+    assert np.array_equal(out, np.repeat(keys, 4, axis=0))
+
+
 def test_round_to_bf16_matches_torch_on_fp32_values():
     x = rng(40).standard_normal(50000).astype(np.float32) * np.exp2(rng(41).integers(-20, 20, 50000))
     x = x.astype(np.float32)
