@@ -44,6 +44,23 @@ bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t str
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The paged bf16 cache seen as a 4-D tensor [8-token groups][9 chunks][8
+// rows][64 columns] (strides: row 1152 bytes, chunk 128 bytes, group 9216
+// bytes); boxes of [8 groups][`chunks`][8 rows][64 columns] (one page's
+// chunks, starting at the chunk given at load time) with 128-byte swizzle,
+// landing as [group][chunk][row][128 bytes].
+bool make_quad_map(CUtensorMap* m, const void* base, uint64_t num_pages, uint32_t chunks) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {64u, 8u, static_cast<cuuint64_t>(kDqk / 64), num_pages * (kPage / 8)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kDqk) * 2u, 128u, static_cast<cuuint64_t>(kDqk) * 2u * 8u};
+  const cuuint32_t box[4] = {64u, 8u, chunks, static_cast<cuuint32_t>(kPage / 8)};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D bf16 tensor [rows, cols] whose rows start `stride_bytes` apart; boxes of
 // [box_rows x 64 columns] with 128-byte swizzle.
 bool make_strided_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
@@ -113,8 +130,11 @@ int launch_split(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const SplitP
   return e == cudaSuccess ? MLA_OK : record_cuda_error("split kernel launch", e);
 }
 
+// tm_qa, tm_qb: the group-interleaved maps of the paged cache (chunks 0..3,
+// 4..6 of a page); the sparse kernel does not read them.
 template <bool kSparse>
-int launch_pair(const CUtensorMap& tm_kv, const SplitParams& prm, cudaStream_t stream) {
+int launch_pair(const CUtensorMap& tm_kv, const CUtensorMap& tm_qa, const CUtensorMap& tm_qb,
+                const SplitParams& prm, cudaStream_t stream) {
   static int state = 0;  // 0 unset, 1 ok, -1 failed (per instantiation)
   static std::mutex mu;
   {
@@ -143,7 +163,7 @@ int launch_pair(const CUtensorMap& tm_kv, const SplitParams& prm, cudaStream_t s
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::mla_pair_kernel<kSparse>, tm_kv, prm);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::mla_pair_kernel<kSparse>, tm_kv, tm_qa, tm_qb, prm);
   return e == cudaSuccess ? MLA_OK : record_cuda_error("pair kernel launch", e);
 }
 
@@ -240,7 +260,13 @@ extern "C" int mla_decode_splitkv(const void* q, const void* kv_cache, int kv_fo
   if (v41) return launch_split<KvMode::kPagedFp8V41>(tm_q, tm_kv, prm, stream, &tm_codes, &tm_scales);
   if (fp8) return launch_split<KvMode::kPagedFp8>(tm_q, tm_kv, prm, stream, &tm_codes, &tm_scales);
   // 128 query rows: the two-SM kernel (scores and softmax on one SM, P.V on the other)
-  if (h_q == pair::kRows) return launch_pair<false>(tm_kv, prm, stream);
+  if (h_q == pair::kRows) {
+    CUtensorMap tm_qa, tm_qb;
+    if (!make_quad_map(&tm_qa, kv_cache, static_cast<uint64_t>(num_pages), 4) ||
+        !make_quad_map(&tm_qb, kv_cache, static_cast<uint64_t>(num_pages), 3))
+      return record_error("cuTensorMapEncodeTiled failed for the kv_cache page groups", MLA_ERR_CUDA);
+    return launch_pair<false>(tm_kv, tm_qa, tm_qb, prm, stream);
+  }
   return launch_split<KvMode::kPagedBf16>(tm_q, tm_kv, prm, stream);
 }
 
@@ -307,7 +333,7 @@ extern "C" int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t 
   prm.rows = rows;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
   // 128 query rows: the two-SM kernel with gathered keys
-  return h_q == pair::kRows ? launch_pair<true>(tm_kv, prm, stream)
+  return h_q == pair::kRows ? launch_pair<true>(tm_kv, tm_kv, tm_kv, prm, stream)
                             : launch_split<KvMode::kSparseBf16>(tm_q, tm_kv, prm, stream);
 }
 

@@ -3,51 +3,48 @@
 // A cluster of two CTAs on two SMs shares one schedule part.  Per 128-key tile:
 //
 //   score CTA (rank 0):  S[128 rows x 128 tokens] = Q[128 x 576] . K_tile^T
-//                        (tcgen05; the 512 latent columns with A = Q in TMEM,
-//                        the 64 RoPE columns with A = Q's RoPE part in shared
-//                        memory), then the online softmax with one thread per
-//                        query row; P (bf16) goes to its own TMEM and, with the
-//                        per-row rescale factors, to the output CTA by one
-//                        shared-memory bulk copy.  It also owns the last 64
-//                        output columns: O[:, 448:512] += P . V_tile[:, 448:512]
-//                        (A = P in TMEM, B = the tile's latent chunk 7).
-//   output CTA (rank 1): copies P into its TMEM and computes
-//                        O[:, 0:448] += P[128 x 128] . V_tile[128 x 448]
-//                        (A = P in TMEM, B = V in shared memory; O in TMEM).
+//                        (tcgen05, A = Q resident in TMEM, B = K tile in smem,
+//                        N = 128), then the online softmax with one thread per
+//                        query row; P (bf16) and the per-row rescale factors go
+//                        to the output CTA by a shared-memory bulk copy.
+//   output CTA (rank 1): O[128 rows x 512] += P[128 x 128] . V_tile[128 x 512]
+//                        (tcgen05, both operands in smem, N = 128 per d quarter),
+//                        O in TMEM (all 512 columns); it writes the output rows.
 //
-// Both CTAs read the same cached rows: the score CTA all 576 columns, the
-// output CTA the first 448 (V is the latent part of the same row, FlashMLA
-// deep dive, "Theoretical Analysis"; the second reader finds the rows in L2).
-// Every PV product takes its A operand from TMEM: on this GPU a cluster whose
-// CTAs keep issuing MMAs with A from TMEM in one CTA and A from shared memory
-// in the other runs all of them at about half rate, while TMEM-A in both runs
-// at full rate (a handful of shared-memory-A MMAs for the RoPE columns does
-// not matter).  TMEM use:
-//   score CTA:  [0, 256) Q latent part (bf16 pairs), [256, 384) S (fp32, one
-//               buffer: the row threads load a tile's scores into registers
-//               at once and free it), [384, 448) P (bf16 pairs), [448, 512)
-//               O columns 448..511 (fp32)
-//   output CTA: [0, 448) O columns 0..447 (fp32), [448, 512) P (bf16 pairs)
+// Both CTAs read the same cached rows (the score CTA all 576 columns, the
+// output CTA the first 512: V is the latent part of the same row, FlashMLA
+// deep dive, "Theoretical Analysis").  Splitting the two products over two SMs
+// lets each issue MMAs of 128 x 128 x 16 (full tensor rate) and keeps keys
+// loading while the previous tile is multiplied.  Score CTA TMEM: Q's 512
+// latent columns (256 columns of bf16 pairs) and two S buffers, so QK of tile
+// t + 1 runs while the softmax still reads tile t; Q's 64 RoPE columns sit in
+// shared memory and enter QK through one smem-smem MMA chunk.  The softmax
+// makes two passes over S in TMEM (row max, then probabilities), 32 columns
+// at a time, so its code stays small.
 //
-// Roles (384 threads, both CTAs; three warps per SM sub-partition, so each
-// thread may hold 168 registers):
-//   warps 0, 2 lane 0    : TMA issuers (dense; chunk c of a tile by issuer c mod
-//                          2).  Sparse: warps 0, 2, 3, every lane gathers.
+// Paged cache: each group of K chunks (3g .. 3g + 2) and each half of V
+// (chunks 0..3, 4..7) arrives as one 4-D box per page that lands as
+// [8-token group][chunk][8 tokens][128 bytes]: a TMA box costs its SM a fixed
+// time besides its bytes, so a [64 x 64] box per chunk and page moves about
+// half as many bytes per SM-second.  In such a region chunk c of all 128
+// tokens is a swizzled K-major operand whose 8-token groups lie 3 KB (V: 4 KB)
+// apart, the second page's groups right after the first's, so QK stays one
+// N = 128 product per chunk, and V read MN-major gives N = 256 products.
+// Sparse keys are gathered four rows at a time into [128 tokens x 64 columns]
+// chunks instead.
+//
+// Roles (256 threads, both CTAs; two warps per SM sub-partition, so each
+// thread may hold 224 registers):
+//   warps 0, 2 lane 0    : TMA issuers (chunk c of a tile by issuer c mod 2 in
+//                          the score CTA; chunk n of the V stream by n mod 2)
 //   warp 1               : TMEM owner; lane 0 issues every MMA
-//   warp 3 (dense)       : score CTA: the P bulk copies (named barriers 1, 2
-//                          with warps 4..11 around the staging buffer);
+//   warp 3               : score CTA: issues the P bulk copies (named barriers 1, 2
+//                          with warps 4..7 around the staging buffer);
 //                          output CTA: hands consumed P buffers back
-//   warps 4..11          : row threads: two per query row, thread (h, r) with
-//                          r = 32 (warp mod 4) + lane = TMEM lane r and half
-//                          h = 0 (warps 4..7) or 1 (warps 8..11).  Score CTA:
-//                          tokens 64h .. 64h + 63 of each tile (Q loads, the
-//                          softmax on those 64 scores, their P), output
-//                          columns 448 + 32h .. +31 and, for h = 0, the LSE;
-//                          output CTA: P tokens 64h .. +63 into TMEM, the
-//                          rescale and epilogue of columns 224h .. 224h + 223.
+//   warps 4..7           : row threads, thread r = query row r = TMEM lane r
 //
 // Waits are bounded (mbar_wait*); after an abort every role keeps walking its
-// schedule without waiting, so the named barriers between warps 3..11 stay
+// schedule without waiting, so the named barriers between warps 4..8 stay
 // matched and every thread reaches the final cluster barrier.
 #pragma once
 
@@ -65,72 +62,63 @@
 namespace mla {
 namespace pair {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 256;
 constexpr int kRows = 128;                         // query rows per cluster = TMEM lanes
 constexpr int kChunk = kTileTokens * 64 * 2;       // 16 KB: [128 tokens x 64 columns] bf16
-// ---- score CTA shared memory
-constexpr int kKGroups = 3;                        // K tile: groups {0,1,2}, {3,4,5}, {6,7,8}
-constexpr int kKSlot2 = 6 * kChunk;                // group 2 slot: chunk 6, then chunk 8 (RoPE)
-constexpr int kC7 = 8 * kChunk;                    // chunk 7 (columns 448..511), two buffers
-constexpr int kQRope = 10 * kChunk;                // 163840: Q RoPE columns [128 x 64] bf16
-constexpr int kStage = 11 * kChunk;                // 180224: P staging for the output CTA
+// score CTA
+constexpr int kKGroups = 3;                        // K ring: 3 groups of 3 chunks
+constexpr int kKGroupBytes = 3 * kChunk;           // 48 KB
+constexpr int kQRope = kKGroups * kKGroupBytes;    // 147456: Q RoPE columns [128 x 64] bf16
+constexpr int kStage = kQRope + kChunk;            // 163840: P staging
 constexpr int kPBytes = kRows * kTileTokens * 2;   // 32768: P[128 rows x 128 tokens] bf16
 constexpr int kSideAlpha = kPBytes;                // float alpha[128]
 constexpr int kSideInvL = kPBytes + 512;           // float inv_l[128] (last tile of a piece)
 constexpr int kSideFlags = kPBytes + 1024;         // uint32 per row warp: any alpha != 1
 constexpr int kXferBytes = kPBytes + 1040;         // 33808 bytes per tile
-// ---- output CTA shared memory
-constexpr int kVGroups = 4;                        // V quarters: chunks {0,1}, {2,3}, {4,5}, {6}
+// output CTA
+constexpr int kVGroups = 4;                        // V ring: 128-wide d quarters
 constexpr int kVGroupBytes = 2 * kChunk;           // 32 KB
 constexpr int kPBuf0 = kVGroups * kVGroupBytes;    // 131072
 constexpr int kPBufStride = 34816;                 // kXferBytes rounded up to 1 KB
-constexpr int kEpi = kPBuf0 + 2 * kPBufStride;     // 200704: 2 KB per row warp for the epilogue
-// score CTA: the two row threads of a query row exchange partial row maxima
-// (per tile parity) and, at a piece's end, partial sums
-constexpr int kRedMax = kStage + kXferBytes;       // 214032: float [2 parity][2 halves][128]
-constexpr int kRedSum = kRedMax + 2048;            // float [2 sums][2 halves][128]
-constexpr int kBarOffset = 219136;                 // after both layouts, same offset in both CTAs
-// ---- output columns
-constexpr int kDvOut = 448;                        // output CTA: columns 0..447
-constexpr int kDvTail = kDv - kDvOut;              // score CTA: columns 448..511
-// ---- TMEM columns
-constexpr uint32_t kQCol = 0;                      // score CTA: Q latent part
-constexpr uint32_t kSCol = 256;                    // score CTA: S
-constexpr uint32_t kPColS = 384;                   // score CTA: P
-constexpr uint32_t kOTailCol = 448;                // score CTA: O columns 448..511
-constexpr uint32_t kOCol = 0;                      // output CTA: O columns 0..447
-constexpr uint32_t kPColO = 448;                   // output CTA: P
+constexpr int kBarOffset = kPBuf0 + 2 * kPBufStride;  // 200704 (score CTA ends at 197648)
+constexpr int kEpi = kBarOffset + 1024;            // output CTA: 4 KB per row warp for the epilogue
+// TMEM columns
+constexpr uint32_t kQCol = 0;                      // score CTA: Q latent part, 256 columns
+constexpr uint32_t kSCol = 256;                    // score CTA: S buffers at 256 and 384
 constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
-constexpr uint32_t kIdescO128 = idesc_bf16(128, 128, false, true);
-constexpr uint32_t kIdescO64 = idesc_bf16(128, 64, false, true);
-constexpr uint32_t kRowThreads = 256;              // warps 4..11
-constexpr uint32_t kXferNamedThreads = 288;        // dense: warps 3..11
-constexpr uint32_t kRowExchange = 3;               // named barrier of the row-thread exchanges
+constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
+constexpr uint32_t kIdescO256 = idesc_bf16(128, 256, false, true);
+// paged: one page's part of a K group ([8 groups][3 chunks][1 KB]) and of a V
+// half ([8 groups][4 chunks][1 KB])
+constexpr int kGroupPage = 3 * kPage * 128;        // 24 KB
+constexpr int kHalfPage = 4 * kPage * 128;         // 32 KB
+static_assert(2 * kGroupPage == kKGroupBytes && 4 * kHalfPage == kVGroups * kVGroupBytes, "paged regions");
+constexpr uint32_t kRowThreads = 128;              // warps 4..7
+// Softmax: one pass over S per tile after a piece's first (the row max comes
+// with the probabilities; a row whose reference must move redoes the pass).
+constexpr bool kSinglePass = true;
+constexpr uint32_t kXferNamedThreads = 160;        // dense: warps 3..7
 
 struct Bars {
-  // score CTA
-  uint64_t kfull[kKGroups], kempty[kKGroups];      // K ring (group 2 includes chunk 7's buffer)
-  uint64_t c7empty[2];                             // chunk-7 buffers, released by the P.V tail
-  uint64_t q_full, q_free, s_full, s_free;
-  uint64_t p_ready, p_tmem_free, o_tail_full;
-  uint64_t p_free[2];                              // arrived by the output CTA
-  // output CTA
-  uint64_t vfull[kVGroups], vempty[kVGroups];      // V ring
-  uint64_t p_full[2];                              // completed by the bulk copies
-  uint64_t p_tmem_full, pv_done, o_full;
-  uint64_t side_read[2];                           // row warps have read P buffer b
+  uint64_t kfull[kKGroups], kempty[kKGroups];      // score CTA K ring
+  uint64_t vfull[kVGroups], vempty[kVGroups];      // output CTA V ring
+  uint64_t q_full, q_free, s_full[2], s_free[2];   // score CTA
+  uint64_t p_free[2];                              // score CTA, arrived by the output CTA
+  uint64_t p_full[2];                              // output CTA, completed by bulk copies
+  uint64_t pv_done[2], o_full, o_free, o_drained, o_rescaled;  // output CTA
+  uint64_t side_read[2];                           // output CTA: row threads read P's side data
   uint32_t tmem_base;
   uint32_t abort;
 };
-constexpr int kSmemBytes = kBarOffset + 1024 + 1024;  // + barriers + alignment slack
+constexpr int kSmemBytes = kEpi + 4 * 4096 + 1024;
+static_assert(kBarOffset % 16 == 0, "barrier block alignment");
 static_assert(sizeof(Bars) <= 1024, "barrier block size");
-static_assert(kRedSum + 2048 <= kBarOffset && kEpi + 8 * 2048 <= kBarOffset && kBarOffset % 1024 == 0,
-              "CTA layouts");
+static_assert(kStage + kXferBytes <= kBarOffset, "score CTA layout");
 static_assert(kXferBytes <= kPBufStride && kXferBytes % 16 == 0, "P transfer size");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // Sparse: the index list entries of key slots 128 t + 4 lane .. + 3 of
-// sequence q (-1 past its n_slots = topk or topk_length).
+// sequence q (-1 past its n_slots = topk or topk_length); validated by the caller.
 __device__ __forceinline__ void load_idx4(const SplitParams& p, int q, int t, int lane, int n_slots,
                                           int32_t (&id)[4]) {
   const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
@@ -147,23 +135,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// Score CTA: the K tile's chunk c lands at this shared-memory offset for tile
-// counter tc (chunk 7 alternates between two buffers).
-__device__ __forceinline__ uint32_t k_chunk_offset(int c, uint32_t tc) {
-  if (c < 6) return static_cast<uint32_t>(c * kChunk);
-  if (c == 6) return kKSlot2;
-  if (c == 7) return kC7 + (tc & 1) * kChunk;
-  return kKSlot2 + kChunk;  // c == 8: RoPE columns
-}
-
-// One CTA per SM (shared memory); up to 168 registers per thread (12 warps,
-// three per sub-partition), so a row thread's 64 scores stay in registers.
+// One CTA per SM (shared memory); up to 224 registers per thread (8 warps, two
+// per sub-partition), so each row thread's 128 scores stay in registers.
 // kSparse: keys are pool rows named by p.indices (DSA top-k, -1 = none), read
 // with tile::gather4 (the tensor map's box is one row); otherwise pages of the
-// block table, read as [64 rows x 64 columns] boxes.
+// block table.  Paged: tm_qa, tm_qb view the cache as [8-token groups][9
+// chunks][8 rows][64 columns] and load one page's [8][4][8][64] (V half) and
+// [8][3][8][64] (K group) boxes; tm_kv is then unused.
 template <bool kSparse>
-__global__ void __launch_bounds__(kThreads, 1)
-    mla_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ SplitParams p) {
+__global__ void __maxnreg__(224)
+    mla_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qa,
+                    const __grid_constant__ CUtensorMap tm_qb, const __grid_constant__ SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -175,29 +157,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKGroups; ++i) {
-      mbar_init(smem_u32(&bars->kfull[i]), 3);  // three chunks per group
+      mbar_init(smem_u32(&bars->kfull[i]), kSparse ? 3 : 1);  // sparse: three chunks per group
       mbar_init(smem_u32(&bars->kempty[i]), 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars->c7empty[b]), 1);
-    mbar_init(smem_u32(&bars->q_full), 8);  // one arrive per row warp
-    mbar_init(smem_u32(&bars->q_free), 1);
-    mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->s_free), 8);
-    mbar_init(smem_u32(&bars->p_ready), 8);
-    mbar_init(smem_u32(&bars->p_tmem_free), 1);
-    mbar_init(smem_u32(&bars->o_tail_full), 1);
     for (int i = 0; i < kVGroups; ++i) {
-      mbar_init(smem_u32(&bars->vfull[i]), i < kVGroups - 1 ? 2 : 1);  // chunks per quarter
+      // sparse: two chunks per d quarter; paged: vfull[0], vfull[1] are the V halves
+      mbar_init(smem_u32(&bars->vfull[i]), kSparse ? 2 : 1);
       mbar_init(smem_u32(&bars->vempty[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->q_full), 4);
+    mbar_init(smem_u32(&bars->q_free), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->s_full[b]), 1);
+      mbar_init(smem_u32(&bars->s_free[b]), 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars->p_free[b]), 1);
       mbar_init(smem_u32(&bars->p_full[b]), 1);
-      mbar_init(smem_u32(&bars->side_read[b]), 8);
+      mbar_init(smem_u32(&bars->pv_done[b]), 1);
+      mbar_init(smem_u32(&bars->side_read[b]), 4);
     }
-    mbar_init(smem_u32(&bars->p_tmem_full), 8);
-    mbar_init(smem_u32(&bars->pv_done), 1);
     mbar_init(smem_u32(&bars->o_full), 1);
+    mbar_init(smem_u32(&bars->o_free), 4);
+    mbar_init(smem_u32(&bars->o_drained), 1);
+    mbar_init(smem_u32(&bars->o_rescaled), 4);
     bars->abort = 0;
     fence_mbarrier_init();
     if (rank == 1) {  // both P buffers start empty and armed for their first copy
@@ -218,8 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait_primary();
   pdl_launch_dependents();  // the combine may launch now; it waits for this grid to finish
   // Schedule B (whole sequences) is walked when it is at most kSplitPenalty
-  // tiles longer than A: every extra piece costs a Q load and an epilogue and
-  // every split row a combine read.
+  // tiles longer than A: on b=64, t=4096 (~2.3 us per dense tile) splitting
+  // over 76 parts cost ~26 us in extra pieces and the combine for ~12 us of
+  // better balance; a sparse tile takes about twice as long.
   constexpr int kSplitPenalty = kSparse ? 5 : 11;
   // The metadata must describe this call; otherwise nothing is read or written.
   const bool meta_ok = meta_header_matches(p.meta, p.batch, p.s_q, p.num_parts, p.topk, p.causal);
@@ -245,21 +229,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ score CTA
     if (warp == 0 || warp == 2 || (kSparse && warp == 3)) {
       // ---------------------------------------------------- K tile producers
-      // Dense: lane 0 of warps 0, 2 loads each chunk as two page boxes.
+      // Paged: lane 0 of warp 0 loads each group as one box per page.
       // Sparse: warps 0, 2, 3 share the chunks (one gather4 costs its warp
       // ~80 clk to issue, so gathers need more issuing warps); lane L gathers
-      // rows 4L..4L+3 of the tile for each chunk; lane 0 owns the barriers.
-      // Chunks 0..6 and 8 reuse their group's slot once that group's QK is
-      // done; chunk 7 alternates between two buffers, each free once the P.V
-      // tail of the tile two back has read it.
-      if (lane == 0 || kSparse) {
+      // rows 4L..4L+3 of the tile for each chunk (invalid slots fetch pool
+      // row 0; the softmax gives them zero weight); lane 0 owns the barriers.
+      // Each group of 3 chunks has a chunk of every issuer, so each issuer
+      // waits on every slot in order.
+      if ((lane == 0 || kSparse) && (kSparse || warp == 0)) {
         constexpr int kIssuers = kSparse ? 3 : 2;
         const int pw = warp == 0 ? 0 : warp - 1;
         const uint64_t pol = l2_policy_evict_first();
         PartCursor cur = part_cursor(meta, part);
         int q, t0, t1, split;
         uint32_t tc = 0;
-        int32_t issued[kKGroups];  // ring round of this issuer's last load per group
+        int32_t issued[kKGroups];  // ring round of this issuer's last load per group slot
         for (int i = 0; i < kKGroups; ++i) issued[i] = -1;
         bool ok = true;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
@@ -290,30 +274,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 y[h2] = blk * kPage;
               }
             }
-            for (int c = pw; c < kChunks && ok; c += kIssuers) {
-              const int g = c / 3;
-              if (lane == 0) {
-                // every chunk waits for its group's previous round to be consumed,
-                // so no arrival can land in a phase of kfull[g] before the
-                // previous phase has completed (chunk 7's own buffers are fresh
-                // for the first two tiles and would not hold it back); chunk 7
-                // also waits for its buffer's last P.V tail
+            if constexpr (!kSparse) {
+              for (int g = 0; g < kKGroups && ok; ++g) {
                 ok = mbar_wait(smem_u32(&bars->kempty[g]), (tc & 1) ^ 1, abort_flag, p.err);
-                if (ok && c == 7)
-                  ok = mbar_wait(smem_u32(&bars->c7empty[tc & 1]), ((tc >> 1) & 1) ^ 1, abort_flag, p.err);
-                if (ok) mbar_arrive_expect_tx(smem_u32(&bars->kfull[g]), kChunk);
+                if (!ok) break;
+                const uint32_t bar = smem_u32(&bars->kfull[g]);
+                mbar_arrive_expect_tx(bar, kKGroupBytes);
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2)  // the page's first 8-token group is y / 8
+                  tma_load_4d(base + g * kKGroupBytes + h2 * kGroupPage, &tm_qb, 0, 0, 3 * g, y[h2] / 8, bar, pol);
+                issued[g] = static_cast<int32_t>(tc);
+              }
+            }
+            for (int c = pw; kSparse && c < kChunks && ok; c += kIssuers) {
+              const int g = c / 3;
+              const uint32_t slot = g, round = tc;  // one ring round per tile
+              if (lane == 0) {
+                ok = mbar_wait(smem_u32(&bars->kempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
+                if (ok) mbar_arrive_expect_tx(smem_u32(&bars->kfull[slot]), kChunk);
               }
               if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
               if (!ok) break;
-              const uint32_t bar = smem_u32(&bars->kfull[g]);
-              const uint32_t dst = base + k_chunk_offset(c, tc);
-              if constexpr (kSparse) {
-                tma_gather4(dst + 4 * lane * 128, &tm_kv, c * 64, y[0], y[1], y[2], y[3], bar);
-              } else {
-                tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol);
-                tma_load_2d(dst + kChunk / 2, &tm_kv, c * 64, y[1], bar, pol);
-              }
-              issued[g] = static_cast<int32_t>(tc);
+              const uint32_t bar = smem_u32(&bars->kfull[slot]);
+              const uint32_t dst = base + slot * kKGroupBytes + (c - 3 * g) * kChunk;
+              tma_gather4(dst + 4 * lane * 128, &tm_kv, c * 64, y[0], y[1], y[2], y[3], bar);
+              issued[slot] = static_cast<int32_t>(round);
             }
           }
         }
@@ -328,97 +313,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == 1) {
-      // ---------------------------------------------------- S = Q . K^T, O tail += P . V
-      // Per tile: QK of tile tc (after the row threads have loaded S of tile
-      // tc - 1), then the P.V tail of tile tc - 1 (its P is ready about when
-      // QK of tile tc is issued).  The last tile's tail follows the piece.
+      // ---------------------------------------------------- S = Q . K^T
       if (lane == 0) {
         PartCursor cur = part_cursor(meta, part);
         int q, t0, t1, split;
         uint32_t tc = 0, item = 0;
         bool ok = true;
-        const uint64_t rope_desc = sw128_desc(base + kQRope, 16, 1024);
-        // O[:, 448:512] (+)= P(u) . chunk 7 of tile u
-        auto pv_tail = [&](uint32_t u, bool first) {
-          ok = mbar_wait(smem_u32(&bars->p_ready), u & 1, abort_flag, p.err);
-          if (!ok) return;
-          tc_fence_after();
-          const uint64_t vdesc = sw128_desc(base + kC7 + (u & 1) * kChunk, kChunk, 1024);
-#pragma unroll
-          for (int s = 0; s < 8; ++s)
-            mma_bf16_ts(tmem + kOTailCol, tmem + kPColS + 8 * s, vdesc + static_cast<uint64_t>((2048 * s) >> 4),
-                        kIdescO64, (!first || s != 0) ? 1u : 0u);
-          mma_commit(smem_u32(&bars->c7empty[u & 1]));
-          mma_commit(smem_u32(&bars->p_tmem_free));
-        };
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           if (ok) ok = mbar_wait(smem_u32(&bars->q_full), item & 1, abort_flag, p.err);
+          const uint64_t rope_desc = sw128_desc(base + kQRope, 16, 1024);
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
-            ok = mbar_wait(smem_u32(&bars->s_free), (tc & 1) ^ 1, abort_flag, p.err);
+            const uint32_t sb = tc & 1;
+            ok = mbar_wait(smem_u32(&bars->s_free[sb]), ((tc >> 1) & 1) ^ 1, abort_flag, p.err);
             if (!ok) continue;
             tc_fence_after();
-            const uint32_t d = tmem + kSCol;
+            const uint32_t d = tmem + kSCol + 128 * sb;
 #pragma unroll
-            for (int g = 0; g < kKGroups; ++g) {
-              ok = mbar_wait(smem_u32(&bars->kfull[g]), tc & 1, abort_flag, p.err);
+            for (int g = 0; g < 3; ++g) {
+              const uint32_t slot = g;  // group g of every tile lives in slot g
+              ok = mbar_wait(smem_u32(&bars->kfull[slot]), tc & 1, abort_flag, p.err);
               if (!ok) break;
               tc_fence_after();
+              // paged: chunk 3g + cc at +1 KB cc, 8-token groups 3 KB apart;
+              // sparse: [128 tokens x 128 B] chunks 16 KB apart
+              const uint64_t bdesc = sw128_desc(base + slot * kKGroupBytes, 16, kSparse ? 1024 : 3072);
 #pragma unroll
-              for (int cc = 0; cc < 3; ++cc) {
-                const int c = 3 * g + cc;
-                const uint64_t bdesc = sw128_desc(base + k_chunk_offset(c, tc), 16, 1024);
+              for (int cc = 0; cc < 3; ++cc)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  const uint64_t b = bdesc + static_cast<uint64_t>((32 * k) >> 4);
-                  const uint32_t acc = (c | k) != 0 ? 1u : 0u;
-                  if (c < 8)  // latent columns: A = Q in TMEM
-                    mma_bf16_ts(d, tmem + kQCol + 8 * (4 * c + k), b, kIdescS, acc);
-                  else  // RoPE columns: A = Q's RoPE part in shared memory
+                  const uint64_t b = bdesc + static_cast<uint64_t>(((kSparse ? cc * kChunk : cc * 1024) + 32 * k) >> 4);
+                  const uint32_t acc = (g | cc | k) != 0 ? 1u : 0u;
+                  if (3 * g + cc < 8)  // latent columns: A = Q in TMEM
+                    mma_bf16_ts(d, tmem + kQCol + 8 * (4 * (3 * g + cc) + k), b, kIdescS, acc);
+                  else  // RoPE columns: A = Q RoPE part in smem
                     mma_bf16_ss(d, rope_desc + static_cast<uint64_t>((32 * k) >> 4), b, kIdescS, acc);
                 }
-              }
-              mma_commit(smem_u32(&bars->kempty[g]));  // chunk 7's buffer is released by the tail
+              mma_commit(smem_u32(&bars->kempty[slot]));
             }
             if (!ok) continue;
-            mma_commit(smem_u32(&bars->s_full));
+            mma_commit(smem_u32(&bars->s_full[sb]));
             if (t == t1 - 1) mma_commit(smem_u32(&bars->q_free));
-            if (t > t0) pv_tail(tc - 1, t - 1 == t0);
-          }
-          if (ok && t1 > t0) {
-            pv_tail(tc - 1, t1 - 1 == t0);
-            if (ok) mma_commit(smem_u32(&bars->o_tail_full));
           }
           ++item;
         }
       }
-    } else if (warp >= 4) {
-      // ---------------------------------------------------- Q load, softmax, P, O tail
-      // Thread (h, r) owns tokens 64h .. 64h + 63 of query row r: its scores
-      // are TMEM lane r, columns 64h .., so the 64 scores of a tile are loaded
-      // into registers at once, which frees S for the next tile's QK.
-      // Probabilities are taken against a per-row reference m (log2 units):
-      // the first tile of a piece sets it to that tile's row max; a later
-      // tile moves it only when a score exceeds it by more than kRescaleLog2,
-      // and then O and the sums are rescaled by alpha = 2^(m_old - m_new).
-      // The two threads of a row meet (named barrier 3, partial maxima in
-      // shared memory) on a piece's first tile, and on a later tile only when
-      // some row of the CTA has to move its reference.  Two running sums per
-      // thread: of the fp32 probabilities (for the LSE) and of their bf16
-      // roundings, which are the weights the PV product multiplies (to
-      // normalise O); the halves add theirs at the piece's end.
-      const int h = warp >= 8 ? 1 : 0;
-      const int r = 32 * (warp & 3) + lane;
-      const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    } else if (warp >= 4 && warp < 8) {
+      // ---------------------------------------------------- Q load, softmax, P
+      // Thread r owns query row r: its scores are TMEM lane r, so the row max
+      // and sums need no cross-thread exchange.  Probabilities are taken
+      // against a per-row reference m (log2 units): the first tile of a piece
+      // sets it to that tile's row max; a later tile moves it only when a
+      // score exceeds it by more than kRescaleLog2, and then O and the sums
+      // are rescaled by alpha = 2^(m_old - m_new).  Two running sums: of the
+      // fp32 probabilities (for the LSE) and of their bf16 roundings, which
+      // are the weights the PV product multiplies (to normalise O).
+      const int r = threadIdx.x - 128;
+      const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
       const uint32_t t_q = tmem + lane_off + kQCol;
-      const uint32_t t_s = tmem + lane_off + kSCol + 64 * h;
-      const uint32_t t_p = tmem + lane_off + kPColS + 32 * h;
-      const uint32_t t_ot = tmem + lane_off + kOTailCol + 32 * h;
       const uint32_t stage = base + kStage;
-      const uint32_t prow = stage + h * 16384 + (r >> 3) * 1024 + (r & 7) * 128;  // staging chunk h, row r
+      const uint32_t prow = stage + (r >> 3) * 1024 + (r & 7) * 128;
       const uint32_t qrope_row = base + kQRope + (r >> 3) * 1024 + (r & 7) * 128;
-      float* red_max = reinterpret_cast<float*>(smem + kRedMax);  // [parity][half][row]
-      float* red_sum = reinterpret_cast<float*>(smem + kRedSum);  // [lsum, bsum][half][row]
       const float sc = p.scale_log2;
       PartCursor cur = part_cursor(meta, part);
       int q, t0, t1, split;
@@ -428,40 +383,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t* srec = meta_seq(meta, p.num_parts, q);
         const int32_t keys = srec[kSKeys];
         // Q row r of token q: 512 latent columns -> TMEM (bf16 pairs, even k in
-        // the low half), 64 RoPE columns -> smem (128-byte swizzled row r).
-        // 72 16-byte units = nine blocks of 8 (blocks 0..7 latent, block 8
-        // RoPE); half 0 loads blocks 0..3, half 1 blocks 4..8, two blocks (16
-        // loads in flight) per round (sparse: one).
+        // the low half), 64 RoPE columns -> smem (128-byte swizzled row r)
         if (ok) ok = mbar_wait(smem_u32(&bars->q_free), (item & 1) ^ 1, abort_flag, p.err);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
           tc_fence_after();
           const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(q) * kRows + r) * kDqk);
-          const int n_blk = h == 0 ? 4 : 5;  // h = 0: blocks 0..3; h = 1: blocks 4..8
-          constexpr int kStep = kSparse ? 1 : 2;  // sparse keeps index registers live: one block per round
-#pragma unroll 1
-          for (int k = 0; k < n_blk; k += kStep) {
-            const int blk = 4 * h + k;
-            const bool two = kStep == 2 && k + 1 < n_blk;
-            uint4 v[16];
+          // 72 16-byte units = nine blocks of 8 (blocks 0..7 latent, block 8 RoPE),
+          // read three blocks per round so that 24 loads are in flight at once
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = ldg_nc_v4(qrow + 8 * blk + i);
-            if (two) {
+          for (int rnd = 0; rnd < 3; ++rnd) {
+            uint4 v[24];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) v[8 + i] = ldg_nc_v4(qrow + 8 * (blk + 1) + i);
-            }
+            for (int i = 0; i < 24; ++i) v[i] = ldg_nc_v4(qrow + 24 * rnd + i);
 #pragma unroll
-            for (int bb = 0; bb < 2; ++bb) {
-              if (bb == 1 && !two) break;
-              if (blk + bb < kDv / 64) {
+            for (int bb = 0; bb < 3; ++bb) {
+              const int blk = 3 * rnd + bb;
+              if (blk < kDv / 64) {
                 uint32_t w[32];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   w[4 * i] = v[8 * bb + i].x; w[4 * i + 1] = v[8 * bb + i].y;
                   w[4 * i + 2] = v[8 * bb + i].z; w[4 * i + 3] = v[8 * bb + i].w;
                 }
-                tmem_st32u(t_q + 32 * (blk + bb), w);
-              } else {  // block 8: the RoPE columns
+                tmem_st32u(t_q + 32 * blk, w);
+              } else {
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                   st_shared_v4(qrope_row + ((u ^ (r & 7)) << 4), v[8 * bb + u].x, v[8 * bb + u].y,
@@ -469,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          if (h == 0 && r == 0) {  // the next piece's query rows (147 KB, contiguous) start towards L2
+          if (r == 0) {  // the next piece's query rows (147 KB, contiguous) start towards L2
             PartCursor nc = cur;
             int nq, nt0, nt1, nsplit;
             if (next_piece(meta, p.num_parts, &nc, &nq, &nt0, &nt1, &nsplit))
@@ -481,105 +427,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->q_full));
-        float m_use = 0.f, lsum = 0.f, bsum = 0.f, inv_l = 0.f;
+        float m_use = 0.f, lsum = 0.f, bsum = 0.f;
         for (int t = t0; t < t1; ++t, ++tc) {
-          // sparse: bit L of vm[k] = key slot t * 128 + 64 h + 32 k + L names a pool row
-          uint32_t vm[2] = {~0u, ~0u};
-          int32_t sid[2];  // sparse: requested before the S wait, used after it
+          const uint32_t sb = tc & 1;
+          const uint32_t t_s = tmem + lane_off + kSCol + 128 * sb;
+          // sparse: bit L of vm[k] = key slot t * 128 + 32 k + L names a pool row
+          uint32_t vm[4] = {~0u, ~0u, ~0u, ~0u};
+          int32_t sid[4];  // sparse: requested before the S wait, used after it
           if constexpr (kSparse) {
             const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int slot = t * kTileTokens + 64 * h + 32 * k + lane;
+            for (int k = 0; k < 4; ++k) {
+              const int slot = t * kTileTokens + 32 * k + lane;
               sid[k] = slot < keys ? idx_row[slot] : -1;
             }
           }
-          // this thread's 64 scores of the tile, into registers; S is then free
-          float s[64];
-          if (ok) ok = mbar_wait(smem_u32(&bars->s_full), tc & 1, abort_flag, p.err);
+          if (ok) ok = mbar_wait(smem_u32(&bars->s_full[sb]), (tc >> 1) & 1, abort_flag, p.err);
           ok = __all_sync(0xffffffffu, ok);
-          if (ok) {
-            tc_fence_after();
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              float v[32];
-              tmem_ld32(t_s + 32 * i, v);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) s[32 * i + j] = v[j];
-            }
-            tmem_wait_ld();
-            tc_fence_before();
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
           if constexpr (kSparse) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
+            for (int k = 0; k < 4; ++k)
               vm[k] = __ballot_sync(0xffffffffu, sid[k] >= 0 && static_cast<int64_t>(sid[k]) < p.s_kv);
           }
-          // masked keys: -inf by selection (keys past the end, slots naming no row)
-          const int n_valid = keys - t * kTileTokens - 64 * h;  // < 64 only on the last tile
-          if (!kSparse && n_valid < 64) {
+          const int n_valid = keys - t * kTileTokens;  // >= 1; < 128 only on the last tile
+          const bool full = kSparse || n_valid >= kTileTokens;
+          // Row max (raw scores; the scale is positive).  The first tile of a
+          // piece reads S once for it (pass 1); later tiles take it from the
+          // probabilities pass, against the current reference, and redo that
+          // pass only in the rare rows whose reference has to move.
+          float u = -INFINITY;
+          if (ok && (t == t0 || !kSinglePass)) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+              float v[32];
+              tmem_ld32(t_s + 32 * i, v);
+              tmem_wait_ld();
+              if (!full) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) s[j] = j < n_valid ? s[j] : -INFINITY;
-          }
-          if constexpr (kSparse) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) s[j] = (vm[j >> 5] >> (j & 31)) & 1u ? s[j] : -INFINITY;
-          }
-          // Row max.  The first tile of a piece sets the reference to it; a
-          // later tile moves the reference only when its max exceeds it by
-          // more than kRescaleLog2 (O and the sums are then rescaled by alpha).
-          float alpha = 1.f;
-          {
-            float u = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 64; j += 2) u = fmax3(u, s[j], s[j + 1]);
-            u *= sc;
-            // a later tile meets its partner only when some row must move
-            const bool meet = t == t0 || named_barrier_or(kRowExchange, kRowThreads, u > m_use + kRescaleLog2);
-            if (meet) {
-              float* slot = red_max + (tc & 1) * 256;
-              slot[128 * h + r] = u;
-              named_barrier_sync(kRowExchange, kRowThreads);
-              u = fmaxf(u, slot[128 * (h ^ 1) + r]);
-              if (t == t0) {
-                m_use = u == -INFINITY ? 0.f : u;
-              } else if (u > m_use + kRescaleLog2) {
-                alpha = fast_exp2(m_use - u);
-                m_use = u;
-                lsum *= alpha;
-                bsum *= alpha;
+                for (int j = 0; j < 32; ++j) v[j] = 32 * i + j < n_valid ? v[j] : -INFINITY;
               }
+              if constexpr (kSparse) {
+                const uint32_t w = vm[0] * (i == 0) | vm[1] * (i == 1) | vm[2] * (i == 2) | vm[3] * (i == 3);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = (w >> j) & 1u ? v[j] : -INFINITY;
+              }
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) u = fmax3(u, v[j], v[j + 1]);
             }
           }
-          // the staging buffer is free once the previous bulk copy has read it
+          u *= sc;
+          float alpha = 1.f;
+          if (t == t0) {
+            m_use = u == -INFINITY ? 0.f : u;
+          } else if (!kSinglePass && u > m_use + kRescaleLog2) {
+            alpha = fast_exp2(m_use - u);
+            m_use = u;
+            lsum *= alpha;
+            bsum *= alpha;
+          }
+          // pass 2: p = 2^(s * scale - m) -> bf16 P row r in the staging buffer
+          // (two 64-token chunks, 128-byte swizzle), and the two sums
           if constexpr (kSparse) {
-            if (h == 0 && r == 0 && tc > 0) bulk_wait_read_all();
+            if (r == 0 && tc > 0) bulk_wait_read_all();  // the previous copy has read the staging
             named_barrier_sync(1, kRowThreads);
           } else {
             named_barrier_sync(1, kXferNamedThreads);  // warp 3's previous copy has read the staging
           }
-          // P in TMEM is free once the previous tile's P.V tail has read it
-          if (ok) ok = mbar_wait(smem_u32(&bars->p_tmem_free), (tc & 1) ^ 1, abort_flag, p.err);
-          ok = __all_sync(0xffffffffu, ok);
-          // p = 2^(s * scale - m) -> bf16: this thread's 64 P values into TMEM
-          // and into staging chunk h (128-byte swizzle), and the two sums
-          // (tcgen05.st is warp-wide, so the warp runs this together)
+          if (ok && kSinglePass && t != t0) tc_fence_after();
           float ls = 0.f, bs = 0.f, ls2 = 0.f, bs2 = 0.f;
-          if (ok) {
-            tc_fence_after();
+          for (bool again = ok; again;) {
+            again = false;
             const float neg_m = -m_use;
+            float xm = -INFINITY;  // raw row max seen by this pass
+            ls = 0.f; bs = 0.f; ls2 = 0.f; bs2 = 0.f;
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+              float v[32];
+              tmem_ld32(t_s + 32 * i, v);
+              tmem_wait_ld();
+              if (!full) {  // keys past the end: s = -inf, p = 2^-inf = 0
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
+                for (int j = 0; j < 32; ++j) v[j] = 32 * i + j < n_valid ? v[j] : -INFINITY;
+              }
+              if constexpr (kSparse) {  // slots without a pool row: p = 0
+                const uint32_t w = vm[0] * (i == 0) | vm[1] * (i == 1) | vm[2] * (i == 2) | vm[3] * (i == 3);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = (w >> j) & 1u ? v[j] : -INFINITY;
+              }
               // packed fp32x2 FMA/adds: one instruction per key pair
               uint32_t pk[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
+                if constexpr (kSinglePass) xm = fmax3(xm, v[2 * j], v[2 * j + 1]);
                 float x0, x1;
                 asm("{ .reg .b64 a, b, c, d; mov.b64 a, {%2, %3}; mov.b64 b, {%4, %4}; mov.b64 c, {%5, %5};"
                     " fma.rn.f32x2 d, a, b, c; mov.b64 {%0, %1}, d; }"
-                    : "=f"(x0), "=f"(x1) : "f"(s[32 * i + 2 * j]), "f"(s[32 * i + 2 * j + 1]), "f"(sc), "f"(neg_m));
+                    : "=f"(x0), "=f"(x1) : "f"(v[2 * j]), "f"(v[2 * j + 1]), "f"(sc), "f"(neg_m));
                 const float e0 = fast_exp2(x0);
                 const float e1 = fast_exp2(x1);
                 pk[j] = pack_bf16x2(e0, e1);
@@ -588,58 +532,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     : "+f"(ls), "+f"(ls2), "+f"(bs), "+f"(bs2)
                     : "f"(e0), "f"(e1), "f"(__uint_as_float(pk[j] << 16)), "f"(__uint_as_float(pk[j] & 0xFFFF0000u)));
               }
-              tmem_st16u(t_p + 16 * i, pk);
+              const uint32_t chunk = prow + (i >> 1) * 16384;
 #pragma unroll
               for (int uu = 0; uu < 4; ++uu)
-                st_shared_v4(prow + (((4 * i + uu) ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2],
-                             pk[4 * uu + 3]);
+                st_shared_v4(chunk + ((((i & 1) * 4 + uu) ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1],
+                             pk[4 * uu + 2], pk[4 * uu + 3]);
             }
+            xm *= sc;
+            const bool move = kSinglePass && t != t0 && xm > m_use + kRescaleLog2;
+            if (move) {  // move the reference; the warp redoes the pass (TMEM loads are warp-wide)
+              const float a_new = fast_exp2(m_use - xm);
+              alpha *= a_new;
+              m_use = xm;
+              lsum *= a_new;
+              bsum *= a_new;
+            }
+            again = __any_sync(0xffffffffu, move);
           }
           const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
-          if (ok) {
-            tmem_wait_st();
-            // this CTA's share of O follows the reference: rescaled after the
-            // previous tile's tail (p_tmem_free) and before this tile's
-            if (t != t0 && any != 0u) {
-              float v[32];
-              tmem_ld32(t_ot, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= alpha;
-              tmem_st32(t_ot, v);
-              tmem_wait_st();
-            }
-            tc_fence_before();
-          }
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready));  // this warp's P of the tile is in TMEM
+          if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[sb]));  // S buffer sb may be rewritten
           lsum += ls + ls2;
           bsum += bs + bs2;
-          const bool last = t == t1 - 1;
-          if (last) {
-            // the two halves of the row add their sums
-            red_sum[128 * h + r] = lsum;
-            red_sum[256 + 128 * h + r] = bsum;
-            named_barrier_sync(kRowExchange, kRowThreads);
-            lsum = h == 0 ? lsum + red_sum[128 + r] : red_sum[r] + lsum;
-            bsum = h == 0 ? bsum + red_sum[256 + 128 + r] : red_sum[256 + r] + bsum;
-            inv_l = bsum > 0.f ? 1.f / bsum : 0.f;
+          st_shared_f32(stage + kSideAlpha + 4 * r, alpha);
+          if (t == t1 - 1) {
+            float inv_l = bsum > 0.f ? 1.f / bsum : 0.f;
             // attention sink: applied with 1/l to a final row, by the combine to a split row
             if (kSparse && p.attn_sink && srec[kSNSplits] == 1) {
               const float lse_t = (lsum > 0.f && bsum > 0.f) ? (m_use + __log2f(lsum)) * 0.69314718055994531f
                                                              : -INFINITY;
               inv_l *= attn_sink_factor(lse_t, p.attn_sink[r]);
             }
+            st_shared_f32(stage + kSideInvL + 4 * r, inv_l);
           }
-          if (h == 0) {
-            st_shared_f32(stage + kSideAlpha + 4 * r, alpha);
-            if (last) st_shared_f32(stage + kSideInvL + 4 * r, inv_l);
-            if (lane == 0) st_shared_u32(stage + kSideFlags + 4 * (warp - 4), any);
-          }
+          if (lane == 0) st_shared_u32(stage + kSideFlags + 4 * (warp - 4), any);
           fence_proxy_async_smem();
           if constexpr (!kSparse) named_barrier_arrive(2, kXferNamedThreads);  // staging full: warp 3 copies
           if constexpr (kSparse) named_barrier_sync(2, kRowThreads);  // staging full
-          if (kSparse && h == 0 && r == 0 && ok) {  // one copy of tile tc into the peer's P buffer tc mod 2
+          if (kSparse && r == 0 && ok) {  // one copy of tile tc into the peer's P buffer tc mod 2
             const uint32_t b = tc & 1;
             ok = mbar_wait_cluster(smem_u32(&bars->p_free[b]), ((tc >> 1) & 1) ^ 1, abort_flag, p.err);
             if (ok) {
@@ -649,47 +580,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // LSE of row r for this piece, and output columns 448 + 32h .. +31
+        // LSE of row r for this piece
         const float lse_v = (lsum > 0.f && bsum > 0.f) ? (m_use + __log2f(lsum)) * 0.69314718055994531f
                                                        : -INFINITY;
-        if (ok) ok = mbar_wait(smem_u32(&bars->o_tail_full), item & 1, abort_flag, p.err);
-        ok = __all_sync(0xffffffffu, ok);
         if (ok) {
-          tc_fence_after();
-          const bool final_out = srec[kSNSplits] == 1;
-          float v[32];
-          tmem_ld32(t_ot, v);
-          tmem_wait_ld();
-          // a row without keys (inv_l = 0) is written as exact zeros: its O
-          // may hold products of zero weights with rows nobody named
-          const float f = inv_l;
-          if (final_out) {
+          if (srec[kSNSplits] == 1) {
             const int b = q / p.s_q, j = q % p.s_q;
-            uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(q) * kRows + r) * kDv + kDvOut + 32 * h);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float* x = &v[8 * u];
-              dst[u] = f != 0.f ? make_uint4(pack_bf16x2(x[0] * f, x[1] * f), pack_bf16x2(x[2] * f, x[3] * f),
-                                             pack_bf16x2(x[4] * f, x[5] * f), pack_bf16x2(x[6] * f, x[7] * f))
-                                : make_uint4(0u, 0u, 0u, 0u);
-            }
-            if (h == 0) p.lse[(static_cast<int64_t>(b) * kRows + r) * p.s_q + j] = lse_v;
+            p.lse[(static_cast<int64_t>(b) * kRows + r) * p.s_q + j] = lse_v;
           } else {
-            const int64_t row = static_cast<int64_t>(srec[kSSplitOff] + split) * kRows + r;
-            float4* dst = reinterpret_cast<float4*>(p.ws_o + row * kDv + kDvOut + 32 * h);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float* x = &v[4 * u];
-              dst[u] = f != 0.f ? make_float4(x[0] * f, x[1] * f, x[2] * f, x[3] * f)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            if (h == 0) p.ws_lse[row] = lse_v;
+            p.ws_lse[static_cast<int64_t>(srec[kSSplitOff] + split) * kRows + r] = lse_v;
           }
-          tc_fence_before();
         }
         ++item;
       }
-      if (kSparse && h == 0 && r == 0) bulk_wait_all();  // the last copy has landed in the peer
+      if (kSparse && r == 0) bulk_wait_all();  // the last copy has landed in the peer
     } else if (warp == 3 && !kSparse) {
       // ---------------------------------------------------- P transfers (dense)
       PartCursor cur = part_cursor(meta, part);
@@ -720,10 +624,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ output CTA
     if (warp == 0 || warp == 2 || (kSparse && warp == 3)) {
       // ---------------------------------------------------- V tile producers
-      // Columns 0..447 (chunks 0..6) of each tile, as four quarters: chunk c
-      // into quarter c / 2.  Dense: lane 0 of warps 0, 2 (chunk c by c mod 2).
-      // Sparse: warps 0, 2, 3 gather (chunk c by issuer c mod 3).
-      if (lane == 0 || kSparse) {
+      // Paged: lane 0 of warp 0 loads each V half (chunks 0..3, 4..7) as one
+      // box per page.  Sparse: warps 0, 2, 3 gather (chunk c by issuer c mod
+      // 3); each issuer loads into the same d quarters every tile, so it waits
+      // on those slots in order.
+      if ((lane == 0 || kSparse) && (kSparse || warp == 0)) {
         constexpr int kIssuers = kSparse ? 3 : 2;
         const int pw = warp == 0 ? 0 : warp - 1;
         const uint64_t pol = l2_policy_evict_first();
@@ -757,23 +662,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 y[h2] = blk * kPage;
               }
             }
-            for (int c = pw; c < kDvOut / 64 && ok; c += kIssuers) {
-              const int qd = c >> 1;
+            if constexpr (!kSparse) {
+              for (int hf = 0; hf < 2 && ok; ++hf) {
+                ok = mbar_wait(smem_u32(&bars->vempty[hf]), (tc & 1) ^ 1, abort_flag, p.err);
+                if (!ok) break;
+                const uint32_t bar = smem_u32(&bars->vfull[hf]);
+                mbar_arrive_expect_tx(bar, 2 * kHalfPage);
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2)
+                  tma_load_4d(base + hf * 2 * kHalfPage + h2 * kHalfPage, &tm_qa, 0, 0, 4 * hf, y[h2] / 8, bar, pol);
+                issued[hf] = static_cast<int32_t>(tc);
+              }
+            }
+            for (int c = pw; kSparse && c < 8 && ok; c += kIssuers) {
+              const uint32_t gv = 4 * tc + (c >> 1), slot = gv % kVGroups, round = gv / kVGroups;
               if (lane == 0) {
-                ok = mbar_wait(smem_u32(&bars->vempty[qd]), (tc & 1) ^ 1, abort_flag, p.err);
-                if (ok) mbar_arrive_expect_tx(smem_u32(&bars->vfull[qd]), kChunk);
+                ok = mbar_wait(smem_u32(&bars->vempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
+                if (ok) mbar_arrive_expect_tx(smem_u32(&bars->vfull[slot]), kChunk);
               }
               if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
               if (!ok) break;
-              const uint32_t bar = smem_u32(&bars->vfull[qd]);
-              const uint32_t dst = base + qd * kVGroupBytes + (c & 1) * kChunk;
-              if constexpr (kSparse) {
-                tma_gather4(dst + 4 * lane * 128, &tm_kv, c * 64, y[0], y[1], y[2], y[3], bar);
-              } else {
-                tma_load_2d(dst, &tm_kv, c * 64, y[0], bar, pol);
-                tma_load_2d(dst + kChunk / 2, &tm_kv, c * 64, y[1], bar, pol);
-              }
-              issued[qd] = static_cast<int32_t>(tc);
+              const uint32_t bar = smem_u32(&bars->vfull[slot]);
+              const uint32_t dst = base + slot * kVGroupBytes + (c & 1) * kChunk;
+              tma_gather4(dst + 4 * lane * 128, &tm_kv, c * 64, y[0], y[1], y[2], y[3], bar);
+              issued[slot] = static_cast<int32_t>(round);
             }
           }
         }
@@ -788,50 +700,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == 1) {
-      // ---------------------------------------------------- O[:, 0:448] += P . V
+      // ---------------------------------------------------- O += P . V
       if (lane == 0) {
         PartCursor cur = part_cursor(meta, part);
         int q, t0, t1, split;
-        uint32_t tc = 0;
+        uint32_t tc = 0, item = 0, rc = 0;
         bool ok = true;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
-            // P of this tile in TMEM (and O rescaled, and the previous piece's
-            // epilogue done: the row threads do those first)
-            ok = mbar_wait(smem_u32(&bars->p_tmem_full), tc & 1, abort_flag, p.err);
+            const uint32_t b = tc & 1;
+            const uint32_t pbuf = base + kPBuf0 + b * kPBufStride;
+            ok = mbar_wait_cluster(smem_u32(&bars->p_full[b]), (tc >> 1) & 1, abort_flag, p.err);
             if (!ok) continue;
-            tc_fence_after();
-            for (int qd = 0; qd < kVGroups && ok; ++qd) {
-              ok = mbar_wait(smem_u32(&bars->vfull[qd]), tc & 1, abort_flag, p.err);
-              if (!ok) break;
-              tc_fence_after();
-              const uint64_t vdesc = sw128_desc(base + qd * kVGroupBytes, kChunk, 1024);
-              const uint32_t idesc = qd < kVGroups - 1 ? kIdescO128 : kIdescO64;
-#pragma unroll
-              for (int s = 0; s < 8; ++s)
-                mma_bf16_ts(tmem + kOCol + 128 * qd, tmem + kPColO + 8 * s,
-                            vdesc + static_cast<uint64_t>((2048 * s) >> 4), idesc, (t != t0 || s != 0) ? 1u : 0u);
-              mma_commit(smem_u32(&bars->vempty[qd]));
+            if (t == t0) {
+              ok = mbar_wait(smem_u32(&bars->o_free), (item & 1) ^ 1, abort_flag, p.err);
+            } else {
+              const uint4 f = ld_shared_v4(pbuf + kSideFlags);
+              if ((f.x | f.y | f.z | f.w) != 0u) {
+                mma_commit(smem_u32(&bars->o_drained));
+                ok = mbar_wait(smem_u32(&bars->o_rescaled), rc & 1, abort_flag, p.err);
+                ++rc;
+              }
             }
             if (!ok) continue;
-            mma_commit(smem_u32(&bars->pv_done));
+            tc_fence_after();
+            const uint64_t pdesc = sw128_desc(pbuf, 16, 1024);
+            if constexpr (!kSparse) {
+              // paged: V half hf (N = 256: 64-column blocks 1 KB apart, 8-token
+              // groups 4 KB apart) into O columns 256 hf ..
+              for (int hf = 0; hf < 2 && ok; ++hf) {
+                ok = mbar_wait(smem_u32(&bars->vfull[hf]), tc & 1, abort_flag, p.err);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t vdesc = sw128_desc(base + hf * 2 * kHalfPage, 1024, 4096);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                  mma_bf16_ss(tmem + 256 * hf,
+                              pdesc + static_cast<uint64_t>(((s >> 2) * 16384 + (s & 3) * 32) >> 4),
+                              vdesc + static_cast<uint64_t>((8192 * s) >> 4), kIdescO256,
+                              (t != t0 || s != 0) ? 1u : 0u);
+                mma_commit(smem_u32(&bars->vempty[hf]));
+              }
+            }
+            for (int qd = 0; kSparse && qd < 4 && ok; ++qd) {
+              const uint32_t gv = 4 * tc + qd, slot = gv % kVGroups;
+              ok = mbar_wait(smem_u32(&bars->vfull[slot]), (gv / kVGroups) & 1, abort_flag, p.err);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t vdesc = sw128_desc(base + slot * kVGroupBytes, kChunk, 1024);
+#pragma unroll
+              for (int s = 0; s < 8; ++s)
+                mma_bf16_ss(tmem + 128 * qd,
+                            pdesc + static_cast<uint64_t>(((s >> 2) * 16384 + (s & 3) * 32) >> 4),
+                            vdesc + static_cast<uint64_t>((2048 * s) >> 4), kIdescO,
+                            (t != t0 || s != 0) ? 1u : 0u);
+              mma_commit(smem_u32(&bars->vempty[slot]));
+            }
+            if (!ok) continue;
+            mma_commit(smem_u32(&bars->pv_done[b]));
             if (t == t1 - 1) mma_commit(smem_u32(&bars->o_full));
           }
+          ++item;
         }
       }
-    } else if (warp >= 4) {
-      // ---------------------------------------------------- P into TMEM, rescale, epilogue
-      // Thread (h, r): row r (TMEM lane r), P tokens 64h .. 64h + 63 and O
-      // columns 224h .. 224h + 223.
-      const int h = warp >= 8 ? 1 : 0;
-      const int r = 32 * (warp & 3) + lane;
-      const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-      const uint32_t t_o = tmem + lane_off + kOCol + (kDvOut / 2) * h;
-      const uint32_t t_p = tmem + lane_off + kPColO + 32 * h;
+    } else if (warp >= 4 && warp < 8) {
+      // ---------------------------------------------------- rescale, epilogue
+      const int r = threadIdx.x - 128;
+      const uint32_t t_o = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16);
       PartCursor cur = part_cursor(meta, part);
       int q, t0, t1, split;
-      uint32_t tc = 0, item = 0;
+      uint32_t tc = 0, item = 0, rc = 0;
       bool ok = true;
       while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
         const int32_t* srec = meta_seq(meta, p.num_parts, q);
@@ -840,51 +779,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b = tc & 1;
           const uint32_t side = base + kPBuf0 + b * kPBufStride;
           if (ok) ok = mbar_wait_cluster(smem_u32(&bars->p_full[b]), (tc >> 1) & 1, abort_flag, p.err);
-          // the previous tile's P.V is done: O holds it, P in TMEM may be rewritten
-          if (ok && tc > 0) ok = mbar_wait(smem_u32(&bars->pv_done), (tc - 1) & 1, abort_flag, p.err);
           ok = __all_sync(0xffffffffu, ok);
+          float alpha = 1.f;
+          uint32_t any = 0;
           if (ok) {
-            tc_fence_after();
-            const float alpha = ld_shared_f32(side + kSideAlpha + 4 * r);
+            alpha = ld_shared_f32(side + kSideAlpha + 4 * r);
             const uint4 f = ld_shared_v4(side + kSideFlags);
+            any = f.x | f.y | f.z | f.w;
             if (t == t1 - 1) inv_l = ld_shared_f32(side + kSideInvL + 4 * r);
-            if (t != t0 && (f.x | f.y | f.z | f.w) != 0u && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-              for (int blk = 0; blk < kDvOut / 64; ++blk) {
-                float v[32];
-                tmem_ld32(t_o + 32 * blk, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                tmem_st32(t_o + 32 * blk, v);
-              }
-            }
-            // P row r, tokens 64h .. 64h + 63: chunk h of the buffer, 8 swizzled 16-byte units
-            const uint32_t prow_o = side + h * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
-            uint32_t w[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint4 x = ld_shared_v4(prow_o + ((u ^ (r & 7)) << 4));
-              w[4 * u] = x.x; w[4 * u + 1] = x.y; w[4 * u + 2] = x.z; w[4 * u + 3] = x.w;
-            }
-            tmem_st32u(t_p, w);
-            tmem_wait_st();
-            tc_fence_before();
           }
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(smem_u32(&bars->p_tmem_full));
-            mbar_arrive(smem_u32(&bars->side_read[b]));  // done with P buffer b
-          }
+          if (lane == 0) mbar_arrive(smem_u32(&bars->side_read[b]));  // done with the side data
           if (kSparse && warp == 4 && lane == 0 && ok && tc >= 1) {
             // hand P buffer (tc - 1) mod 2 back: every row warp has read tile
-            // tc - 1's buffer; armed for tile tc + 1
+            // tc - 1's side data and its PV has completed; armed for tile tc + 1
             const uint32_t pb = (tc - 1) & 1, ph = ((tc - 1) >> 1) & 1;
             ok = mbar_wait(smem_u32(&bars->side_read[pb]), ph, abort_flag, p.err);
+            if (ok) ok = mbar_wait(smem_u32(&bars->pv_done[pb]), ph, abort_flag, p.err);
             if (ok) {
               mbar_arrive_expect_tx(smem_u32(&bars->p_full[pb]), kXferBytes);
               mbar_remote_arrive(mapa_shared(smem_u32(&bars->p_free[pb]), 0));
             }
+          }
+          if (ok && t != t0 && any != 0u) {
+            ok = mbar_wait(smem_u32(&bars->o_drained), rc & 1, abort_flag, p.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+              tc_fence_after();
+              if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                for (int blk = 0; blk < kDv / 32; ++blk) {
+                  float v[32];
+                  tmem_ld32(t_o + 32 * blk, v);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                  tmem_st32(t_o + 32 * blk, v);
+                }
+                tmem_wait_st();
+              }
+              tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->o_rescaled));
+            ++rc;
           }
         }
         // epilogue: O row r / sum of bf16(p) -> out (single split) or fp32 partial
@@ -892,73 +830,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
           tc_fence_after();
-          // Thread (h, r) holds row r of O's columns 224h ..; each 64-byte slice
-          // of the warp's 32 rows goes through a swizzled 2 KB staging area so
-          // that every global store instruction writes eight whole 64-byte row
-          // segments.
+          // Thread r holds row r of O; each 128-byte slice of the warp's 32 rows
+          // goes through a swizzled 4 KB staging area so that every global
+          // store instruction writes four whole 128-byte row segments.
           const bool final_out = srec[kSNSplits] == 1;
           const int64_t row0 = (final_out ? static_cast<int64_t>(q) : static_cast<int64_t>(srec[kSSplitOff] + split)) *
-                                   kRows + 32 * (warp & 3);
-          const uint32_t stg = base + kEpi + (warp - 4) * 2048;
-          const int rr0 = lane >> 2, uu = lane & 3;
-          const int col0 = (kDvOut / 2) * h;
+                                   kRows + 32 * (warp - 4);
+          const uint32_t stg = base + kEpi + (warp - 4) * 4096;
+          const int rr0 = lane >> 3, uu = lane & 7;
           if (final_out) {
 #pragma unroll 1
-            for (int blk = 0; blk < kDvOut / 64; ++blk) {  // 32 bf16 columns = 64 bytes per row
-              float v[32];
-              tmem_ld32(t_o + 32 * blk, v);
-              tmem_wait_ld();
-              // a row without keys (inv_l = 0) is written as exact zeros: its O
-              // may hold products of zero weights with rows nobody named
-              uint32_t pk[16];
+            for (int blk = 0; blk < kDv / 64; ++blk) {  // 64 bf16 columns = 128 bytes per row
+              uint32_t pk[32];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) pk[i] = inv_l != 0.f ? pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l) : 0u;
+              for (int h2 = 0; h2 < 2; ++h2) {
+                float v[32];
+                tmem_ld32(t_o + 64 * blk + 32 * h2, v);
+                tmem_wait_ld();
+                // a row without keys (inv_l = 0) is written as exact zeros: its O
+                // may hold products of zero weights with rows nobody named
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                st_shared_v4(stg + lane * 64 + ((u ^ (lane & 3)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                for (int i = 0; i < 16; ++i)
+                  pk[16 * h2 + i] = inv_l != 0.f ? pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l) : 0u;
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
                              pk[4 * u + 3]);
               __syncwarp();
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int rr = 8 * j + rr0;
-                const uint4 x = ld_shared_v4(stg + rr * 64 + ((uu ^ (rr & 3)) << 4));
-                *reinterpret_cast<uint4*>(p.out + (row0 + rr) * kDv + col0 + 32 * blk + 8 * uu) = x;
+              for (int j = 0; j < 8; ++j) {
+                const int rr = 4 * j + rr0;
+                const uint4 x = ld_shared_v4(stg + rr * 128 + ((uu ^ (rr & 7)) << 4));
+                *reinterpret_cast<uint4*>(p.out + (row0 + rr) * kDv + 64 * blk + 8 * uu) = x;
               }
               __syncwarp();
             }
           } else {
 #pragma unroll 1
-            for (int blk = 0; blk < kDvOut / 32; ++blk) {  // 16 fp32 columns = 64 bytes per row
-              float v[16];
-              tmem_ld16(t_o + 16 * blk, v);
+            for (int blk = 0; blk < kDv / 32; ++blk) {  // 32 fp32 columns = 128 bytes per row
+              float v[32];
+              tmem_ld32(t_o + 32 * blk, v);
               tmem_wait_ld();
               if (inv_l == 0.f) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
               }
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                st_shared_v4(stg + lane * 64 + ((u ^ (lane & 3)) << 4), __float_as_uint(v[4 * u] * inv_l),
+              for (int u = 0; u < 8; ++u)
+                st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) << 4), __float_as_uint(v[4 * u] * inv_l),
                              __float_as_uint(v[4 * u + 1] * inv_l), __float_as_uint(v[4 * u + 2] * inv_l),
                              __float_as_uint(v[4 * u + 3] * inv_l));
               __syncwarp();
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int rr = 8 * j + rr0;
-                const uint4 x = ld_shared_v4(stg + rr * 64 + ((uu ^ (rr & 3)) << 4));
-                *reinterpret_cast<uint4*>(p.ws_o + (row0 + rr) * kDv + col0 + 16 * blk + 4 * uu) = x;
+              for (int j = 0; j < 8; ++j) {
+                const int rr = 4 * j + rr0;
+                const uint4 x = ld_shared_v4(stg + rr * 128 + ((uu ^ (rr & 7)) << 4));
+                *reinterpret_cast<uint4*>(p.ws_o + (row0 + rr) * kDv + 32 * blk + 4 * uu) = x;
               }
               __syncwarp();
             }
           }
           tc_fence_before();
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));
         ++item;
       }
     } else if (warp == 3 && !kSparse) {
       // ---------------------------------------------------- P buffer hand-back
-      // A P buffer is free once the four row warps have copied it into TMEM
-      // (P.V reads TMEM, not the buffer); armed for the tile two ahead.
       PartCursor cur = part_cursor(meta, part);
       int q, t0, t1, split;
       uint32_t tc = 0;
@@ -968,8 +908,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && ok) {
             const uint32_t b = tc & 1;
             ok = mbar_wait(smem_u32(&bars->side_read[b]), (tc >> 1) & 1, abort_flag, p.err);
+            if (ok) ok = mbar_wait(smem_u32(&bars->pv_done[b]), (tc >> 1) & 1, abort_flag, p.err);
             if (ok) {
-              mbar_arrive_expect_tx(smem_u32(&bars->p_full[b]), kXferBytes);
+              mbar_arrive_expect_tx(smem_u32(&bars->p_full[b]), kXferBytes);  // armed for tile tc + 2
               mbar_remote_arrive(mapa_shared(smem_u32(&bars->p_free[b]), 0));
             }
           }
