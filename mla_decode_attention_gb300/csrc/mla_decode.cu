@@ -130,11 +130,31 @@ int launch_split(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const SplitP
   return e == cudaSuccess ? MLA_OK : record_cuda_error("split kernel launch", e);
 }
 
+// The query rows [n_seq * 128, 576] seen as [9 chunks][rows][64 columns]
+// (chunk stride 128 bytes); boxes of [8 chunks x 128 rows x 64 columns] (the
+// latent part of one token's rows, 128 KB) with 128-byte swizzle.
+bool make_q_latent_map(CUtensorMap* m, const void* q, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {64u, rows, static_cast<cuuint64_t>(kDqk / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDqk) * 2u, 128u};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(pair::kRows), static_cast<cuuint32_t>(kDv / 64)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // tm_qa, tm_qb: the group-interleaved maps of the paged cache (chunks 0..3,
-// 4..6 of a page); the sparse kernel does not read them.
+// 4..6 of a page); the sparse kernel does not read them.  The kernel loads the
+// part's first query rows with the two query maps made here.
 template <bool kSparse>
 int launch_pair(const CUtensorMap& tm_kv, const CUtensorMap& tm_qa, const CUtensorMap& tm_qb,
                 const SplitParams& prm, cudaStream_t stream) {
+  CUtensorMap tm_ql, tm_qr;
+  const uint64_t q_rows = static_cast<uint64_t>(prm.batch) * prm.s_q * pair::kRows;
+  if (!make_q_latent_map(&tm_ql, prm.q, q_rows) || !make_rows_map(&tm_qr, prm.q, q_rows, kDqk * 2, pair::kRows))
+    return record_error("cuTensorMapEncodeTiled failed for the query rows", MLA_ERR_CUDA);
   static int state = 0;  // 0 unset, 1 ok, -1 failed (per instantiation)
   static std::mutex mu;
   {
@@ -163,7 +183,8 @@ int launch_pair(const CUtensorMap& tm_kv, const CUtensorMap& tm_qa, const CUtens
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::mla_pair_kernel<kSparse>, tm_kv, tm_qa, tm_qb, prm);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, pair::mla_pair_kernel<kSparse>, tm_kv, tm_qa, tm_qb, tm_ql, tm_qr, prm);
   return e == cudaSuccess ? MLA_OK : record_cuda_error("pair kernel launch", e);
 }
 

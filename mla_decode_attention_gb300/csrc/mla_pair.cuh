@@ -103,6 +103,7 @@ struct Bars {
   uint64_t kfull[kKGroups], kempty[kKGroups];      // score CTA K ring
   uint64_t vfull[kVGroups], vempty[kVGroups];      // output CTA V ring
   uint64_t q_full, q_free, s_full[2], s_free[2];   // score CTA
+  uint64_t q_tma, q_smem_free;                     // score CTA: the first piece's Q through the K ring
   uint64_t p_free[2];                              // score CTA, arrived by the output CTA
   uint64_t p_full[2];                              // output CTA, completed by bulk copies
   uint64_t pv_done[2], o_full, o_free, o_drained, o_rescaled;  // output CTA
@@ -111,6 +112,10 @@ struct Bars {
   uint32_t abort;
 };
 constexpr int kSmemBytes = kEpi + 4 * 4096 + 1024;
+// The part's first query rows arrive by TMA: the latent columns as [8 chunks]
+// [128 rows][128 B] in the (still empty) K ring, the RoPE columns in kQRope.
+constexpr int kQLatentBytes = 8 * kRows * 128;     // 128 KB
+static_assert(kQLatentBytes <= kQRope, "Q staging in the K ring");
 static_assert(kBarOffset % 16 == 0, "barrier block alignment");
 static_assert(sizeof(Bars) <= 1024, "barrier block size");
 static_assert(kStage + kXferBytes <= kBarOffset, "score CTA layout");
@@ -141,11 +146,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // with tile::gather4 (the tensor map's box is one row); otherwise pages of the
 // block table.  Paged: tm_qa, tm_qb view the cache as [8-token groups][9
 // chunks][8 rows][64 columns] and load one page's [8][4][8][64] (V half) and
-// [8][3][8][64] (K group) boxes; tm_kv is then unused.
+// [8][3][8][64] (K group) boxes; tm_kv is then unused.  tm_ql views the
+// query rows as [9 chunks][rows][64 columns] with [8 x 128 x 64] boxes (the
+// latent part of one token's 128 rows), tm_qr as [rows][576] with [128 x 64]
+// boxes (its RoPE part).
 template <bool kSparse>
 __global__ void __maxnreg__(224)
     mla_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qa,
-                    const __grid_constant__ CUtensorMap tm_qb, const __grid_constant__ SplitParams p) {
+                    const __grid_constant__ CUtensorMap tm_qb, const __grid_constant__ CUtensorMap tm_ql,
+                    const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -167,6 +176,8 @@ __global__ void __maxnreg__(224)
     }
     mbar_init(smem_u32(&bars->q_full), 4);
     mbar_init(smem_u32(&bars->q_free), 1);
+    mbar_init(smem_u32(&bars->q_tma), 1);
+    mbar_init(smem_u32(&bars->q_smem_free), 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars->s_full[b]), 1);
       mbar_init(smem_u32(&bars->s_free[b]), 4);
@@ -214,12 +225,6 @@ __global__ void __maxnreg__(224)
     p.ws_ctrl[0] = meta_ok ? (meta == p.meta ? 0 : 1) : -1;
     if (!meta_ok && p.err) atomicOr(p.err, MLA_DEVERR_METADATA);
   }
-  if (meta_ok && threadIdx.x == 0 && rank == 0) {  // the first piece's query rows start towards L2
-    PartCursor c0 = part_cursor(meta, part);
-    int q0, a0, b0, s0;
-    if (next_piece(meta, p.num_parts, &c0, &q0, &a0, &b0, &s0))
-      prefetch_l2(p.q + static_cast<int64_t>(q0) * kRows * kDqk, kRows * kDqk * 2);
-  }
   const uint32_t tmem = bars->tmem_base;
   volatile uint32_t* abort_flag = &bars->abort;
 
@@ -246,7 +251,22 @@ __global__ void __maxnreg__(224)
         int32_t issued[kKGroups];  // ring round of this issuer's last load per group slot
         for (int i = 0; i < kKGroups; ++i) issued[i] = -1;
         bool ok = true;
+        bool first = true, q_issued = false;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+          if (first) {
+            // the part's first query rows go through the K ring: requested
+            // here, moved into TMEM by the row threads, then the ring is free
+            first = false;
+            if (pw == 0 && lane == 0) {
+              const uint32_t bar = smem_u32(&bars->q_tma);
+              mbar_arrive_expect_tx(bar, kQLatentBytes + kChunk);
+              tma_load_3d(base, &tm_ql, 0, q * kRows, 0, bar, pol);
+              tma_load_2d(base + kQRope, &tm_qr, kDv, q * kRows, bar, pol);
+              q_issued = true;
+            }
+            if (lane == 0) ok = mbar_wait(smem_u32(&bars->q_smem_free), 0, abort_flag, p.err);
+            if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
+          }
           int32_t nid[4];  // sparse: the next tile's indices, requested one tile ahead
           const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
           const int32_t* idx_row = p.indices + static_cast<int64_t>(q) * p.topk;
@@ -303,6 +323,11 @@ __global__ void __maxnreg__(224)
           }
         }
         if (!ok && lane == 0) {  // let this issuer's copies in flight land before the CTA exits
+          if (q_issued) {
+            const uint64_t t_start = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&bars->q_tma), 0) && globaltimer_ns() - t_start < 1000000ull) {
+            }
+          }
           for (int s = 0; s < kKGroups; ++s) {
             if (issued[s] < 0) continue;
             const uint64_t t_start = globaltimer_ns();
@@ -385,8 +410,33 @@ __global__ void __maxnreg__(224)
         // Q row r of token q: 512 latent columns -> TMEM (bf16 pairs, even k in
         // the low half), 64 RoPE columns -> smem (128-byte swizzled row r)
         if (ok) ok = mbar_wait(smem_u32(&bars->q_free), (item & 1) ^ 1, abort_flag, p.err);
+        if (ok && item == 0) ok = mbar_wait(smem_u32(&bars->q_tma), 0, abort_flag, p.err);
         ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
+        if (ok && item == 0) {
+          // row r of the TMA-staged latent part: chunk c at c * 16 KB, row r at
+          // r * 128 B, 16-byte unit u at (u ^ (r mod 8)) * 16 (128-byte swizzle);
+          // the RoPE part already sits in kQRope
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < kDv / 64; ++c) {
+            const uint32_t src = base + c * (kRows * 128) + r * 128;
+            uint32_t w[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint4 x = ld_shared_v4(src + ((u ^ (r & 7)) << 4));
+              w[4 * u] = x.x; w[4 * u + 1] = x.y; w[4 * u + 2] = x.z; w[4 * u + 3] = x.w;
+            }
+            tmem_st32u(t_q + 32 * c, w);
+          }
+          if (r == 0) {  // the next piece's query rows (147 KB, contiguous) start towards L2
+            PartCursor nc = cur;
+            int nq, nt0, nt1, nsplit;
+            if (next_piece(meta, p.num_parts, &nc, &nq, &nt0, &nt1, &nsplit))
+              prefetch_l2(p.q + static_cast<int64_t>(nq) * kRows * kDqk, kRows * kDqk * 2);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+        } else if (ok) {
           tc_fence_after();
           const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(q) * kRows + r) * kDqk);
           // 72 16-byte units = nine blocks of 8 (blocks 0..7 latent, block 8 RoPE),
@@ -426,7 +476,10 @@ __global__ void __maxnreg__(224)
           tc_fence_before();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->q_full));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&bars->q_full));
+          if (item == 0) mbar_arrive(smem_u32(&bars->q_smem_free));  // the K ring may be loaded
+        }
         float m_use = 0.f, lsum = 0.f, bsum = 0.f;
         for (int t = t0; t < t1; ++t, ++tc) {
           const uint32_t sb = tc & 1;
