@@ -221,9 +221,13 @@ def run_ours(args, rank, world, local_rank):
         if sparse:
             if not split_only:
                 binding.mla_get_metadata(None, b, s_q, False, w.topk, parts, buf.metadata, stream)
-            fn = binding.mla_sparse_decode_splitkv if split_only else binding.mla_sparse_decode
-            fn(s["q"], s["kv"], s["indices"], scale, meta, parts, buf.workspace, buf.out,
-               buf.lse, buf.err, stream)
+            if w.prefill and not split_only:  # b query tokens in the prefill call's layouts
+                binding.mla_sparse_prefill(s["q"][:, 0], s["kv"], s["indices"][:, 0], scale, meta, parts,
+                                           buf.workspace, buf.out[:, 0], buf.lse[:, :, 0], buf.err, stream)
+            else:
+                fn = binding.mla_sparse_decode_splitkv if split_only else binding.mla_sparse_decode
+                fn(s["q"], s["kv"], s["indices"], scale, meta, parts, buf.workspace, buf.out,
+                   buf.lse, buf.err, stream)
         elif not split_only:
             binding.mla_get_metadata(s["cache_seqlens"], b, s_q, True, 0, parts, buf.metadata,
                                      stream)
@@ -367,6 +371,12 @@ def run_ours(args, rank, world, local_rank):
     roof_tf = min(peaks["bf16_tflops"], peaks["hbm_gbs"] * ai / 1e3)
     split_gbs = bytes_ / (split_ms * 1e-3) / 1e9
     bound = "hbm" if peaks["hbm_gbs"] * ai / 1e3 < peaks["bf16_tflops"] else "tensor"
+    if w.prefill:
+        # sparse prefill: the pool is read again by every query token, mostly
+        # from L2 (the byte count above counts each gathered row per token);
+        # the pages quote this call in TFLOPS, as compute-bound work
+        bound = "tensor"
+        roof_tf = peaks["bf16_tflops"]
     if bound == "hbm":
         achieved, peak, unit = split_gbs, peaks["hbm_gbs"], "GB/s"
     else:
@@ -425,6 +435,20 @@ def oracle_worker(argv):
     w = workloads.WORKLOADS[cfg]
     inp = workloads.make_inputs(w)
     import torch
+    if w.kind == "sparse":  # n_req query tokens of the top-k sparse workload
+        q = inp["q"].contiguous().view(torch.int16).numpy().view(np.uint16)
+        pool = inp["kv"].contiguous().view(torch.int16).numpy().view(np.uint16)
+        idx = inp["indices"].numpy()
+        toks = [(bi, j) for bi in range(w.b) for j in range(w.s_q)][:n_req]
+        times = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            oracle.sparse_decode(q, pool, idx, inp["softmax_scale"], toks)
+            times.append(time.perf_counter() - t0)
+        valid = [int(((idx[bi, j] >= 0) & (idx[bi, j] < w.s_kv)).sum()) for bi, j in toks]
+        flops, _, _, _ = roofline.sparse_counts(valid, w.h, w.topk)
+        print(json.dumps({"times": times, "flops": flops, "requests": len(toks)}))
+        return
     q = inp["q"].contiguous().view(torch.int16).numpy().view(np.uint16)
     kv = inp["kv_cache"].contiguous().view(torch.int16).numpy().view(np.uint16)
     bt = inp["block_table"].numpy()
@@ -437,6 +461,11 @@ def oracle_worker(argv):
         times.append(time.perf_counter() - t0)
     flops, _, _ = roofline.dense_counts(sl[:min(n_req, w.b)].tolist(), w.s_q, w.h)
     print(json.dumps({"times": times, "flops": flops, "requests": min(n_req, w.b)}))
+
+
+def workloads_module():
+    from mla_decode_attention_gb300 import workloads
+    return workloads
 
 
 def time_oracle(cfg, n_req, reps, threads):
@@ -459,10 +488,12 @@ def cpu_baseline(cfg):
     n_req = max(1, min(64, int(20.0 / per_req)))
     res = time_oracle(cfg, n_req, 1, threads)
     t = res["times"][0]
+    w = workloads_module().WORKLOADS[cfg]
+    what = (f"{res['requests']} of {w.b * w.s_q} query tokens of the same workload (all {w.h} heads, "
+            f"{w.topk} index slots each)" if w.kind == "sparse" else
+            f"{res['requests']} of {w.b} requests of the same workload (all {w.h} heads)")
     return {"value": round(res["flops"] / t / 1e12, 6), "unit": UNIT, "cores": threads,
-            "kind": "oracle",
-            "sample": f"{res['requests']} of 64 requests of the same workload (all 128 heads, "
-                      f"4096 keys each), fp64 numpy, one pass, {t:.2f} s"}
+            "kind": "oracle", "sample": f"{what}, fp64 numpy, one pass, {t:.2f} s"}
 
 
 def run_reference(args):

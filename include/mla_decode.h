@@ -266,6 +266,38 @@ int mla_sparse_decode_splitkv(const void* q, const void* kv, int64_t s_kv, const
                               cudaStream_t stream);
 
 /*
+ * DSA sparse prefill (FlashMLA README, "DeepSeek Sparse Attention (DSA)
+ * Prefill", flash_mla_sparse_fwd): s_q query tokens, each attending to the
+ * pool rows its own index list names.  The same computation as
+ * mla_sparse_decode with each query token as a request of one token
+ * (batch = s_q, s_q = 1), and run by the same kernels; only the argument
+ * shapes follow the prefill interface:
+ *
+ *  q        [s_q, h_q, 576] bf16
+ *  kv       [s_kv, h_kv = 1, 576] bf16 pool (MLA: one latent row per token)
+ *  indices  [s_q, h_kv = 1, topk] int32; -1 marks an invalid slot (other
+ *           out-of-range values are skipped and flagged as for
+ *           mla_sparse_decode)
+ *  softmax_scale  the pages' sm_scale; d_v is 512, the only value they allow
+ *  attn_sink optional [h_q] fp32 (NULL = none), as for mla_sparse_decode
+ *  metadata from mla_get_metadata(topk_length, s_q, 1, 0, topk,
+ *           num_sm_parts, ...); topk_length is NULL or an int32 device
+ *           array [s_q]: token i attends only to its first topk_length[i]
+ *           slots (clamped to [0, topk])
+ *  workspace mla_workspace_size(s_q, 1, h_q, num_sm_parts) bytes
+ *  out      [s_q, h_q, 512] bf16
+ *  lse      [s_q, h_q] fp32 natural-log LSE (the pages' return-value text
+ *           for this call is cut off; this is the decode call's
+ *           [batch, h_q, seq_len_q] with one query token per batch entry)
+ *
+ * Errors, streams and ownership as for mla_sparse_decode.
+ */
+int mla_sparse_prefill(const void* q, const void* kv, int64_t s_kv, const int32_t* indices, int topk,
+                       int s_q, int h_q, float softmax_scale, const float* attn_sink,
+                       const void* metadata, int num_sm_parts, void* workspace, void* out,
+                       float* lse, uint32_t* err, cudaStream_t stream);
+
+/*
  * Failure-path check (no counterpart on the pages): launches one thread that
  * waits on a shared-memory barrier nothing ever completes, through the same
  * bounded wait every kernel of this library uses.  The wait gives up after

@@ -55,6 +55,8 @@ _SIGS = {
                                _vp, _vp, _vp]),
     "mla_sparse_decode_splitkv": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _i, _f, _vp, _vp, _i, _vp,
                                        _vp, _vp, _vp, _vp]),
+    "mla_sparse_prefill": (_i, [_vp, _vp, _i64, _vp, _i, _i, _i, _f, _vp, _vp, _i, _vp, _vp, _vp,
+                                _vp, _vp]),
     "mla_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "mla_check_wait_timeout": (_i, [_vp, _vp]),
 }
@@ -274,6 +276,36 @@ def mla_sparse_decode(q, kv, indices, softmax_scale, metadata, num_sm_parts, wor
     mla_get_metadata in place of cache_seqlens."""
     _sparse_call("mla_sparse_decode", q, kv, indices, softmax_scale, metadata, num_sm_parts,
                  workspace, out, lse, err, stream, attn_sink)
+
+
+def mla_sparse_prefill(q, kv, indices, softmax_scale, metadata, num_sm_parts, workspace, out, lse,
+                       err=None, stream=None, attn_sink=None) -> None:
+    """DSA sparse prefill: q [s_q, h, 576] bf16; kv [s_kv, 576] or [s_kv, 1, 576]
+    bf16; indices [s_q, topk] or [s_q, 1, topk] int32; out [s_q, h, 512] bf16;
+    lse [s_q, h] float32.  metadata from mla_get_metadata(topk_length, s_q, 1,
+    False, topk, ...) (each query token a request of one token)."""
+    _dev(q, torch.bfloat16, "q")
+    if attn_sink is not None:
+        _dev(attn_sink, torch.float32, "attn_sink")
+        if attn_sink.numel() != q.shape[1]:
+            raise ValueError("attn_sink must hold one value per query head")
+    _dev(kv, torch.bfloat16, "kv")
+    _dev(indices, torch.int32, "indices")
+    _dev(metadata, torch.int32, "metadata")
+    _dev(out, torch.bfloat16, "out")
+    _dev(lse, torch.float32, "lse")
+    if err is not None:
+        _dev(err, torch.int32, "err")
+    if q.dim() != 3 or kv.shape[-1] != q.shape[-1] or (kv.dim() == 3 and kv.shape[1] != 1):
+        raise ValueError("q must be [s_q, h, 576] and kv [s_kv, 576] or [s_kv, 1, 576]")
+    s_q, h, _ = q.shape
+    topk = indices.shape[-1]
+    if indices.numel() != s_q * topk:
+        raise ValueError("indices must be [s_q, topk] or [s_q, 1, topk]")
+    _check("mla_sparse_prefill",
+           lib().mla_sparse_prefill(_ptr(q), _ptr(kv), kv.shape[0], _ptr(indices), topk, s_q, h,
+                                    float(softmax_scale), _ptr(attn_sink), _ptr(metadata), num_sm_parts,
+                                    _ptr(workspace), _ptr(out), _ptr(lse), _ptr(err), _stream(stream)))
 
 
 def mla_sparse_decode_splitkv(q, kv, indices, softmax_scale, metadata, num_sm_parts, workspace,

@@ -370,3 +370,15 @@ extern "C" int mla_sparse_decode(const void* q, const void* kv, int64_t s_kv,
   return launch_combine(metadata, batch, s_q, h_q, num_sm_parts, workspace, attn_sink, out, lse, stream,
                         true);
 }
+
+// DSA sparse prefill through the sparse decode path, each query token a
+// request of one token (q [s_q, h_q, 576] is [s_q, 1, h_q, 576], indices
+// [s_q, 1, topk] is [s_q, 1, topk], out [s_q, h_q, 512] is [s_q, 1, h_q, 512],
+// lse [s_q, h_q] is [s_q, h_q, 1]).
+extern "C" int mla_sparse_prefill(const void* q, const void* kv, int64_t s_kv, const int32_t* indices,
+                                  int topk, int s_q, int h_q, float softmax_scale, const float* attn_sink,
+                                  const void* metadata, int num_sm_parts, void* workspace, void* out,
+                                  float* lse, uint32_t* err, cudaStream_t stream) {
+  return mla_sparse_decode(q, kv, s_kv, indices, topk, s_q, 1, h_q, softmax_scale, attn_sink, metadata,
+                           num_sm_parts, workspace, out, lse, err, stream);
+}

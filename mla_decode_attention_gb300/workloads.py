@@ -56,6 +56,7 @@ class Workload:
     topk: int = 0
     invalid_per_row: int = 0  # sparse: indices set to -1 per row
     seed: int = 0
+    prefill: bool = False     # sparse: run through the prefill entry point (b tokens, s_q = 1)
 
 
 # The five graded shapes.  Seeds 1..5 follow the configuration order.
@@ -71,6 +72,12 @@ WORKLOADS = {
     "fp8": Workload("fp8", "fp8", b=64, s_q=1, h=128, seqlens=(8192,) * 64,
                     seed=5),
 }
+# Sparse prefill (FlashMLA README, "DeepSeek Sparse Attention (DSA) Prefill";
+# no shape is given there): a chunk of 2048 query tokens over a 32768-row pool,
+# 2048 index slots per token with the DSA recipe above.  Held as 2048
+# "requests" of one query token each, the layout the prefill call maps to.
+WORKLOADS["sparse_prefill"] = Workload("sparse_prefill", "sparse", b=2048, s_q=1, h=128, s_kv=32768,
+                                       topk=2048, invalid_per_row=102, seed=6, prefill=True)
 
 
 def scaled(w: Workload, **kw) -> Workload:

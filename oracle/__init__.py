@@ -24,6 +24,10 @@ What it computes (one "row" = one query token of one head):
   ``{indices[b, s, k] : index valid}``; each index is a flat pool row
   (page * page_size + offset), -1 marks an invalid slot (FlashMLA README,
   "indices Tensor").
+* Sparse (DSA) prefill (FlashMLA README, "DeepSeek Sparse Attention (DSA)
+  Prefill"): q [s_q, h_q, 576], kv [s_kv, 1, 576], indices [s_q, 1, topk];
+  token i attends to the rows its own index list names, i.e. the sparse decode
+  definition for one request of s_q query tokens (``sparse_prefill``).
 * FP8 cache: 656 bytes per token = 512 e4m3 codes, 4 fp32 scales (one per 128
   channels), 64 bf16 RoPE values (FlashMLA "Hopper FP8 sparse decode" note,
   "The FP8 KVCache Format").
@@ -340,3 +344,25 @@ def sparse_decode(q, kv_pool, indices, softmax_scale, rows=None, attn_sink=None,
         out[bi, j] = o
         lse[bi, :, j] = l
     return out, lse
+
+
+def sparse_prefill(q, kv_pool, indices, softmax_scale, tokens=None, attn_sink=None, topk_length=None):
+    """DSA sparse prefill (FlashMLA README, "DeepSeek Sparse Attention (DSA)
+    Prefill", flash_mla_sparse_fwd): q [s_q, h, 576], kv_pool [s_kv, 576] or
+    [s_kv, 1, 576], indices [s_q, topk] or [s_q, 1, topk] (-1 = invalid),
+    optional attn_sink [h] and topk_length [s_q] as for sparse_decode.
+
+    Each query token attends to the rows its own index list names: the sparse
+    decode definition with each token a request of one query token.  Returns
+    out [s_q, h, 512] and lse [s_q, h] (the decode call's lse [b, h, s_q] with
+    b = s_q tokens of one query each).  ``tokens`` limits the work to those
+    query tokens (others stay NaN)."""
+    q = np.asarray(q)
+    s_q = q.shape[0]
+    pool = np.asarray(kv_pool).reshape(np.asarray(kv_pool).shape[0], -1)
+    idx = np.asarray(indices).reshape(s_q, 1, -1)
+    rows = None if tokens is None else [(int(j), 0) for j in tokens]
+    tl = None if topk_length is None else np.asarray(topk_length).reshape(s_q, 1)
+    out, lse = sparse_decode(q[:, None], pool, idx, softmax_scale, rows=rows, attn_sink=attn_sink,
+                             topk_length=tl)
+    return out[:, 0], lse[:, :, 0]

@@ -246,3 +246,65 @@ def test_unnamed_pool_rows_never_reach_the_output(h, parts):
     ref_o, ref_l = oracle_sparse(case)
     assert_parity(out[:2], ref_o[:2], lse[:2], ref_l[:2], "unnamed rows are NaN")
     assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
+
+
+# ------------------------------------------------------------ sparse prefill
+
+def run_prefill(q, kv, idx, scale, topk_length=None, attn_sink=None, num_sm_parts=None):
+    """mla_sparse_prefill through the C ABI: q [s_q, h, 576], kv [s_kv, 1, 576],
+    indices [s_q, 1, topk]; returns out [s_q, h, 512], lse [s_q, h], err."""
+    q, kv, idx = q.to(DEV), kv.to(DEV), idx.to(DEV)
+    s_q, h, _ = q.shape
+    topk = idx.shape[-1]
+    buf = binding.DecodeBuffers(s_q, 1, h, DEV, num_sm_parts)
+    tl = None if topk_length is None else topk_length.to(DEV)
+    sink = None if attn_sink is None else attn_sink.to(DEV)
+    binding.mla_get_metadata(tl, s_q, 1, False, topk, buf.num_sm_parts, buf.metadata)
+    out = torch.empty((s_q, h, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((s_q, h), dtype=torch.float32, device=DEV)
+    binding.mla_sparse_prefill(q, kv, idx, scale, buf.metadata, buf.num_sm_parts, buf.workspace, out, lse,
+                               buf.err, attn_sink=sink)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy(), int(buf.err.item())
+
+
+def prefill_inputs(seed, s_q, h, s_kv, topk, invalid):
+    inp = small(seed, b=s_q, s_q=1, h=h, s_kv=s_kv, topk=topk, invalid=invalid)
+    return (inp["q"][:, 0], inp["kv"].reshape(s_kv, 1, 576), inp["indices"].reshape(s_q, 1, topk),
+            inp["softmax_scale"])
+
+
+@pytest.mark.parametrize("h,parts", [(128, None), (64, None), (128, 7)])
+def test_sparse_prefill_parity(h, parts):
+    """Many query tokens with their own index lists (ragged tiles, invalid
+    slots, a per-token topk_length and an attention sink), every token
+    compared with the oracle."""
+    s_q, s_kv, topk = 96, 6000, 400
+    q, kv, idx, scale = prefill_inputs(70 + h, s_q, h, s_kv, topk, 20)
+    g = torch.Generator().manual_seed(71)
+    tl = torch.randint(0, topk + 1, (s_q,), generator=g, dtype=torch.int64).to(torch.int32)
+    tl[:4] = torch.tensor([topk, 1, 0, 129], dtype=torch.int32)
+    sink = torch.randn((h,), generator=g, dtype=torch.float32)
+    out, lse, err = run_prefill(q, kv, idx, scale, tl, sink, parts)
+    ref_o, ref_l = oracle.sparse_prefill(bf16_np(q), bf16_np(kv), idx.numpy(), scale, attn_sink=sink.numpy(),
+                                         topk_length=tl.numpy())
+    # the decode helpers take [b, s_q, h, 512] / [b, h, s_q]
+    assert_parity(out[:, None], ref_o[:, None], lse[:, :, None], ref_l[:, :, None], f"sparse prefill h={h}")
+    assert err == 0
+
+
+def test_sparse_prefill_single_index_rows_are_exact():
+    """Each token names one row (the rest -1): its output is that row's V
+    part bit for bit, so the per-token index gather is exact."""
+    s_q, s_kv, h = 256, 5000, 128
+    g = torch.Generator().manual_seed(72)
+    kv = torch.randn((s_kv, 1, 576), generator=g).to(torch.bfloat16)
+    q = torch.randn((s_q, h, 576), generator=g).to(torch.bfloat16)
+    rows = torch.randperm(s_kv, generator=g)[:s_q].to(torch.int32)
+    idx = torch.full((s_q, 1, 64), -1, dtype=torch.int32)
+    slot = torch.randint(0, 64, (s_q,), generator=g)
+    idx[torch.arange(s_q), 0, slot] = rows
+    out, _, err = run_prefill(q, kv, idx, workloads.SOFTMAX_SCALE)
+    want = kv[rows.long(), 0, :512].float().numpy()
+    assert np.array_equal(out, np.broadcast_to(want[:, None, :], out.shape))
+    assert err == 0

@@ -395,6 +395,48 @@ def test_sparse_invalid_and_out_of_range_are_skipped():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+def test_sparse_prefill_brute_force_and_layout():
+    """Sparse prefill on a tiny case against a brute-force softmax written
+    here: token i's output is the softmax over the rows its list names (each
+    named slot counted once, -1 skipped), out is [s_q, h, 512] and lse
+    [s_q, h]."""
+    pool = rng(60).standard_normal((7, 576))
+    idx = np.array([[0, 3, -1], [6, 6, 2], [5, -1, -1], [-1, -1, -1]])
+    q = rng(61).standard_normal((4, 3, 576))
+    out, lse = oracle.sparse_prefill(q, pool.reshape(7, 1, 576), idx.reshape(4, 1, 3), SCALE)
+    assert out.shape == (4, 3, 512) and lse.shape == (4, 3)
+    for i in range(4):
+        rows = [int(r) for r in idx[i] if r >= 0]
+        for hh in range(3):
+            if not rows:
+                assert np.all(out[i, hh] == 0.0) and np.isneginf(lse[i, hh])
+                continue
+            sc = np.array([SCALE * float(np.dot(q[i, hh], pool[r])) for r in rows])
+            w = np.exp(sc - sc.max())
+            ref_out = sum(w[k] * pool[rows[k], :512] for k in range(len(rows))) / w.sum()
+            ref_lse = sc.max() + math.log(w.sum())
+            assert np.allclose(out[i, hh], ref_out, rtol=1e-12, atol=1e-12)
+            assert abs(lse[i, hh] - ref_lse) < 1e-12
+    # a token naming exactly one row returns that row's V part exactly
+    assert np.array_equal(out[2, 1], pool[5, :512])
+
+
+def test_sparse_prefill_topk_length_and_sink_follow_decode_rules():
+    pool = rng(62).standard_normal((40, 576))
+    idx = rng(63).permutation(40)[:30].reshape(3, 10)
+    q = rng(64).standard_normal((3, 2, 576))
+    tl = np.array([10, 4, 0])
+    sink = np.array([0.5, -1.0])
+    out, lse = oracle.sparse_prefill(q, pool, idx, SCALE, attn_sink=sink, topk_length=tl)
+    for i in range(3):
+        cut = idx[i].copy()
+        cut[tl[i]:] = -1
+        o1, l1 = oracle.sparse_prefill(q[i:i + 1], pool, cut.reshape(1, 10), SCALE)
+        f = oracle.sink_factor(l1[0], sink)
+        assert np.allclose(out[i], o1[0] * f[:, None], rtol=0, atol=1e-12)
+        assert np.allclose(lse[i], l1[0], rtol=0, atol=1e-12, equal_nan=True)
+
+
 def test_dense_equals_sparse_over_all_rows_of_the_request():
     kv = rng(24).standard_normal((10, 64, 576))
     bt = rng(25).permutation(10).reshape(2, 5)
