@@ -94,9 +94,10 @@ constexpr int kGroupPage = 3 * kPage * 128;        // 24 KB
 constexpr int kHalfPage = 4 * kPage * 128;         // 32 KB
 static_assert(2 * kGroupPage == kKGroupBytes && 4 * kHalfPage == kVGroups * kVGroupBytes, "paged regions");
 constexpr uint32_t kRowThreads = 128;              // warps 4..7
-// Softmax: one pass over S per tile after a piece's first (the row max comes
-// with the probabilities; a row whose reference must move redoes the pass).
-constexpr bool kSinglePass = true;
+// Softmax: one pass over S per tile after a piece's first; the row max is
+// taken only when a tile's probabilities sum to more than this (2^kRescaleLog2).
+constexpr float kMoveSum = 256.f;
+static_assert(kMoveSum == 256.f && kRescaleLog2 == 8.f, "kMoveSum = 2^kRescaleLog2");
 constexpr uint32_t kXferNamedThreads = 160;        // dense: warps 3..7
 
 struct Bars {
@@ -504,13 +505,14 @@ __global__ void __maxnreg__(224)
           }
           const int n_valid = keys - t * kTileTokens;  // >= 1; < 128 only on the last tile
           const bool full = kSparse || n_valid >= kTileTokens;
-          // Row max (raw scores; the scale is positive).  The first tile of a
-          // piece reads S once for it (pass 1); later tiles take it from the
-          // probabilities pass, against the current reference, and redo that
-          // pass only in the rare rows whose reference has to move.
-          float u = -INFINITY;
-          if (ok && (t == t0 || !kSinglePass)) {
-            tc_fence_after();
+          // Row max of the raw scores (the scale is positive) over the tile's
+          // keys.  The first tile of a piece takes its reference from it.  A
+          // later tile needs it only when its probabilities against the current
+          // reference sum to more than 2^kRescaleLog2 (necessary for one of
+          // them to exceed that bound), which is rare: then the warp finds the
+          // max and, if the reference has to move, redoes the pass.
+          auto row_max = [&]() {
+            float u = -INFINITY;
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
               float v[32];
@@ -528,31 +530,27 @@ __global__ void __maxnreg__(224)
 #pragma unroll
               for (int j = 0; j < 32; j += 2) u = fmax3(u, v[j], v[j + 1]);
             }
-          }
-          u *= sc;
+            return u * sc;
+          };
           float alpha = 1.f;
-          if (t == t0) {
+          if (ok && t == t0) {
+            tc_fence_after();
+            const float u = row_max();
             m_use = u == -INFINITY ? 0.f : u;
-          } else if (!kSinglePass && u > m_use + kRescaleLog2) {
-            alpha = fast_exp2(m_use - u);
-            m_use = u;
-            lsum *= alpha;
-            bsum *= alpha;
           }
-          // pass 2: p = 2^(s * scale - m) -> bf16 P row r in the staging buffer
-          // (two 64-token chunks, 128-byte swizzle), and the two sums
+          // p = 2^(s * scale - m) -> bf16 P row r in the staging buffer (two
+          // 64-token chunks, 128-byte swizzle), and the two sums
           if constexpr (kSparse) {
             if (r == 0 && tc > 0) bulk_wait_read_all();  // the previous copy has read the staging
             named_barrier_sync(1, kRowThreads);
           } else {
             named_barrier_sync(1, kXferNamedThreads);  // warp 3's previous copy has read the staging
           }
-          if (ok && kSinglePass && t != t0) tc_fence_after();
+          if (ok && t != t0) tc_fence_after();
           float ls = 0.f, bs = 0.f, ls2 = 0.f, bs2 = 0.f;
           for (bool again = ok; again;) {
             again = false;
             const float neg_m = -m_use;
-            float xm = -INFINITY;  // raw row max seen by this pass
             ls = 0.f; bs = 0.f; ls2 = 0.f; bs2 = 0.f;
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
@@ -572,7 +570,6 @@ __global__ void __maxnreg__(224)
               uint32_t pk[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                if constexpr (kSinglePass) xm = fmax3(xm, v[2 * j], v[2 * j + 1]);
                 float x0, x1;
                 asm("{ .reg .b64 a, b, c, d; mov.b64 a, {%2, %3}; mov.b64 b, {%4, %4}; mov.b64 c, {%5, %5};"
                     " fma.rn.f32x2 d, a, b, c; mov.b64 {%0, %1}, d; }"
@@ -591,14 +588,17 @@ __global__ void __maxnreg__(224)
                 st_shared_v4(chunk + ((((i & 1) * 4 + uu) ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1],
                              pk[4 * uu + 2], pk[4 * uu + 3]);
             }
-            xm *= sc;
-            const bool move = kSinglePass && t != t0 && xm > m_use + kRescaleLog2;
-            if (move) {  // move the reference; the warp redoes the pass (TMEM loads are warp-wide)
-              const float a_new = fast_exp2(m_use - xm);
-              alpha *= a_new;
-              m_use = xm;
-              lsum *= a_new;
-              bsum *= a_new;
+            bool move = false;
+            if (__any_sync(0xffffffffu, t != t0 && !(ls + ls2 <= kMoveSum))) {
+              const float u = row_max();
+              if (u > m_use + kRescaleLog2) {  // move the reference; the warp redoes the pass
+                const float a_new = fast_exp2(m_use - u);
+                alpha *= a_new;
+                m_use = u;
+                lsum *= a_new;
+                bsum *= a_new;
+                move = true;
+              }
             }
             again = __any_sync(0xffffffffu, move);
           }
