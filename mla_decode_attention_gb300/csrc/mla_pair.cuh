@@ -178,7 +178,7 @@ __global__ void __maxnreg__(224)
     mbar_init(smem_u32(&bars->q_full), 4);
     mbar_init(smem_u32(&bars->q_free), 1);
     mbar_init(smem_u32(&bars->q_tma), 1);
-    mbar_init(smem_u32(&bars->q_smem_free), 4);
+    mbar_init(smem_u32(&bars->q_smem_free), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars->s_full[b]), 1);
       mbar_init(smem_u32(&bars->s_free[b]), 4);
@@ -252,12 +252,14 @@ __global__ void __maxnreg__(224)
         int32_t issued[kKGroups];  // ring round of this issuer's last load per group slot
         for (int i = 0; i < kKGroups; ++i) issued[i] = -1;
         bool ok = true;
-        bool first = true, q_issued = false;
+        bool first = true, q_issued = false, q_wait = false;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           if (first) {
             // the part's first query rows go through the K ring: requested
-            // here, moved into TMEM by the row threads, then the ring is free
+            // here, copied into TMEM by the QK issuer, then the ring is free
+            // (waited for below, once the first tile's rows are looked up)
             first = false;
+            q_wait = true;
             if (pw == 0 && lane == 0) {
               const uint32_t bar = smem_u32(&bars->q_tma);
               mbar_arrive_expect_tx(bar, kQLatentBytes + kChunk);
@@ -265,8 +267,6 @@ __global__ void __maxnreg__(224)
               tma_load_2d(base + kQRope, &tm_qr, kDv, q * kRows, bar, pol);
               q_issued = true;
             }
-            if (lane == 0) ok = mbar_wait(smem_u32(&bars->q_smem_free), 0, abort_flag, p.err);
-            if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
           }
           int32_t nid[4];  // sparse: the next tile's indices, requested one tile ahead
           const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
@@ -294,6 +294,12 @@ __global__ void __maxnreg__(224)
                 }
                 y[h2] = blk * kPage;
               }
+            }
+            if (q_wait) {
+              q_wait = false;
+              if (lane == 0) ok = mbar_wait(smem_u32(&bars->q_smem_free), 0, abort_flag, p.err);
+              if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
+              if (!ok) continue;
             }
             if constexpr (!kSparse) {
               for (int g = 0; g < kKGroups && ok; ++g) {
@@ -346,6 +352,23 @@ __global__ void __maxnreg__(224)
         uint32_t tc = 0, item = 0;
         bool ok = true;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+          if (item == 0) {
+            // the first piece's latent Q, TMA-staged as [8 chunks][128 rows]
+            // [128 B] (128-byte swizzle), goes into TMEM by tcgen05.cp, one
+            // K = 16 step (8 columns) per copy; its RoPE part is in kQRope
+            if (ok) ok = mbar_wait(smem_u32(&bars->q_tma), 0, abort_flag, p.err);
+            if (ok) {
+              tc_fence_after();
+#pragma unroll 1
+              for (int c = 0; c < kDv / 64; ++c) {
+                const uint64_t qdesc = sw128_desc(base + c * (kRows * 128), 16, 1024);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  tmem_cp_128x256b(tmem + kQCol + 8 * (4 * c + k), qdesc + static_cast<uint64_t>((32 * k) >> 4));
+              }
+              mma_commit(smem_u32(&bars->q_smem_free));  // the K ring may be loaded once the copies have read it
+            }
+          }
           if (ok) ok = mbar_wait(smem_u32(&bars->q_full), item & 1, abort_flag, p.err);
           const uint64_t rope_desc = sw128_desc(base + kQRope, 16, 1024);
           for (int t = t0; t < t1; ++t, ++tc) {
@@ -411,32 +434,15 @@ __global__ void __maxnreg__(224)
         // Q row r of token q: 512 latent columns -> TMEM (bf16 pairs, even k in
         // the low half), 64 RoPE columns -> smem (128-byte swizzled row r)
         if (ok) ok = mbar_wait(smem_u32(&bars->q_free), (item & 1) ^ 1, abort_flag, p.err);
-        if (ok && item == 0) ok = mbar_wait(smem_u32(&bars->q_tma), 0, abort_flag, p.err);
         ok = __all_sync(0xffffffffu, ok);
         if (ok && item == 0) {
-          // row r of the TMA-staged latent part: chunk c at c * 16 KB, row r at
-          // r * 128 B, 16-byte unit u at (u ^ (r mod 8)) * 16 (128-byte swizzle);
-          // the RoPE part already sits in kQRope
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < kDv / 64; ++c) {
-            const uint32_t src = base + c * (kRows * 128) + r * 128;
-            uint32_t w[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint4 x = ld_shared_v4(src + ((u ^ (r & 7)) << 4));
-              w[4 * u] = x.x; w[4 * u + 1] = x.y; w[4 * u + 2] = x.z; w[4 * u + 3] = x.w;
-            }
-            tmem_st32u(t_q + 32 * c, w);
-          }
+          // the first piece's query rows come by TMA and tcgen05.cp (QK issuer)
           if (r == 0) {  // the next piece's query rows (147 KB, contiguous) start towards L2
             PartCursor nc = cur;
             int nq, nt0, nt1, nsplit;
             if (next_piece(meta, p.num_parts, &nc, &nq, &nt0, &nt1, &nsplit))
               prefetch_l2(p.q + static_cast<int64_t>(nq) * kRows * kDqk, kRows * kDqk * 2);
           }
-          tmem_wait_st();
-          tc_fence_before();
         } else if (ok) {
           tc_fence_after();
           const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(q) * kRows + r) * kDqk);
@@ -477,10 +483,7 @@ __global__ void __maxnreg__(224)
           tc_fence_before();
         }
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&bars->q_full));
-          if (item == 0) mbar_arrive(smem_u32(&bars->q_smem_free));  // the K ring may be loaded
-        }
+        if (lane == 0) mbar_arrive(smem_u32(&bars->q_full));
         float m_use = 0.f, lsum = 0.f, bsum = 0.f;
         for (int t = t0; t < t1; ++t, ++tc) {
           const uint32_t sb = tc & 1;

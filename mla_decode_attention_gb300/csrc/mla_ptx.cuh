@@ -234,6 +234,14 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// Copies a [128 rows x 32 bytes] shared-memory matrix, described like an MMA
+// operand by `sdesc`, into TMEM lanes 0..127 at column taddr.. + 7 (row i's 16
+// bf16 values in order, two per 32-bit column).  Asynchronous: completion is
+// tracked by tcgen05.commit, and MMAs this thread issues afterwards see the data.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrives once on `bar` in every CTA of `cta_mask` (same shared-memory offset)
 // when every tcgen05 operation issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
