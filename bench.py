@@ -409,7 +409,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kernel_name, "kernel_ms": round(split_ms, 5),
-                     "peak_source": f"{peaks.get('source')} (MEASURED_PEAKS.json burst copy)"},
+                     "peak_source": f"{peaks.get('source')} (MEASURED_PEAKS.json "
+                                    f"{'burst copy' if bound == 'hbm' else 'bf16 GEMM burst'})"},
         "e2e": {"value": round(job_rate(flops, e2e_ms, world) / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
