@@ -169,7 +169,7 @@ int launch_pair(const CUtensorMap& tm_kv, const CUtensorMap& tm_qa, const CUtens
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.num_parts * 2, 1, 1);
-  cfg.blockDim = dim3(pair::kThreads, 1, 1);
+  cfg.blockDim = dim3(kSparse ? pair::kThreadsSparse : pair::kThreads, 1, 1);
   cfg.dynamicSmemBytes = pair::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

@@ -33,14 +33,15 @@
 // Sparse keys are gathered four rows at a time into [128 tokens x 64 columns]
 // chunks instead.
 //
-// Roles (256 threads, both CTAs; two warps per SM sub-partition, so each
-// thread may hold 224 registers):
-//   warps 0, 2 lane 0    : TMA issuers (chunk c of a tile by issuer c mod 2 in
-//                          the score CTA; chunk n of the V stream by n mod 2)
+// Roles (paged cache: 256 threads per CTA, two warps per SM sub-partition, up
+// to 224 registers each; gathered keys: 512 threads, 128 registers):
+//   warp 0 lane 0        : paged: TMA issuer (K groups / V halves, one box per page)
+//   warps 0, 2, 3, 8..13 : gathered: tile::gather4 issuers, one chunk of a tile
+//                          each (score CTA: 9 chunks, output CTA: 8)
 //   warp 1               : TMEM owner; lane 0 issues every MMA
-//   warp 3               : score CTA: issues the P bulk copies (named barriers 1, 2
-//                          with warps 4..7 around the staging buffer);
-//                          output CTA: hands consumed P buffers back
+//   warp 3               : paged score CTA: issues the P bulk copies (named
+//                          barriers 1, 2 with warps 4..7 around the staging
+//                          buffer); paged output CTA: hands P buffers back
 //   warps 4..7           : row threads, thread r = query row r = TMEM lane r
 //
 // Waits are bounded (mbar_wait*); after an abort every role keeps walking its
@@ -62,7 +63,14 @@
 namespace mla {
 namespace pair {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;                      // paged cache
+// Gathered keys: one tile::gather4 costs its issuing warp ~84 clk (a warp's
+// gathers go out one at a time), so the sparse kernel runs 16 warps (128
+// registers each) and spreads the gathers of a tile over 9 warps in the score
+// CTA (one chunk each) and 8 in the output CTA.
+constexpr int kThreadsSparse = 512;
+constexpr int kKIssuersSparse = 9;
+constexpr int kVIssuersSparse = 8;
 constexpr int kRows = 128;                         // query rows per cluster = TMEM lanes
 constexpr int kChunk = kTileTokens * 64 * 2;       // 16 KB: [128 tokens x 64 columns] bf16
 // score CTA
@@ -141,6 +149,10 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// Gather issuer index of a warp: warps 0, 2, 3, then 8, 9, ... (1 issues the
+// MMAs, 4..7 are the row warps).
+__device__ __forceinline__ int issuer_index(int warp) { return warp == 0 ? 0 : (warp < 4 ? warp - 1 : warp - 5); }
+
 // One CTA per SM (shared memory); up to 224 registers per thread (8 warps, two
 // per sub-partition), so each row thread's 128 scores stay in registers.
 // kSparse: keys are pool rows named by p.indices (DSA top-k, -1 = none), read
@@ -152,7 +164,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // latent part of one token's 128 rows), tm_qr as [rows][576] with [128 x 64]
 // boxes (its RoPE part).
 template <bool kSparse>
-__global__ void __maxnreg__(224)
+__global__ void __maxnreg__(kSparse ? 128 : 224)
     mla_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qa,
                     const __grid_constant__ CUtensorMap tm_qb, const __grid_constant__ CUtensorMap tm_ql,
                     const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ SplitParams p) {
@@ -233,18 +245,15 @@ __global__ void __maxnreg__(224)
     // nothing to do: every role is skipped, the teardown below still runs
   } else if (rank == 0) {
     // ================================================================ score CTA
-    if (warp == 0 || warp == 2 || (kSparse && warp == 3)) {
+    if (warp == 0 || warp == 2 || (kSparse && (warp == 3 || warp >= 8))) {
       // ---------------------------------------------------- K tile producers
       // Paged: lane 0 of warp 0 loads each group as one box per page.
-      // Sparse: warps 0, 2, 3 share the chunks (one gather4 costs its warp
-      // ~80 clk to issue, so gathers need more issuing warps); lane L gathers
-      // rows 4L..4L+3 of the tile for each chunk (invalid slots fetch pool
-      // row 0; the softmax gives them zero weight); lane 0 owns the barriers.
-      // Each group of 3 chunks has a chunk of every issuer, so each issuer
-      // waits on every slot in order.
-      if ((lane == 0 || kSparse) && (kSparse || warp == 0)) {
-        constexpr int kIssuers = kSparse ? 3 : 2;
-        const int pw = warp == 0 ? 0 : warp - 1;
+      // Sparse: nine warps gather one chunk each; lane L gathers rows
+      // 4L..4L+3 of the tile (invalid slots fetch pool row 0; the softmax
+      // gives them zero weight); lane 0 owns the barriers.
+      if (kSparse ? issuer_index(warp) < kKIssuersSparse : (warp == 0 && lane == 0)) {
+        constexpr int kIssuers = kSparse ? kKIssuersSparse : 2;
+        const int pw = issuer_index(warp);
         const uint64_t pol = l2_policy_evict_first();
         PartCursor cur = part_cursor(meta, part);
         int q, t0, t1, split;
@@ -678,15 +687,15 @@ __global__ void __maxnreg__(224)
     }
   } else {
     // ================================================================ output CTA
-    if (warp == 0 || warp == 2 || (kSparse && warp == 3)) {
+    if (warp == 0 || warp == 2 || (kSparse && (warp == 3 || warp >= 8))) {
       // ---------------------------------------------------- V tile producers
       // Paged: lane 0 of warp 0 loads each V half (chunks 0..3, 4..7) as one
-      // box per page.  Sparse: warps 0, 2, 3 gather (chunk c by issuer c mod
-      // 3); each issuer loads into the same d quarters every tile, so it waits
-      // on those slots in order.
-      if ((lane == 0 || kSparse) && (kSparse || warp == 0)) {
-        constexpr int kIssuers = kSparse ? 3 : 2;
-        const int pw = warp == 0 ? 0 : warp - 1;
+      // box per page.  Sparse: eight warps gather one chunk each; each issuer
+      // loads into the same d quarter every tile, so it waits on that slot in
+      // order.
+      if (kSparse ? issuer_index(warp) < kVIssuersSparse : (warp == 0 && lane == 0)) {
+        constexpr int kIssuers = kSparse ? kVIssuersSparse : 2;
+        const int pw = issuer_index(warp);
         const uint64_t pol = l2_policy_evict_first();
         PartCursor cur = part_cursor(meta, part);
         int q, t0, t1, split;
