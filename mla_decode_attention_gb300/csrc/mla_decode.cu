@@ -131,14 +131,14 @@ int launch_split(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const SplitP
 }
 
 // The query rows [n_seq * 128, 576] seen as [9 chunks][rows][64 columns]
-// (chunk stride 128 bytes); boxes of [8 chunks x 128 rows x 64 columns] (the
-// latent part of one token's rows, 128 KB) with 128-byte swizzle.
+// (chunk stride 128 bytes); boxes of [2 chunks x 128 rows x 64 columns] (a
+// quarter of the latent part of one token's rows, 32 KB) with 128-byte swizzle.
 bool make_q_latent_map(CUtensorMap* m, const void* q, uint64_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {64u, rows, static_cast<cuuint64_t>(kDqk / 64)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDqk) * 2u, 128u};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(pair::kRows), static_cast<cuuint32_t>(kDv / 64)};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(pair::kRows), 2u};  // two chunks per box
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

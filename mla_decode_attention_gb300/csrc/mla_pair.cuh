@@ -111,8 +111,9 @@ constexpr uint32_t kXferNamedThreads = 160;        // dense: warps 3..7
 struct Bars {
   uint64_t kfull[kKGroups], kempty[kKGroups];      // score CTA K ring
   uint64_t vfull[kVGroups], vempty[kVGroups];      // output CTA V ring
-  uint64_t q_full, q_free, s_full[2], s_free[2];   // score CTA
-  uint64_t q_tma, q_smem_free;                     // score CTA: the first piece's Q through the K ring
+  uint64_t s_full[2], s_free[2];                   // score CTA
+  uint64_t q_tma, q_smem_free;                     // score CTA: a piece's Q by TMA (the first through the K ring)
+  uint64_t q_stage_free, q_cp;                     // score CTA: later pieces' Q through the P staging buffer
   uint64_t p_free[2];                              // score CTA, arrived by the output CTA
   uint64_t p_full[2];                              // output CTA, completed by bulk copies
   uint64_t pv_done[2], o_full, o_free, o_drained, o_rescaled;  // output CTA
@@ -124,6 +125,8 @@ constexpr int kSmemBytes = kEpi + 4 * 4096 + 1024;
 // The part's first query rows arrive by TMA: the latent columns as [8 chunks]
 // [128 rows][128 B] in the (still empty) K ring, the RoPE columns in kQRope.
 constexpr int kQLatentBytes = 8 * kRows * 128;     // 128 KB
+constexpr int kQBoxBytes = 2 * kRows * 128;        // 32 KB: one query box, two chunks
+static_assert(kQBoxBytes <= kXferBytes, "a query box fits the P staging buffer");
 static_assert(kQLatentBytes <= kQRope, "Q staging in the K ring");
 static_assert(kBarOffset % 16 == 0, "barrier block alignment");
 static_assert(sizeof(Bars) <= 1024, "barrier block size");
@@ -160,9 +163,9 @@ __device__ __forceinline__ int issuer_index(int warp) { return warp == 0 ? 0 : (
 // block table.  Paged: tm_qa, tm_qb view the cache as [8-token groups][9
 // chunks][8 rows][64 columns] and load one page's [8][4][8][64] (V half) and
 // [8][3][8][64] (K group) boxes; tm_kv is then unused.  tm_ql views the
-// query rows as [9 chunks][rows][64 columns] with [8 x 128 x 64] boxes (the
-// latent part of one token's 128 rows), tm_qr as [rows][576] with [128 x 64]
-// boxes (its RoPE part).
+// query rows as [9 chunks][rows][64 columns] with [2 x 128 x 64] boxes (a
+// quarter of the latent part of one token's 128 rows), tm_qr as [rows][576]
+// with [128 x 64] boxes (its RoPE part).
 template <bool kSparse>
 __global__ void __maxnreg__(kSparse ? 128 : 224)
     mla_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qa,
@@ -187,9 +190,9 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
       mbar_init(smem_u32(&bars->vfull[i]), kSparse ? 2 : 1);
       mbar_init(smem_u32(&bars->vempty[i]), 1);
     }
-    mbar_init(smem_u32(&bars->q_full), 4);
-    mbar_init(smem_u32(&bars->q_free), 1);
     mbar_init(smem_u32(&bars->q_tma), 1);
+    mbar_init(smem_u32(&bars->q_stage_free), 1);
+    mbar_init(smem_u32(&bars->q_cp), 1);
     mbar_init(smem_u32(&bars->q_smem_free), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars->s_full[b]), 1);
@@ -272,7 +275,8 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
             if (pw == 0 && lane == 0) {
               const uint32_t bar = smem_u32(&bars->q_tma);
               mbar_arrive_expect_tx(bar, kQLatentBytes + kChunk);
-              tma_load_3d(base, &tm_ql, 0, q * kRows, 0, bar, pol);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) tma_load_3d(base + i * kQBoxBytes, &tm_ql, 0, q * kRows, 2 * i, bar, pol);
               tma_load_2d(base + kQRope, &tm_qr, kDv, q * kRows, bar, pol);
               q_issued = true;
             }
@@ -358,9 +362,39 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
       if (lane == 0) {
         PartCursor cur = part_cursor(meta, part);
         int q, t0, t1, split;
-        uint32_t tc = 0, item = 0;
+        uint32_t tc = 0, item = 0, qtma_n = 1, qcp_n = 0;  // completed phases of q_tma, q_cp
         bool ok = true;
+        const uint64_t qpol = l2_policy_evict_first();
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
+          if (item > 0) {
+            // a later piece's query rows: the RoPE part into kQRope and the
+            // latent part two chunks at a time through the P staging buffer
+            // (free once the previous piece's last P copy has read it, which
+            // also means its QK products have completed), each pair moved into
+            // TMEM by tcgen05.cp before the next one lands
+            if (ok) ok = mbar_wait(smem_u32(&bars->q_stage_free), (item - 1) & 1, abort_flag, p.err);
+            if (ok) tc_fence_after();
+            for (int i = 0; i < 4 && ok; ++i) {
+              const uint32_t bar = smem_u32(&bars->q_tma);
+              mbar_arrive_expect_tx(bar, kQBoxBytes + (i == 0 ? kChunk : 0));
+              if (i == 0) tma_load_2d(base + kQRope, &tm_qr, kDv, q * kRows, bar, qpol);
+              tma_load_3d(base + kStage, &tm_ql, 0, q * kRows, 2 * i, bar, qpol);
+              ok = mbar_wait(bar, qtma_n & 1, abort_flag, p.err);
+              ++qtma_n;
+              if (!ok) break;
+              tc_fence_after();
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const uint64_t qdesc = sw128_desc(base + kStage + c * (kRows * 128), 16, 1024);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  tmem_cp_128x256b(tmem + kQCol + 8 * (4 * (2 * i + c) + k), qdesc + static_cast<uint64_t>((32 * k) >> 4));
+              }
+              mma_commit(smem_u32(&bars->q_cp));
+              ok = mbar_wait(smem_u32(&bars->q_cp), qcp_n & 1, abort_flag, p.err);  // the buffer takes the next pair
+              ++qcp_n;
+            }
+          }
           if (item == 0) {
             // the first piece's latent Q, TMA-staged as [8 chunks][128 rows]
             // [128 B] (128-byte swizzle), goes into TMEM by tcgen05.cp, one
@@ -378,7 +412,6 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
               mma_commit(smem_u32(&bars->q_smem_free));  // the K ring may be loaded once the copies have read it
             }
           }
-          if (ok) ok = mbar_wait(smem_u32(&bars->q_full), item & 1, abort_flag, p.err);
           const uint64_t rope_desc = sw128_desc(base + kQRope, 16, 1024);
           for (int t = t0; t < t1; ++t, ++tc) {
             if (!ok) continue;
@@ -411,7 +444,6 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
             }
             if (!ok) continue;
             mma_commit(smem_u32(&bars->s_full[sb]));
-            if (t == t1 - 1) mma_commit(smem_u32(&bars->q_free));
           }
           ++item;
         }
@@ -428,10 +460,8 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
       // are the weights the PV product multiplies (to normalise O).
       const int r = threadIdx.x - 128;
       const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
-      const uint32_t t_q = tmem + lane_off + kQCol;
       const uint32_t stage = base + kStage;
       const uint32_t prow = stage + (r >> 3) * 1024 + (r & 7) * 128;
-      const uint32_t qrope_row = base + kQRope + (r >> 3) * 1024 + (r & 7) * 128;
       const float sc = p.scale_log2;
       PartCursor cur = part_cursor(meta, part);
       int q, t0, t1, split;
@@ -440,59 +470,14 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
       while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
         const int32_t* srec = meta_seq(meta, p.num_parts, q);
         const int32_t keys = srec[kSKeys];
-        // Q row r of token q: 512 latent columns -> TMEM (bf16 pairs, even k in
-        // the low half), 64 RoPE columns -> smem (128-byte swizzled row r)
-        if (ok) ok = mbar_wait(smem_u32(&bars->q_free), (item & 1) ^ 1, abort_flag, p.err);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok && item == 0) {
-          // the first piece's query rows come by TMA and tcgen05.cp (QK issuer)
-          if (r == 0) {  // the next piece's query rows (147 KB, contiguous) start towards L2
-            PartCursor nc = cur;
-            int nq, nt0, nt1, nsplit;
-            if (next_piece(meta, p.num_parts, &nc, &nq, &nt0, &nt1, &nsplit))
-              prefetch_l2(p.q + static_cast<int64_t>(nq) * kRows * kDqk, kRows * kDqk * 2);
-          }
-        } else if (ok) {
-          tc_fence_after();
-          const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(q) * kRows + r) * kDqk);
-          // 72 16-byte units = nine blocks of 8 (blocks 0..7 latent, block 8 RoPE),
-          // read three blocks per round so that 24 loads are in flight at once
-#pragma unroll
-          for (int rnd = 0; rnd < 3; ++rnd) {
-            uint4 v[24];
-#pragma unroll
-            for (int i = 0; i < 24; ++i) v[i] = ldg_nc_v4(qrow + 24 * rnd + i);
-#pragma unroll
-            for (int bb = 0; bb < 3; ++bb) {
-              const int blk = 3 * rnd + bb;
-              if (blk < kDv / 64) {
-                uint32_t w[32];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  w[4 * i] = v[8 * bb + i].x; w[4 * i + 1] = v[8 * bb + i].y;
-                  w[4 * i + 2] = v[8 * bb + i].z; w[4 * i + 3] = v[8 * bb + i].w;
-                }
-                tmem_st32u(t_q + 32 * blk, w);
-              } else {
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                  st_shared_v4(qrope_row + ((u ^ (r & 7)) << 4), v[8 * bb + u].x, v[8 * bb + u].y,
-                               v[8 * bb + u].z, v[8 * bb + u].w);
-              }
-            }
-          }
-          if (r == 0) {  // the next piece's query rows (147 KB, contiguous) start towards L2
-            PartCursor nc = cur;
-            int nq, nt0, nt1, nsplit;
-            if (next_piece(meta, p.num_parts, &nc, &nq, &nt0, &nt1, &nsplit))
-              prefetch_l2(p.q + static_cast<int64_t>(nq) * kRows * kDqk, kRows * kDqk * 2);
-          }
-          tmem_wait_st();
-          fence_proxy_async_smem();
-          tc_fence_before();
+        // the piece's query rows come by TMA and tcgen05.cp (QK issuer); the
+        // next piece's rows (147 KB, contiguous) start towards L2
+        if (r == 0) {
+          PartCursor nc = cur;
+          int nq, nt0, nt1, nsplit;
+          if (next_piece(meta, p.num_parts, &nc, &nq, &nt0, &nt1, &nsplit))
+            prefetch_l2(p.q + static_cast<int64_t>(nq) * kRows * kDqk, kRows * kDqk * 2);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->q_full));
         float m_use = 0.f, lsum = 0.f, bsum = 0.f;
         for (int t = t0; t < t1; ++t, ++tc) {
           const uint32_t sb = tc & 1;
@@ -644,6 +629,10 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
               bulk_commit_group();
             }
           }
+          if (kSparse && r == 0 && t == t1 - 1) {  // the staging buffer may take the next piece's query rows
+            bulk_wait_read_all();
+            mbar_arrive(smem_u32(&bars->q_stage_free));
+          }
         }
         // LSE of row r for this piece
         const float lse_v = (lsum > 0.f && bsum > 0.f) ? (m_use + __log2f(lsum)) * 0.69314718055994531f
@@ -679,6 +668,10 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
                                 mapa_shared(smem_u32(&bars->p_full[b]), 1));
               bulk_commit_group();
             }
+          }
+          if (lane == 0 && t == t1 - 1) {  // the staging buffer may take the next piece's query rows
+            bulk_wait_read_all();
+            mbar_arrive(smem_u32(&bars->q_stage_free));
           }
           __syncwarp();
         }
