@@ -112,7 +112,8 @@ struct Bars {
   uint64_t kfull[kKGroups], kempty[kKGroups];      // score CTA K ring
   uint64_t vfull[kVGroups], vempty[kVGroups];      // output CTA V ring
   uint64_t s_full[2], s_free[2];                   // score CTA
-  uint64_t q_tma, q_smem_free;                     // score CTA: a piece's Q by TMA (the first through the K ring)
+  uint64_t q_tma;                                  // score CTA: a later piece's Q by TMA
+  uint64_t q_box[4];                               // score CTA: the first piece's Q boxes in the K ring
   uint64_t q_stage_free, q_cp;                     // score CTA: later pieces' Q through the P staging buffer
   uint64_t p_free[2];                              // score CTA, arrived by the output CTA
   uint64_t p_full[2];                              // output CTA, completed by bulk copies
@@ -183,6 +184,8 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKGroups; ++i) {
       mbar_init(smem_u32(&bars->kfull[i]), kSparse ? 3 : 1);  // sparse: three chunks per group
+      // phase 0 completes when the first query rows staged in the slot are in
+      // TMEM, phase t + 1 when tile t's products have read the slot's K group
       mbar_init(smem_u32(&bars->kempty[i]), 1);
     }
     for (int i = 0; i < kVGroups; ++i) {
@@ -193,7 +196,7 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
     mbar_init(smem_u32(&bars->q_tma), 1);
     mbar_init(smem_u32(&bars->q_stage_free), 1);
     mbar_init(smem_u32(&bars->q_cp), 1);
-    mbar_init(smem_u32(&bars->q_smem_free), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars->q_box[i]), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars->s_full[b]), 1);
       mbar_init(smem_u32(&bars->s_free[b]), 4);
@@ -264,20 +267,22 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
         int32_t issued[kKGroups];  // ring round of this issuer's last load per group slot
         for (int i = 0; i < kKGroups; ++i) issued[i] = -1;
         bool ok = true;
-        bool first = true, q_issued = false, q_wait = false;
+        bool first = true, q_issued = false;
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           if (first) {
-            // the part's first query rows go through the K ring: requested
-            // here, copied into TMEM by the QK issuer, then the ring is free
-            // (waited for below, once the first tile's rows are looked up)
+            // the part's first query rows go through the K ring as four boxes,
+            // each with its own barrier; the QK issuer moves each into TMEM as
+            // it lands and releases a ring slot once the boxes in it are
+            // moved, so K group g is requested while later boxes still arrive
             first = false;
-            q_wait = true;
             if (pw == 0 && lane == 0) {
-              const uint32_t bar = smem_u32(&bars->q_tma);
-              mbar_arrive_expect_tx(bar, kQLatentBytes + kChunk);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) tma_load_3d(base + i * kQBoxBytes, &tm_ql, 0, q * kRows, 2 * i, bar, pol);
-              tma_load_2d(base + kQRope, &tm_qr, kDv, q * kRows, bar, pol);
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t bar = smem_u32(&bars->q_box[i]);
+                mbar_arrive_expect_tx(bar, kQBoxBytes + (i == 0 ? kChunk : 0));
+                if (i == 0) tma_load_2d(base + kQRope, &tm_qr, kDv, q * kRows, bar, pol);
+                tma_load_3d(base + i * kQBoxBytes, &tm_ql, 0, q * kRows, 2 * i, bar, pol);
+              }
               q_issued = true;
             }
           }
@@ -308,15 +313,9 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
                 y[h2] = blk * kPage;
               }
             }
-            if (q_wait) {
-              q_wait = false;
-              if (lane == 0) ok = mbar_wait(smem_u32(&bars->q_smem_free), 0, abort_flag, p.err);
-              if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
-              if (!ok) continue;
-            }
             if constexpr (!kSparse) {
               for (int g = 0; g < kKGroups && ok; ++g) {
-                ok = mbar_wait(smem_u32(&bars->kempty[g]), (tc & 1) ^ 1, abort_flag, p.err);
+                ok = mbar_wait(smem_u32(&bars->kempty[g]), tc & 1, abort_flag, p.err);
                 if (!ok) break;
                 const uint32_t bar = smem_u32(&bars->kfull[g]);
                 mbar_arrive_expect_tx(bar, kKGroupBytes);
@@ -330,7 +329,7 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
               const int g = c / 3;
               const uint32_t slot = g, round = tc;  // one ring round per tile
               if (lane == 0) {
-                ok = mbar_wait(smem_u32(&bars->kempty[slot]), (round & 1) ^ 1, abort_flag, p.err);
+                ok = mbar_wait(smem_u32(&bars->kempty[slot]), round & 1, abort_flag, p.err);
                 if (ok) mbar_arrive_expect_tx(smem_u32(&bars->kfull[slot]), kChunk);
               }
               if constexpr (kSparse) ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -343,9 +342,9 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
           }
         }
         if (!ok && lane == 0) {  // let this issuer's copies in flight land before the CTA exits
-          if (q_issued) {
+          for (int i = 0; q_issued && i < 4; ++i) {
             const uint64_t t_start = globaltimer_ns();
-            while (!mbar_try_wait(smem_u32(&bars->q_tma), 0) && globaltimer_ns() - t_start < 1000000ull) {
+            while (!mbar_try_wait(smem_u32(&bars->q_box[i]), 0) && globaltimer_ns() - t_start < 1000000ull) {
             }
           }
           for (int s = 0; s < kKGroups; ++s) {
@@ -362,8 +361,8 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
       if (lane == 0) {
         PartCursor cur = part_cursor(meta, part);
         int q, t0, t1, split;
-        uint32_t tc = 0, item = 0, qtma_n = 1, qcp_n = 0;  // completed phases of q_tma, q_cp
-        bool ok = true;
+        uint32_t tc = 0, item = 0, qtma_n = 0, qcp_n = 0;  // completed phases of q_tma, q_cp
+        bool ok = true, q_pending = false;  // q_pending: a query box is in flight
         const uint64_t qpol = l2_policy_evict_first();
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           if (item > 0) {
@@ -379,9 +378,11 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
               mbar_arrive_expect_tx(bar, kQBoxBytes + (i == 0 ? kChunk : 0));
               if (i == 0) tma_load_2d(base + kQRope, &tm_qr, kDv, q * kRows, bar, qpol);
               tma_load_3d(base + kStage, &tm_ql, 0, q * kRows, 2 * i, bar, qpol);
+              q_pending = true;
               ok = mbar_wait(bar, qtma_n & 1, abort_flag, p.err);
-              ++qtma_n;
               if (!ok) break;
+              q_pending = false;
+              ++qtma_n;
               tc_fence_after();
 #pragma unroll
               for (int c = 0; c < 2; ++c) {
@@ -396,20 +397,27 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
             }
           }
           if (item == 0) {
-            // the first piece's latent Q, TMA-staged as [8 chunks][128 rows]
-            // [128 B] (128-byte swizzle), goes into TMEM by tcgen05.cp, one
-            // K = 16 step (8 columns) per copy; its RoPE part is in kQRope
-            if (ok) ok = mbar_wait(smem_u32(&bars->q_tma), 0, abort_flag, p.err);
-            if (ok) {
-              tc_fence_after();
+            // the first piece's latent Q, TMA-staged in the K ring as [8
+            // chunks][128 rows][128 B] (128-byte swizzle, four two-chunk
+            // boxes), goes into TMEM by tcgen05.cp, one K = 16 step (8
+            // columns) per copy, box by box as they land; ring slot g (48 KB
+            // at 48 g KB) is released once the boxes overlapping it are moved:
+            // slot 0 after boxes 0, 1, slot 1 after box 2, slot 2 after box 3.
+            // Its RoPE part is in kQRope (with box 0).
+            static_assert(kKGroups == 3 && kKGroupBytes == 3 * kQBoxBytes / 2, "query boxes over the K ring slots");
 #pragma unroll 1
-              for (int c = 0; c < kDv / 64; ++c) {
+            for (int i = 0; i < 4 && ok; ++i) {
+              ok = mbar_wait(smem_u32(&bars->q_box[i]), 0, abort_flag, p.err);
+              if (!ok) break;
+              tc_fence_after();
+#pragma unroll
+              for (int c = 2 * i; c < 2 * i + 2; ++c) {
                 const uint64_t qdesc = sw128_desc(base + c * (kRows * 128), 16, 1024);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                   tmem_cp_128x256b(tmem + kQCol + 8 * (4 * c + k), qdesc + static_cast<uint64_t>((32 * k) >> 4));
               }
-              mma_commit(smem_u32(&bars->q_smem_free));  // the K ring may be loaded once the copies have read it
+              if (i >= 1) mma_commit(smem_u32(&bars->kempty[i - 1]));  // the copies have read the slot
             }
           }
           const uint64_t rope_desc = sw128_desc(base + kQRope, 16, 1024);
@@ -446,6 +454,11 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
             mma_commit(smem_u32(&bars->s_full[sb]));
           }
           ++item;
+        }
+        if (q_pending) {  // a query box still in flight: let it land before the CTA exits
+          const uint64_t t_start = globaltimer_ns();
+          while (!mbar_try_wait(smem_u32(&bars->q_tma), qtma_n & 1) && globaltimer_ns() - t_start < 1000000ull) {
+          }
         }
       }
     } else if (warp >= 4 && warp < 8) {
