@@ -167,7 +167,8 @@ int mla_get_metadata_host(const int32_t* cache_seqlens_host, int batch, int s_q,
  * [batch*s_q + num_sm_parts, h_q, 512], fp32 partial LSEs
  * [batch*s_q + num_sm_parts, h_q], then 64 bytes of control words (the
  * split kernel records there which of the metadata's two schedules it
- * walked; mla_combine reads it).  One workspace serves one call at a time.
+ * walked and whether that schedule left rows to merge or fill; mla_combine
+ * reads them).  One workspace serves one call at a time.
  */
 int mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts, size_t* bytes);
 

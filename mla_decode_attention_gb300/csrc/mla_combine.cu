@@ -28,16 +28,17 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(
   const int head = blockIdx.y * kCombineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   pdl_wait_primary();
+  // The split kernel recorded in the workspace which schedule it walked (-1
+  // when it rejected the metadata) and whether that schedule left anything to
+  // merge or fill; with nothing to do, no other word is read.
+  const int32_t walked = ws_ctrl[0];
+  if ((walked != 0 && walked != 1) || ws_ctrl[1] == 0) return;
   // Metadata for another shape: the split kernel computed nothing (and set
   // MLA_DEVERR_METADATA); write nothing either.  The topk and causal words
   // do not change the layout, so any matching batch / s_q / parts passes.
   if (meta[kHMagic] != kMetaMagic || meta[kHVersion] != kMetaVersion || meta[kHNSeq] != batch * s_q ||
       meta[kHParts] != num_parts || meta[kHSq] != s_q || meta[kHBatch] != batch)
     return;
-  // The split kernel recorded in the workspace which schedule it walked, or
-  // -1 when it rejected the metadata (then there is nothing to merge).
-  const int32_t walked = ws_ctrl[0];
-  if (walked != 0 && walked != 1) return;
   const bool use_b = walked == 1 && schedule_b(meta)[kHMagic] == kMetaMagic;
   const int32_t* sched = use_b ? schedule_b(meta) : meta;
   const int32_t* s = meta_seq(sched, num_parts, q);

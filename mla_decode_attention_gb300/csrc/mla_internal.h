@@ -42,7 +42,9 @@ int launch_combine(const void* metadata, int batch, int s_q, int h_q, int num_sm
 // fp32, then kWorkspaceCtrlBytes of control words.  Control word 0 holds the
 // schedule the last split kernel on this workspace walked (0 = A, 1 = B, -1 =
 // metadata rejected); the combine reads it, so the metadata itself is never
-// written by a decode call.
+// written by a decode call.  Control word 1 is 0 when that schedule left the
+// combine nothing to do (schedule B with every sequence non-empty: each one
+// written by the split kernel), else 1.
 constexpr int64_t kWorkspaceCtrlBytes = 64;
 inline int64_t workspace_rows(int batch, int s_q, int num_sm_parts) {
   return static_cast<int64_t>(batch) * s_q + num_sm_parts;

@@ -14,6 +14,10 @@ namespace mla {
 namespace {
 
 constexpr int kSmemPrefixes = 8192;  // sequences whose cost prefixes the schedule keeps in smem
+// Up to this many sequences the schedule builds the sequence records in shared
+// memory and writes them out once at the end (no global read-after-write
+// round trips between the phases).
+constexpr int kSmemRecords = 256;
 // one CTA of 128 threads up to this many sequences (fewer warps to meet at
 // each barrier), else 1024
 constexpr int kSmallMetaSeqs = 2048;
@@ -57,6 +61,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
                                                                 int num_parts, int32_t* meta) {
   __shared__ int64_t warp_sums[32];
   __shared__ int32_t s_prefix[kSmemPrefixes];
+  __shared__ int32_t s_rec[kSmemRecords * kSeqWords];
   // a decode kernel launched next may start its prologue; it waits for this
   // grid to complete before it reads the schedule
   pdl_launch_dependents();
@@ -72,6 +77,10 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   __shared__ int64_t s_group_start[kMaxSq + 1];
   if (threadIdx.x == 0) s_max_cost = 0;
   __syncthreads();
+  // the sequence records of schedule A: built in shared memory when they fit
+  const bool rec_smem = n_seq <= kSmemRecords;
+  int32_t* const recs = rec_smem ? s_rec : meta_seq(meta, num_parts, 0);
+  auto rec = [&](int q) { return recs + kSeqWords * q; };
 
   // 1. tiles, keys and cost per sequence; chunk-local cost prefix.
   int64_t local = 0;
@@ -80,7 +89,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
     const int q = order_to_q(k, n_g, groups);
     const int32_t keys = seq_keys(seqlens, q / s_q, q % s_q, s_q, causal, topk);
     const int32_t nt = tiles_of(keys);
-    int32_t* s = meta_seq(meta, num_parts, q);
+    int32_t* s = rec(q);
     s[kSTiles] = nt; s[kSKeys] = keys; s[5] = 0; s[6] = 0; s[7] = 0;
     s[kSCostPrefix] = static_cast<int32_t>(local);
     local += cost_of(nt);
@@ -97,13 +106,13 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   // where each group starts on the group-major cost line
   for (int k = k0; k < k1; ++k)
     if (k % n_g == 0)
-      s_group_start[k / n_g] = base + meta_seq(meta, num_parts, order_to_q(k, n_g, groups))[kSCostPrefix];
+      s_group_start[k / n_g] = base + rec(order_to_q(k, n_g, groups))[kSCostPrefix];
   if (threadIdx.x == 0) s_group_start[groups] = total;
   __syncthreads();
   // prefixes within each group's own cost line
   for (int k = k0; k < k1; ++k) {
     const int q = order_to_q(k, n_g, groups);
-    int32_t* sq = meta_seq(meta, num_parts, q);
+    int32_t* sq = rec(q);
     sq[kSCostPrefix] = static_cast<int32_t>(base + sq[kSCostPrefix] - s_group_start[k / n_g]);
     if (n_seq <= kSmemPrefixes) s_prefix[q] = sq[kSCostPrefix];
   }
@@ -117,7 +126,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   // 2. split counts per sequence (from the prefixes only).
   int64_t nsplit_local = 0;
   for (int k = k0; k < k1; ++k) {
-    int32_t* s = meta_seq(meta, num_parts, order_to_q(k, n_g, groups));
+    int32_t* s = rec(order_to_q(k, n_g, groups));
     const int32_t nt = s[kSTiles];
     const int32_t ns = nt > 0 ? 1 + inner_boundaries(s[kSCostPrefix], nt, per_part) : 0;
     s[kSNSplits] = ns;
@@ -127,7 +136,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   const int64_t total_splits = block_exclusive_scan<kMetaThreads>(nsplit_local, &split_base, warp_sums);
   int64_t run = split_base;
   for (int k = k0; k < k1; ++k) {
-    int32_t* s = meta_seq(meta, num_parts, order_to_q(k, n_g, groups));
+    int32_t* s = rec(order_to_q(k, n_g, groups));
     s[kSSplitOff] = static_cast<int32_t>(run);
     run += s[kSNSplits];
   }
@@ -153,7 +162,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
     int64_t run_b = b_base;
     for (int k = k0; k < k1; ++k) {
       const int q = order_to_q(k, n_g, groups);
-      const int32_t* sa = meta_seq(meta, num_parts, q);
+      const int32_t* sa = rec(q);
       int32_t* sb = meta_seq(mb, num_parts, q);
       const int32_t nt = sa[kSTiles];
       sb[kSTiles] = nt; sb[kSSplitOff] = static_cast<int32_t>(run_b); sb[kSNSplits] = nt > 0 ? 1 : 0;
@@ -161,6 +170,11 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
       run_b += nt > 0 ? 1 : 0;
     }
     for (int p = threadIdx.x; p < num_parts; p += kMetaThreads) fill_whole_part(mb, num_parts, n_seq, p);
+  }
+  if (rec_smem) {  // schedule A's sequence records out to the metadata
+    __syncthreads();
+    int32_t* out = meta_seq(meta, num_parts, 0);
+    for (int i = threadIdx.x; i < n_seq * kSeqWords; i += kMetaThreads) out[i] = s_rec[i];
   }
 
   if (threadIdx.x == 0) {

@@ -363,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     // read by the combine after this grid: the schedule walked, or -1 when
     // the metadata was rejected (the combine then writes nothing)
+    p.ws_ctrl[1] = (meta_ok && (meta == p.meta || meta[kHTotalSplits] != meta[kHNSeq])) ? 1 : 0;
     p.ws_ctrl[0] = meta_ok ? (meta == p.meta ? 0 : 1) : -1;
     if (!meta_ok && p.err) atomicOr(p.err, MLA_DEVERR_METADATA);
   }

@@ -182,7 +182,7 @@ def test_kernels_record_the_schedule_they_walk(h, parts, walked):
     assert_parity(buf.out.float().cpu().numpy(), ref_o, buf.lse.cpu().numpy(), ref_l, f"h={h} parts={parts}")
 
 
-@pytest.mark.parametrize("batch", [70, 2100])  # the 128- and the 1024-thread schedule kernel
+@pytest.mark.parametrize("batch", [70, 128, 2100])  # the 128- and the 1024-thread schedule kernel
 def test_device_metadata_matches_host_mirror(batch):
     rng = np.random.default_rng(5)
     sl = rng.integers(0, 9000, size=batch).astype(np.int32)
