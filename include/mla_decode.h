@@ -138,10 +138,11 @@ int mla_metadata_size(int batch, int s_q, int num_sm_parts, size_t* bytes);
  * kernel-specific split penalty (4 to 11 tiles) above A's balanced cost:
  * every extra piece costs a Q load and an epilogue, every split row a
  * combine read.  Layout of one schedule (int32):
- *   [0,16)                    header: magic 0x4D4C4131, version (3), n_seq,
+ *   [0,16)                    header: magic 0x4D4C4131, version (4), n_seq,
  *                             num_sm_parts, tile_tokens (128), s_q, batch,
  *                             causal, topk, total_splits, cost_per_part,
- *                             largest sequence cost, 0, groups, 0...
+ *                             largest sequence cost, has_b (1 in A's header
+ *                             when B follows, else 0), groups, 0...
  *   [16, 16 + 8 * parts)      per part: q_begin, t_begin, q_end, t_end,
  *                             split_begin, q_step, 0, 0 (half-open range of
  *                             (sequence, tile) pairs, sequences q_begin,

@@ -119,9 +119,8 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
   int64_t max_group_total = 0;
   for (int j = 0; j < groups; ++j) max_group_total = max(max_group_total, s_group_start[j + 1] - s_group_start[j]);
   __syncthreads();
-  __threadfence_block();
 
-  const int64_t per_part = max_group_total > 0 ? (max_group_total + parts_g - 1) / parts_g : 1;
+  const int64_t per_part = max_group_total > 0 ? floordiv(max_group_total + parts_g - 1, parts_g) : 1;
 
   // 2. split counts per sequence (from the prefixes only).
   int64_t nsplit_local = 0;
@@ -185,13 +184,14 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(const int32_t* s
     meta[kHTotalSplits] = static_cast<int32_t>(total_splits);
     meta[kHPerPart] = static_cast<int32_t>(per_part);
     meta[kHMaxCost] = max_cost;
-    meta[kHReserved] = 0;
+    meta[kHHasB] = has_b ? 1 : 0;
     meta[kHGroups] = groups;
     for (int i = kHGroups + 1; i < kHeaderWords; ++i) meta[i] = 0;
     for (int i = 0; i < kHeaderWords; ++i) mb[i] = has_b ? meta[i] : 0;
     if (has_b) {
       mb[kHTotalSplits] = static_cast<int32_t>(b_splits);
       mb[kHPerPart] = max_cost;
+      mb[kHHasB] = 0;
       mb[kHGroups] = 1;
     }
   }
@@ -335,7 +335,7 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
   }
   int64_t max_group_total = 0;
   for (int j = 0; j < groups; ++j) max_group_total = std::max(max_group_total, group_total[j]);
-  const int64_t per_part = max_group_total > 0 ? (max_group_total + parts_g - 1) / parts_g : 1;
+  const int64_t per_part = max_group_total > 0 ? floordiv(max_group_total + parts_g - 1, parts_g) : 1;
   int64_t splits = 0;
   for (int k = 0; k < n_seq; ++k) {
     int32_t* s = meta_seq(meta, num_sm_parts, order_to_q(k, n_g, groups));
@@ -355,11 +355,11 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
   meta[kHTotalSplits] = static_cast<int32_t>(splits);
   meta[kHPerPart] = static_cast<int32_t>(per_part);
   meta[kHMaxCost] = max_cost;
-  meta[kHReserved] = 0;
-  meta[kHGroups] = groups;
-  for (int i = kHGroups + 1; i < kHeaderWords; ++i) meta[i] = 0;
   // schedule B (one whole sequence per part), when every sequence has a part
   const bool has_b = n_seq <= num_sm_parts;
+  meta[kHHasB] = has_b ? 1 : 0;
+  meta[kHGroups] = groups;
+  for (int i = kHGroups + 1; i < kHeaderWords; ++i) meta[i] = 0;
   int32_t* mb = meta + meta_words(n_seq, num_sm_parts);
   for (int i = 0; i < kHeaderWords; ++i) mb[i] = has_b ? meta[i] : 0;
   if (has_b) {
@@ -376,6 +376,7 @@ extern "C" int mla_get_metadata_host(const int32_t* seqlens, int batch, int s_q,
     for (int p = 0; p < num_sm_parts; ++p) fill_whole_part(mb, num_sm_parts, n_seq, p);
     mb[kHTotalSplits] = static_cast<int32_t>(b_splits);
     mb[kHPerPart] = max_cost;
+    mb[kHHasB] = 0;
     mb[kHGroups] = 1;
   }
   return MLA_OK;

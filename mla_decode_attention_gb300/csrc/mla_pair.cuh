@@ -238,9 +238,10 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
   // The metadata must describe this call; otherwise nothing is read or written.
   const bool meta_ok = meta_header_matches(p.meta, p.batch, p.s_q, p.num_parts, p.topk, p.causal);
   const int32_t* meta = meta_ok ? schedule_for(p.meta, kSplitPenalty) : p.meta;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (blockIdx.x == 0 && threadIdx.x == blockDim.x - 1) {  // a thread with no work at the start
     // read by the combine after this grid: the schedule walked, or -1 when
-    // the metadata was rejected (the combine then writes nothing)
+    // the metadata was rejected (the combine then writes nothing), and
+    // whether that schedule left anything to merge or fill
     p.ws_ctrl[1] = (meta_ok && (meta == p.meta || meta[kHTotalSplits] != meta[kHNSeq])) ? 1 : 0;
     p.ws_ctrl[0] = meta_ok ? (meta == p.meta ? 0 : 1) : -1;
     if (!meta_ok && p.err) atomicOr(p.err, MLA_DEVERR_METADATA);
@@ -262,30 +263,31 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
         constexpr int kIssuers = kSparse ? kKIssuersSparse : 2;
         const int pw = issuer_index(warp);
         const uint64_t pol = l2_policy_evict_first();
-        PartCursor cur = part_cursor(meta, part);
+        PartCursor cur = walked_part_cursor(p.meta, meta, part);
         int q, t0, t1, split;
         uint32_t tc = 0;
         int32_t issued[kKGroups];  // ring round of this issuer's last load per group slot
         for (int i = 0; i < kKGroups; ++i) issued[i] = -1;
         bool ok = true;
         bool first = true, q_issued = false;
+        // The part's first query rows go through the K ring as four boxes,
+        // each with its own barrier; the QK issuer moves each into TMEM as it
+        // lands and releases a ring slot once the boxes in it are moved, so K
+        // group g is requested while later boxes still arrive.
+        auto issue_first_q = [&](int qq) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t bar = smem_u32(&bars->q_box[i]);
+            mbar_arrive_expect_tx(bar, kQBoxBytes + (i == 0 ? kChunk : 0));
+            if (i == 0) tma_load_2d(base + kQRope, &tm_qr, kDv, qq * kRows, bar, pol);
+            tma_load_3d(base + i * kQBoxBytes, &tm_ql, 0, qq * kRows, 2 * i, bar, pol);
+          }
+          q_issued = true;
+        };
         while (next_piece(meta, p.num_parts, &cur, &q, &t0, &t1, &split)) {
           if (first) {
-            // the part's first query rows go through the K ring as four boxes,
-            // each with its own barrier; the QK issuer moves each into TMEM as
-            // it lands and releases a ring slot once the boxes in it are
-            // moved, so K group g is requested while later boxes still arrive
             first = false;
-            if (pw == 0 && lane == 0) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t bar = smem_u32(&bars->q_box[i]);
-                mbar_arrive_expect_tx(bar, kQBoxBytes + (i == 0 ? kChunk : 0));
-                if (i == 0) tma_load_2d(base + kQRope, &tm_qr, kDv, q * kRows, bar, pol);
-                tma_load_3d(base + i * kQBoxBytes, &tm_ql, 0, q * kRows, 2 * i, bar, pol);
-              }
-              q_issued = true;
-            }
+            if (pw == 0 && lane == 0) issue_first_q(q);
           }
           int32_t nid[4];  // sparse: the next tile's indices, requested one tile ahead
           const int32_t keys = meta_seq(meta, p.num_parts, q)[kSKeys];
@@ -360,7 +362,7 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
     } else if (warp == 1) {
       // ---------------------------------------------------- S = Q . K^T
       if (lane == 0) {
-        PartCursor cur = part_cursor(meta, part);
+        PartCursor cur = walked_part_cursor(p.meta, meta, part);
         int q, t0, t1, split;
         uint32_t tc = 0, item = 0, qtma_n = 0, qcp_n = 0;  // completed phases of q_tma, q_cp
         bool ok = true, q_pending = false;  // q_pending: a query box is in flight
@@ -477,7 +479,7 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
       const uint32_t stage = base + kStage;
       const uint32_t prow = stage + (r >> 3) * 1024 + (r & 7) * 128;
       const float sc = p.scale_log2;
-      PartCursor cur = part_cursor(meta, part);
+      PartCursor cur = walked_part_cursor(p.meta, meta, part);
       int q, t0, t1, split;
       uint32_t tc = 0, item = 0;
       bool ok = true;
@@ -664,7 +666,7 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
       if (kSparse && r == 0) bulk_wait_all();  // the last copy has landed in the peer
     } else if (warp == 3 && !kSparse) {
       // ---------------------------------------------------- P transfers (dense)
-      PartCursor cur = part_cursor(meta, part);
+      PartCursor cur = walked_part_cursor(p.meta, meta, part);
       int q, t0, t1, split;
       uint32_t tc = 0;
       bool ok = true;
@@ -704,7 +706,7 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
         constexpr int kIssuers = kSparse ? kVIssuersSparse : 2;
         const int pw = issuer_index(warp);
         const uint64_t pol = l2_policy_evict_first();
-        PartCursor cur = part_cursor(meta, part);
+        PartCursor cur = walked_part_cursor(p.meta, meta, part);
         int q, t0, t1, split;
         uint32_t tc = 0;
         int32_t issued[kVGroups];
@@ -774,7 +776,7 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
     } else if (warp == 1) {
       // ---------------------------------------------------- O += P . V
       if (lane == 0) {
-        PartCursor cur = part_cursor(meta, part);
+        PartCursor cur = walked_part_cursor(p.meta, meta, part);
         int q, t0, t1, split;
         uint32_t tc = 0, item = 0, rc = 0;
         bool ok = true;
@@ -840,7 +842,7 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
       // ---------------------------------------------------- rescale, epilogue
       const int r = threadIdx.x - 128;
       const uint32_t t_o = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16);
-      PartCursor cur = part_cursor(meta, part);
+      PartCursor cur = walked_part_cursor(p.meta, meta, part);
       int q, t0, t1, split;
       uint32_t tc = 0, item = 0, rc = 0;
       bool ok = true;
@@ -971,7 +973,7 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
       }
     } else if (warp == 3 && !kSparse) {
       // ---------------------------------------------------- P buffer hand-back
-      PartCursor cur = part_cursor(meta, part);
+      PartCursor cur = walked_part_cursor(p.meta, meta, part);
       int q, t0, t1, split;
       uint32_t tc = 0;
       bool ok = true;

@@ -34,13 +34,15 @@ namespace mla {
 constexpr int kTileTokens = 128;
 constexpr int kFixedCost = 2;  // a piece switch (Q load, epilogue) costs about two tiles
 constexpr int32_t kMetaMagic = 0x4D4C4131;  // "MLA1"
-constexpr int32_t kMetaVersion = 3;
+constexpr int32_t kMetaVersion = 4;
 
-// header words (kHMaxCost: the largest single-sequence cost; kHReserved: 0;
-// kHGroups: the number of groups of schedule A, 1 or s_q)
+// header words (kHMaxCost: the largest single-sequence cost; kHHasB: 1 in
+// schedule A's header when schedule B follows it, so a decode kernel makes its
+// choice from the header's one cache line; kHGroups: the number of groups of
+// schedule A, 1 or s_q)
 enum : int {
   kHMagic = 0, kHVersion, kHNSeq, kHParts, kHTile, kHSq, kHBatch, kHCausal, kHTopk,
-  kHTotalSplits, kHPerPart, kHMaxCost, kHReserved, kHGroups, kHeaderWords = 16
+  kHTotalSplits, kHPerPart, kHMaxCost, kHHasB, kHGroups, kHeaderWords = 16
 };
 // q_begin, t_begin, q_end, t_end, split_begin, q_step, 0, 0: the part walks
 // sequences q_begin, q_begin + q_step, ... (q_step = the number of groups)
@@ -87,6 +89,8 @@ MLA_HD int32_t tiles_of(int32_t keys) { return (keys + kTileTokens - 1) / kTileT
 MLA_HD int32_t cost_of(int32_t n_tiles) { return n_tiles > 0 ? n_tiles + kFixedCost : 0; }
 
 MLA_HD int64_t floordiv(int64_t a, int64_t b) {  // b > 0
+  if (a >= 0 && a <= 0x7fffffff && b <= 0x7fffffff)  // the usual case: a 32-bit division
+    return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
   return a >= 0 ? a / b : -((-a + b - 1) / b);
 }
 
@@ -177,19 +181,11 @@ MLA_HD int32_t* schedule_b(int32_t* meta) { return meta + meta_words(meta[kHNSeq
 // The schedule a decode kernel with split penalty `penalty` (tile units)
 // walks: B when it exists and costs at most `penalty` more than A.
 MLA_HD bool choose_whole_sequences(const int32_t* meta, int penalty) {
-  return schedule_b(meta)[kHMagic] == kMetaMagic &&
+  return meta[kHHasB] == 1 &&
          static_cast<int64_t>(meta[kHMaxCost]) <= static_cast<int64_t>(meta[kHPerPart]) + penalty;
 }
 MLA_HD const int32_t* schedule_for(const int32_t* meta, int penalty) {
   return choose_whole_sequences(meta, penalty) ? schedule_b(meta) : meta;
-}
-
-// Schedule B's records: part p walks sequence p (none when p >= n_seq).
-MLA_HD void fill_whole_part(int32_t* meta_b, int num_parts, int n_seq, int p) {
-  int32_t* r = meta_part(meta_b, p);
-  const int q = p < n_seq ? p : n_seq;
-  r[0] = q; r[1] = 0; r[2] = p < n_seq ? p + 1 : n_seq; r[3] = 0; r[4] = 0;
-  r[5] = 1; r[6] = 0; r[7] = 0;
 }
 
 // The work a part walks: pieces (q, [t0, t1), split index) in order.
@@ -197,11 +193,33 @@ struct PartCursor {
   int q, t, q_end, t_end, split, step;
 };
 
+// Schedule B's part p walks sequence p (none when p >= n_seq).
+MLA_HD PartCursor whole_part_cursor(int n_seq, int p) {
+  PartCursor c;
+  c.q = p < n_seq ? p : n_seq; c.t = 0; c.q_end = p < n_seq ? p + 1 : n_seq; c.t_end = 0;
+  c.split = 0; c.step = 1;
+  return c;
+}
+
+// Schedule B's records.
+MLA_HD void fill_whole_part(int32_t* meta_b, int num_parts, int n_seq, int p) {
+  int32_t* r = meta_part(meta_b, p);
+  const PartCursor c = whole_part_cursor(n_seq, p);
+  r[0] = c.q; r[1] = c.t; r[2] = c.q_end; r[3] = c.t_end; r[4] = c.split;
+  r[5] = c.step; r[6] = 0; r[7] = 0;
+}
+
 MLA_HD PartCursor part_cursor(const int32_t* meta, int p) {
   const int32_t* r = meta_part(meta, p);
   PartCursor c;
   c.q = r[0]; c.t = r[1]; c.q_end = r[2]; c.t_end = r[3]; c.split = r[4]; c.step = r[5];
   return c;
+}
+
+// The cursor of part p in `walked`, the schedule of metadata `meta_a` that a
+// kernel walks: schedule B's is known from the header without a read.
+MLA_HD PartCursor walked_part_cursor(const int32_t* meta_a, const int32_t* walked, int p) {
+  return walked != meta_a ? whole_part_cursor(meta_a[kHNSeq], p) : part_cursor(walked, p);
 }
 
 // Advances to the next non-empty piece.  Returns false when the part is done.

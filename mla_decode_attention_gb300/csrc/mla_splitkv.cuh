@@ -360,9 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kernel takes ~3-6 us, so the ~26 us that splitting costs is ~4 tiles.
   constexpr int kSplitPenalty = 4;
   const int32_t* meta = meta_ok ? schedule_for(p.meta, kSplitPenalty) : p.meta;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (blockIdx.x == 0 && threadIdx.x == 32 * kSoftmaxWarp0) {  // a softmax thread: nothing to do yet
     // read by the combine after this grid: the schedule walked, or -1 when
-    // the metadata was rejected (the combine then writes nothing)
+    // the metadata was rejected (the combine then writes nothing), and
+    // whether that schedule left anything to merge or fill
     p.ws_ctrl[1] = (meta_ok && (meta == p.meta || meta[kHTotalSplits] != meta[kHNSeq])) ? 1 : 0;
     p.ws_ctrl[0] = meta_ok ? (meta == p.meta ? 0 : 1) : -1;
     if (!meta_ok && p.err) atomicOr(p.err, MLA_DEVERR_METADATA);
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int own0 = share ? hb : 0, own_step = share ? 2 : 1;
       const int n_own = (kChunks - 1) / own_step;
       const int n_req = kMode == KvMode::kPagedFp8V41 ? n_own : n_own + 1;  // + the RoPE chunk
-      PartCursor cur = part_cursor(meta, part);
+      PartCursor cur = walked_part_cursor(p.meta, meta, part);
       int q, t0, t1, split;
       uint32_t tile_ctr = 0, item_ctr = 0;
       bool ok = true;
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Lane L gathers rows 4L..4L+3 of each 128-row tile with one tile::gather4
     // per column chunk; lane 0 owns the barriers.  Invalid slots (-1, out of
     // range, past topk) fetch pool row 0 and are masked by the softmax.
-    PartCursor cur = part_cursor(meta, part);
+    PartCursor cur = walked_part_cursor(p.meta, meta, part);
     int q, t0, t1, split;
     uint32_t tile_ctr = 0, item_ctr = 0;
     int32_t issued[kChunks];  // tile counter of each slot's latest gather, -1 = none
@@ -594,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
-      PartCursor cur = part_cursor(meta, part);
+      PartCursor cur = walked_part_cursor(p.meta, meta, part);
       int q, t0, t1, split;
       uint32_t tile_ctr = 0, item_ctr = 0;
       int32_t issued[kChunks];  // tile counter of each slot's latest load, -1 = none
@@ -658,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ===================================================== MMA issuer
     if (lane == 0) {
-      PartCursor cur = part_cursor(meta, part);
+      PartCursor cur = walked_part_cursor(p.meta, meta, part);
       int q, t0, t1, split;
       uint32_t tile_ctr = 0, item_ctr = 0;
       bool ok = true;
@@ -748,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* red_w = &sm->red_max[g][wq][0];
     float* bc_m = &sm->bcast[g][wq][0];
     float* bc_a = &sm->bcast2[g][wq][0];
-    PartCursor cur = part_cursor(meta, part);
+    PartCursor cur = walked_part_cursor(p.meta, meta, part);
     int q, t0, t1, split;
     uint32_t tile_ctr = 0, item_ctr = 0;
     bool ok = true;

@@ -127,8 +127,9 @@ def test_single_key_rows_are_exact_copies():
         assert np.array_equal(res["out"][b, 0], np.repeat(row[None], 128, axis=0))
 
 
-def test_empty_sequences():
-    w = workloads.Workload("empty", "dense", b=3, s_q=2, h=16, seqlens=(0, 1, 70), seed=16)
+@pytest.mark.parametrize("h", [16, 128])  # the split kernel; the two-SM kernel (schedule B, empty parts)
+def test_empty_sequences(h):
+    w = workloads.Workload("empty", "dense", b=3, s_q=2, h=h, seqlens=(0, 1, 70), seed=16)
     inp = workloads.make_inputs(w)
     res = run_dense(inp)
     ref_o, ref_l = oracle_dense(inp)

@@ -167,7 +167,7 @@ def check_schedule(seqlens, s_q, causal, topk, parts):
     assert groups == (s_q if s_q > 1 and parts % s_q == 0 else 1)
     assert max(per_part_cost) <= hdr[10] + FIXED_COST
     costs = [int(nt) + FIXED_COST if nt > 0 else 0 for nt in seq[:, 0]]
-    assert hdr[11] == max(costs) and hdr[12] == 0
+    assert hdr[11] == max(costs) and hdr[12] == (1 if b * s_q <= parts else 0)
     check_whole_sequence_schedule(m, b * s_q, parts, hdr, seq)
     return m
 
@@ -189,6 +189,7 @@ def check_whole_sequence_schedule(m, n_seq, parts, hdr_a, seq_a):
         assert not hdr.any()
         return
     assert np.array_equal(hdr[:9], hdr_a[:9]) and hdr[10] == hdr[11] == hdr_a[11]
+    assert hdr[12] == 0  # no third schedule follows B
     assert np.array_equal(seq[:, [0, 3, 4]], seq_a[:, [0, 3, 4]])
     assert np.array_equal(seq[:, 2], (seq[:, 0] > 0).astype(np.int32))
     order = walk_order(hdr_a)
@@ -208,7 +209,9 @@ def walks_whole_sequences(m, penalty):
     """The kernels' choice: B when present and at most `penalty` tiles longer."""
     hdr = m[:16]
     words = 16 + 8 * int(hdr[3]) + 8 * int(hdr[2])
-    return m[words] == 0x4D4C4131 and hdr[11] <= hdr[10] + penalty
+    has_b = m[words] == 0x4D4C4131
+    assert hdr[12] == (1 if has_b else 0), "schedule A's header flags whether schedule B follows"
+    return has_b and hdr[11] <= hdr[10] + penalty
 
 
 @pytest.mark.parametrize("parts", [1, 2, 7, 76, 152, 400])
