@@ -228,6 +228,12 @@ __global__ void __maxnreg__(kSparse ? 128 : 224)
   tc_fence_after();
   // Everything above overlaps the previous kernel of the stream (programmatic
   // dependent launch); its results (the schedule, the inputs) are read below.
+  // The query rows of sequence `part` (the rows this part reads first when the
+  // whole-sequence schedule is walked) start towards L2 before the wait: a
+  // prefetch only warms L2, so rows a preceding kernel is still writing are
+  // read for real after the wait all the same.
+  if (rank == 0 && threadIdx.x == 32 * 2 && part < p.batch * p.s_q)
+    prefetch_l2(p.q + static_cast<int64_t>(part) * kRows * kDqk, kRows * kDqk * 2);
   pdl_wait_primary();
   pdl_launch_dependents();  // the combine may launch now; it waits for this grid to finish
   // Schedule B (whole sequences) is walked when it is at most kSplitPenalty
