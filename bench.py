@@ -86,11 +86,13 @@ def load_peaks():
 
 
 def kernel_source_hash():
-    """Hash of the CUDA sources; ncu traffic figures are valid only for it."""
+    """Hash of the sources the decode kernels compile from (mla_decode.cu and
+    every header); ncu traffic figures are valid only for it.  The schedule,
+    combine and no-allocation translation units are not part of it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_decode_attention_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cuh", ".h")) or name == "mla_decode.cu":
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
     with open(os.path.join(ROOT, "include", "mla_decode.h"), "rb") as f:
